@@ -1,0 +1,195 @@
+/*
+ * mg.h -- C ABI of the hybrid local/global grouped-query attention library
+ * (libmg.so, hand-written CUDA for sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] "深度拆解Muse Glimmer，24 GB显存跑30 B Agent，Meta到底做了什么？"
+ *        section 01 "128K 上下文怎么压进 24GB 显存" and section 04
+ *        "一前一后的两个问题".
+ *   [P2] "Tomas Koutsky 解释了 Meta 如何在 24 GB 的容量内容纳 Muse Glimmer",
+ *        sections "窄缓存为长上下文留出空间" and "长上下文仍然带来计算开销".
+ *   [P4] "Meta开源30B模型Muse Glimmer：一张显卡跑本地Agent的实战解析",
+ *        sections "第二招：混合注意力机制节省显存开销" and
+ *        "第三招：D-Flash投机解码实现3倍提速".
+ *
+ * Fixed shape [P1 §01]: 32 query heads, 2 KV heads, head dim 128; query
+ * head h reads KV head h/16.  Layers repeat three local layers (2048-token
+ * sliding window, RoPE) and one global layer (full causal history, no
+ * RoPE): layer l is global iff l % 4 == 3, giving 39 local and 13 global
+ * layers out of 52 [P1 §01; P2 "窄缓存为长上下文留出空间"].
+ *
+ * Conventions shared by every call:
+ *   - All tensors are bf16, row-major, in DEVICE memory owned by the caller.
+ *     The library never allocates or frees memory and keeps no state beyond
+ *     a host-side cache of TMA descriptors.
+ *   - Positions are int32 in DEVICE memory, one per sequence.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream and never synchronise the host.
+ *   - Return value: MG_OK (0) on success; a nonzero mg_status when an
+ *     argument is rejected on the host, in which case nothing is launched;
+ *     MG_ERR_CUDA if a launch failed.
+ *   - `d_err` is a DEVICE uint32 the kernels OR error bits into
+ *     (MG_DERR_*) instead of trapping: a position outside what `max_len`
+ *     or the cache allows is skipped and flagged.  The caller zeroes it and
+ *     reads it back whenever it synchronises.
+ *   - Softmax uses scale `layer->scale` (1/sqrt(128)); products accumulate
+ *     in fp32; outputs are rounded to bf16 (round to nearest even).
+ */
+#ifndef MG_H
+#define MG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MG_HQ 32      /* query heads [P1 §01] */
+#define MG_HKV 2      /* KV heads [P1 §01] */
+#define MG_D 128      /* head dim [P1 §01] */
+#define MG_WINDOW 2048 /* local window = ring slots [P1 §01] */
+#define MG_VERIFY_MAX 16 /* draft block [P1 §04; P4 "第三招"] */
+
+typedef enum { MG_LOCAL = 0, MG_GLOBAL = 1 } mg_kind;
+
+typedef enum {
+  MG_OP_DECODE = 0,
+  MG_OP_VERIFY = 1,
+  MG_OP_PREFILL = 2
+} mg_op;
+
+typedef enum {
+  MG_OK = 0,
+  MG_ERR_INVALID = 1,     /* null pointer, bad kind, negative size, ... */
+  MG_ERR_UNSUPPORTED = 2, /* window != 2048 for local, bad scale/theta, n out of range */
+  MG_ERR_CAPACITY = 3,    /* max_len beyond what the cache can hold */
+  MG_ERR_WORKSPACE = 4,   /* ws_bytes smaller than mg_workspace_bytes() */
+  MG_ERR_CUDA = 5         /* a CUDA launch or driver call failed */
+} mg_status;
+
+/* Bits OR-ed into *d_err by the kernels. */
+#define MG_DERR_POSITION 1u /* a device position was negative or beyond max_len / capacity */
+#define MG_DERR_TIMEOUT 2u  /* a pipeline wait ran out its time limit; the CTA gave up */
+
+/* One attention layer.  kind = MG_LOCAL requires window == 2048 and a
+ * positive rope_theta (10000 is the value used throughout; the pages do not
+ * give theta); kind = MG_GLOBAL requires window == 0 and ignores
+ * rope_theta (global layers carry no RoPE [P2 "长上下文仍然带来计算开销"]). */
+typedef struct {
+  int32_t kind;      /* mg_kind */
+  int32_t window;    /* 2048 (local) or 0 (global) */
+  float rope_theta;  /* local only */
+  float scale;       /* softmax scale, > 0 */
+} mg_layer;
+
+/* One layer's KV cache.  k and v each hold bf16 [batch][2][slots][128]:
+ * a local layer has slots == 2048 and keeps position pos in slot
+ * pos % 2048, reusing the oldest entry [P2 "窄缓存为长上下文留出空间"];
+ * a global layer keeps position pos in slot pos, so slots is its capacity.
+ * K is stored verbatim (un-rotated). */
+typedef struct {
+  void *k;
+  void *v;
+  int32_t batch;
+  int32_t slots;
+} mg_cache;
+
+/* Host-only.  Bytes of one layer's K+V cache: 2 (K,V) x batch x 2 heads x
+ * slots x 128 x 2 bytes, slots = 2048 for MG_LOCAL (capacity is ignored)
+ * and capacity for MG_GLOBAL.  Per token per layer this is 1024 bytes
+ * [P1 §01].  Returns 0 for a bad kind or a negative size. */
+size_t mg_cache_bytes(int32_t kind, int32_t batch, int32_t capacity);
+
+/* Host-only.  Workspace bytes that mg_attn_decode (op MG_OP_DECODE, n = 1),
+ * mg_attn_verify (MG_OP_VERIFY, n = draft tokens) or mg_attn_prefill
+ * (MG_OP_PREFILL, n = chunk tokens) need for this layer, batch and
+ * max_len.  The workspace holds split-KV partials and, for local layers,
+ * RoPE-rotated copies of the queries and of the keys in the window.
+ * Returns 0 if no workspace is needed, (size_t)-1 for bad arguments. */
+size_t mg_workspace_bytes(int32_t op, const mg_layer *layer, int32_t batch,
+                          int32_t n, int32_t max_len);
+
+/* Static description of a status code. */
+const char *mg_status_str(int status);
+
+/* Layer kind of layer index l in the 52-layer stack: MG_GLOBAL iff
+ * l % 4 == 3 (three local layers then one global [P1 §01]).  Returns -1
+ * for l outside [0, 52). */
+int mg_layer_kind(int32_t l);
+
+/*
+ * KV append [P1 §01; P2 "窄缓存为长上下文留出空间"].
+ * Writes K/V of positions pos0[b] .. pos0[b]+n-1 of every sequence b into
+ * the cache, verbatim.  Local: slot = pos % 2048; when n > 2048 only the last
+ * 2048 tokens are written (the earlier ones would be overwritten by the ring
+ * anyway), so the result equals appending one token at a time.  Global:
+ * slot = pos; a position >= slots is skipped and flags MG_DERR_POSITION.
+ *   k_new, v_new : bf16 [batch][n][2][128] (device)
+ *   d_pos0       : int32 [batch] (device)
+ *   n            : 0 <= n; n == 0 is a no-op
+ */
+int mg_kv_append(const mg_layer *layer, const mg_cache *cache,
+                 const int32_t *d_pos0, int32_t n, const void *k_new,
+                 const void *v_new, uint32_t *d_err, void *stream);
+
+/*
+ * Decode attention for one query token per sequence [P1 §04: decode is
+ * autoregressive, one token at a time].  The query of sequence b sits at
+ * position p = pos[b]; its own K/V must already be in the cache
+ * (mg_kv_append first).  Key set: [max(0, p-2047), p] for a local layer,
+ * with RoPE applied to q at p and to each key at its own position;
+ * [0, p] for a global layer, no RoPE.  Split-KV: the key set is cut into
+ * splits handled by separate CTAs, merged by a log-sum-exp combine.
+ *   q, o     : bf16 [batch][32][128] (device)
+ *   max_len  : 1 + the largest pos[b] the caller may pass (sizes the grid
+ *              and the workspace); pos[b] >= max_len is skipped + flagged
+ *   ws       : device workspace of at least
+ *              mg_workspace_bytes(MG_OP_DECODE, layer, batch, 1, max_len)
+ */
+int mg_attn_decode(const mg_layer *layer, const mg_cache *cache,
+                   const int32_t *d_pos, int32_t max_len, const void *q,
+                   void *o, void *ws, size_t ws_bytes, uint32_t *d_err,
+                   void *stream);
+
+/*
+ * Parallel verify of a speculative draft block [P1 §04; P4 "第三招"]:
+ * n (1..16) consecutive query tokens at positions p0[b] .. p0[b]+n-1 in
+ * one pass.  Query i sees the cached keys before p0 inside its window plus
+ * the block's own keys 0..i (causal inside the block).  The block's K/V come
+ * in k_new/v_new; the cache is read-only here and must hold positions
+ * < p0[b].  Appending the accepted prefix afterwards is the caller's call
+ * (mg_kv_append), which keeps a local ring exact when drafts are rejected.
+ *   q, o         : bf16 [batch][n][32][128] (device)
+ *   k_new, v_new : bf16 [batch][n][2][128] (device)
+ *   max_len      : >= 1 + max(p0[b]) + n - 1 (key positions incl. the block)
+ *   ws           : >= mg_workspace_bytes(MG_OP_VERIFY, layer, batch, n, max_len)
+ */
+int mg_attn_verify(const mg_layer *layer, const mg_cache *cache,
+                   const int32_t *d_pos0, int32_t n, int32_t max_len,
+                   const void *q, const void *k_new, const void *v_new,
+                   void *o, void *ws, size_t ws_bytes, uint32_t *d_err,
+                   void *stream);
+
+/*
+ * Causal chunked prefill [P2 "长上下文仍然带来计算开销": full attention,
+ * quadratic in global layers; P4 "第二招"].  Chunk of n tokens at positions
+ * c0[b] .. c0[b]+n-1; key set of each query as in decode, taken from the
+ * cache (positions < c0[b]) and from the chunk's own k_new/v_new.  The cache
+ * is read-only; append the chunk afterwards with mg_kv_append.
+ *   q, o         : bf16 [batch][n][32][128] (device)
+ *   k_new, v_new : bf16 [batch][n][2][128] (device)
+ *   max_len      : >= max(c0[b]) + n
+ *   ws           : >= mg_workspace_bytes(MG_OP_PREFILL, layer, batch, n, max_len)
+ */
+int mg_attn_prefill(const mg_layer *layer, const mg_cache *cache,
+                    const int32_t *d_pos0, int32_t n, int32_t max_len,
+                    const void *q, const void *k_new, const void *v_new,
+                    void *o, void *ws, size_t ws_bytes, uint32_t *d_err,
+                    void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MG_H */

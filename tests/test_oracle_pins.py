@@ -1,0 +1,290 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test would fail under a plausible mistake in the oracle: a window off
+by one, a wrong RoPE sign or pairing, a wrong KV-group map, a ring slot
+formula error, a missing normalisation.  No GPU needed.
+
+Sources: [P1] "深度拆解Muse Glimmer，24 GB显存跑30 B Agent，Meta到底做了什么？"
+§01; [P2] "Tomas Koutsky 解释了 Meta 如何在 24 GB 的容量内容纳 Muse Glimmer",
+"窄缓存为长上下文留出空间" / "长上下文仍然带来计算开销"; [P4]
+"Meta开源30B模型Muse Glimmer：一张显卡跑本地Agent的实战解析", "第二招".
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from hybrid_local_global_attn_b300 import synth
+
+THETA = 10000.0
+SCALE = 1.0 / math.sqrt(128.0)
+
+
+def f64(x):
+    return x.to(torch.float64).numpy()
+
+
+def brute_force(kind, W, rope, k, v, qpos, q):
+    """Explicit-matrix attention: dense score matrix, -inf mask, exp,
+    normalise.  RoPE in complex form z = x[:64] + i x[64:], z *= e^{i t w}.
+    Independent of the C oracle (different formulation, numpy)."""
+    kd, vd, qd = f64(k), f64(v), f64(q)  # [T][2][128], [T][2][128], [nq][32][128]
+    T = kd.shape[0]
+    qpos = np.asarray(qpos)
+    w = THETA ** (-2.0 * np.arange(64) / 128.0)
+
+    def rot(x, t):
+        z = (x[..., :64] + 1j * x[..., 64:]) * np.exp(1j * t[:, None, None] * w)
+        return np.concatenate([z.real, z.imag], axis=-1)
+
+    if rope:
+        kd = rot(kd, np.arange(T, dtype=np.float64))
+        qd = rot(qd, qpos.astype(np.float64))
+    jj = np.arange(T)[None, :]
+    pp = qpos[:, None]
+    allowed = jj <= pp
+    if kind == orc.LOCAL:
+        allowed &= jj >= pp - W + 1
+    mask = np.where(allowed, 0.0, -np.inf)  # [nq][T]
+    out = np.zeros(qd.shape)
+    for h in range(32):
+        g = h // 16
+        S = (qd[:, h, :] @ kd[:, g, :].T) * SCALE + mask
+        S = S - S.max(axis=1, keepdims=True)
+        P = np.exp(S)
+        P /= P.sum(axis=1, keepdims=True)
+        out[:, h, :] = P @ vd[:, g, :]
+    return out
+
+
+def rand_hist(T, seed):
+    k = synth.randn_bf16((T, 2, 128), seed * 10 + 1)
+    v = synth.randn_bf16((T, 2, 128), seed * 10 + 2)
+    return k, v
+
+
+@pytest.mark.parametrize("kind,W,rope", [(orc.LOCAL, 1, 1), (orc.LOCAL, 4, 1), (orc.LOCAL, 64, 1),
+                                         (orc.LOCAL, 4, 0), (orc.GLOBAL, 0, 0), (orc.GLOBAL, 0, 1)])
+def test_brute_force_tiny(kind, W, rope):
+    T = 48
+    k, v = rand_hist(T, 3)
+    qpos = np.array([0, 1, 2, 3, 5, 17, 31, 46, 47], dtype=np.int32)
+    q = synth.randn_bf16((len(qpos), 32, 128), 77)
+    lay = orc.layer(kind, window=max(W, 1), rope=rope)
+    got = orc.attention(lay, k, v, qpos, q)
+    ref = brute_force(kind, W, rope, k, v, qpos, q)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_window_covering_history_is_rope_full_causal():
+    # W >= T: a local layer equals full causal attention with RoPE [P1 §01]
+    T = 200
+    k, v = rand_hist(T, 5)
+    qpos = np.arange(0, T, 7, dtype=np.int32)
+    q = synth.randn_bf16((len(qpos), 32, 128), 8)
+    a = orc.attention(orc.layer(orc.LOCAL, window=2048, rope=1), k, v, qpos, q)
+    b = orc.attention(orc.layer(orc.GLOBAL, rope=1), k, v, qpos, q)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+    # and it differs once the window is shorter than the history
+    c = orc.attention(orc.layer(orc.LOCAL, window=64, rope=1), k, v, qpos, q)
+    assert np.abs(c[-1] - a[-1]).max() > 1e-3
+
+
+def test_rope_off_local_equals_global():
+    # With RoPE switched off and W >= T, local and global compute the same set
+    T = 150
+    k, v = rand_hist(T, 6)
+    qpos = np.arange(T, dtype=np.int32)
+    q = synth.randn_bf16((T, 32, 128), 9)
+    a = orc.attention(orc.layer(orc.LOCAL, window=2048, rope=0), k, v, qpos, q)
+    b = orc.attention(orc.layer(orc.GLOBAL, rope=0), k, v, qpos, q)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("kind", [orc.LOCAL, orc.GLOBAL])
+def test_ring_cache_equals_linear_history(kind):
+    # A 2048-slot ring that reuses the oldest slot [P2 窄缓存为长上下文留出空间]
+    # plus the window mask gives the same outputs as the linear history.
+    T = 2300
+    k, v = rand_hist(T, 11)
+    slots = 2048 if kind == orc.LOCAL else T
+    kc = np.zeros((2, slots, 128), np.uint16)
+    vc = np.zeros((2, slots, 128), np.uint16)
+    lay = orc.layer(kind)
+    # append in uneven pieces and decode the last appended position each
+    # time: 999, 2046, 2047 (ring full), 2048 (first reuse), 2199, 2299
+    cuts = [0, 1000, 2047, 2048, 2049, 2200, 2300]
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        orc.cache_append(kind, kc, vc, a, k[a:b], v[a:b])
+        p = b - 1
+        q = synth.randn_bf16((32, 128), 1000 + p)
+        got = orc.decode_from_cache(lay, kc, vc, p, q)
+        ref = orc.attention(lay, k[:p + 1], v[:p + 1], [p], q.unsqueeze(0))[0]
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_cache_append_slots_bitwise():
+    # local slot = pos mod 2048, global slot = pos; later positions overwrite
+    T = 4200
+    k, v = rand_hist(T, 12)
+    kb = orc.bits(k)
+    kc = np.zeros((2, 2048, 128), np.uint16)
+    vc = np.zeros((2, 2048, 128), np.uint16)
+    orc.cache_append(orc.LOCAL, kc, vc, 0, k[:3000], v[:3000])
+    orc.cache_append(orc.LOCAL, kc, vc, 3000, k[3000:], v[3000:])
+    for s in [0, 1, 103, 2047]:
+        last = max(j for j in range(T) if j % 2048 == s)
+        assert np.array_equal(kc[:, s, :], kb[last])
+    gc = np.zeros((2, T, 128), np.uint16)
+    gv = np.zeros((2, T, 128), np.uint16)
+    orc.cache_append(orc.GLOBAL, gc, gv, 0, k, v)
+    assert np.array_equal(gc.transpose(1, 0, 2), kb)
+    with pytest.raises(ValueError):
+        orc.cache_append(orc.GLOBAL, gc, gv, T, k[:1], v[:1])
+
+
+@pytest.mark.parametrize("kind,p", [(orc.LOCAL, 0), (orc.LOCAL, 100), (orc.LOCAL, 2046),
+                                    (orc.LOCAL, 2047), (orc.LOCAL, 3000), (orc.GLOBAL, 3000)])
+def test_zero_keys_give_window_mean(kind, p):
+    # zero keys give equal scores whatever the rotation, so o is the mean of
+    # V over exactly the key set: 2048 keys including the query itself for a
+    # local layer [P1 §01], all p+1 keys for a global one.
+    T = p + 1
+    _, v = rand_hist(T, 13)
+    k = torch.zeros((T, 2, 128), dtype=torch.bfloat16)
+    q = synth.randn_bf16((1, 32, 128), 14)
+    o = orc.attention(orc.layer(kind), k, v, [p], q)[0]
+    lo = max(0, p - 2047) if kind == orc.LOCAL else 0
+    vd = f64(v)
+    for h in (0, 15, 16, 31):
+        np.testing.assert_allclose(o[h], vd[lo:p + 1, h // 16].mean(axis=0), rtol=0, atol=1e-12)
+
+
+def test_probability_rows_sum_to_one_and_respect_window():
+    T = 3000
+    k, _ = rand_hist(T, 15)
+    q = synth.randn_bf16((128,), 16)
+    for kind, p in [(orc.LOCAL, 2999), (orc.LOCAL, 10), (orc.GLOBAL, 2999)]:
+        pr = orc.probs(orc.layer(kind), k, p, q, head=20)
+        assert abs(pr.sum() - 1.0) < 1e-12
+        lo = max(0, p - 2047) if kind == orc.LOCAL else 0
+        assert (pr[:lo] == 0).all() and (pr[p + 1:] == 0).all()
+        assert (pr[lo:p + 1] > 0).all()
+
+
+def test_single_key_returns_its_value():
+    k, v = rand_hist(1, 17)
+    q = synth.randn_bf16((1, 32, 128), 18)
+    for kind in (orc.LOCAL, orc.GLOBAL):
+        o = orc.attention(orc.layer(kind), k, v, [0], q)[0]
+        for h in range(32):
+            np.testing.assert_allclose(o[h], f64(v)[0, h // 16], rtol=0, atol=0)
+
+
+def test_two_keys_closed_form_with_rope():
+    # q = a e0 at position 1; k0 = k1 = e0 at positions 0 and 1.
+    # R(1) rotates (e0, e64) by angle w0 = 1 rad, so
+    #   s0 = a cos(1) / sqrt(128),  s1 = a / sqrt(128),
+    #   o  = sigmoid(s1 - s0) v1 + sigmoid(s0 - s1) v0.
+    a = 8.0
+    k = torch.zeros((2, 2, 128), dtype=torch.bfloat16)
+    k[:, :, 0] = 1.0
+    _, v = rand_hist(2, 19)
+    q = torch.zeros((1, 32, 128), dtype=torch.bfloat16)
+    q[0, :, 0] = a
+    o = orc.attention(orc.layer(orc.LOCAL), k, v, [1], q)[0]
+    s0 = a * math.cos(1.0) * SCALE
+    s1 = a * SCALE
+    w1 = 1.0 / (1.0 + math.exp(-(s1 - s0)))
+    vd = f64(v)
+    for h in (0, 31):
+        g = h // 16
+        np.testing.assert_allclose(o[h], w1 * vd[1, g] + (1 - w1) * vd[0, g], rtol=0, atol=1e-13)
+
+
+def test_one_hot_large_score_selects_value():
+    T = 500
+    _, v = rand_hist(T, 20)
+    k = torch.zeros((T, 2, 128), dtype=torch.bfloat16)
+    k[321, :, 5] = 64.0
+    q = torch.zeros((1, 32, 128), dtype=torch.bfloat16)
+    q[0, :, 5] = 64.0
+    o = orc.attention(orc.layer(orc.GLOBAL), k, v, [499], q)[0]
+    for h in (0, 17):
+        np.testing.assert_allclose(o[h], f64(v)[321, h // 16], rtol=0, atol=1e-12)
+
+
+def test_rope_identity_norm_composition_and_frequencies():
+    x = np.random.default_rng(0).standard_normal(128)
+    np.testing.assert_array_equal(orc.rope(x, 0.0), x)
+    for t in (1.0, 37.0, 131071.0):
+        np.testing.assert_allclose(np.linalg.norm(orc.rope(x, t)), np.linalg.norm(x), rtol=1e-14)
+    np.testing.assert_allclose(orc.rope(orc.rope(x, 300.0), 45.0), orc.rope(x, 345.0), atol=1e-12)
+    # rotate-half pairing: e_i goes to cos e_i + sin e_{i+64}, w_i = theta^(-2i/128)
+    for i in (0, 1, 33, 63):
+        e = np.zeros(128); e[i] = 1.0
+        t = 5.0
+        wi = THETA ** (-2.0 * i / 128.0)
+        r = orc.rope(e, t)
+        exp = np.zeros(128); exp[i] = math.cos(t * wi); exp[i + 64] = math.sin(t * wi)
+        np.testing.assert_allclose(r, exp, atol=1e-15)
+
+
+def test_local_outputs_invariant_to_position_shift():
+    # RoPE makes scores depend on j - p only: shifting the whole local history
+    # by D positions (padding in front, outside every window) leaves outputs equal.
+    W, T, D = 64, 160, 1000
+    k, v = rand_hist(T, 21)
+    kp, vp = rand_hist(D, 22)
+    qpos = np.arange(W, T, 9, dtype=np.int32)
+    q = synth.randn_bf16((len(qpos), 32, 128), 23)
+    lay = orc.layer(orc.LOCAL, window=W)
+    a = orc.attention(lay, k, v, qpos, q)
+    b = orc.attention(lay, torch.cat([kp, k]), torch.cat([vp, v]), qpos + D, q)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_query_head_reads_kv_group_h_div_16():
+    # swapping the two KV heads and the two halves of the query heads swaps
+    # the output halves: head h reads KV head h // 16 (not h % 2).
+    T = 90
+    k, v = rand_hist(T, 24)
+    q = synth.randn_bf16((3, 32, 128), 25)
+    pos = [10, 50, 89]
+    for kind in (orc.LOCAL, orc.GLOBAL):
+        lay = orc.layer(kind)
+        a = orc.attention(lay, k, v, pos, q)
+        b = orc.attention(lay, k.flip(1), v.flip(1), pos, torch.cat([q[:, 16:], q[:, :16]], 1))
+        np.testing.assert_allclose(a[:, :16], b[:, 16:], atol=1e-13)
+        np.testing.assert_allclose(a[:, 16:], b[:, :16], atol=1e-13)
+        # identical queries within a group give identical outputs
+        qq = q.clone(); qq[:, 1:16] = qq[:, :1]
+        c = orc.attention(lay, k, v, pos, qq)
+        assert np.array_equal(c[:, 0], c[:, 7])
+
+
+def test_block_verify_equals_sequential_decodes():
+    # a 16-token block attended in one pass with a causal mask inside the
+    # block [P1 §04] equals 16 single-token decodes from a growing ring cache
+    T0, n = 2040, 16
+    k, v = rand_hist(T0 + n, 26)
+    q = synth.randn_bf16((n, 32, 128), 27)
+    for kind in (orc.LOCAL, orc.GLOBAL):
+        lay = orc.layer(kind)
+        block = orc.attention(lay, k, v, np.arange(T0, T0 + n, dtype=np.int32), q)
+        slots = 2048 if kind == orc.LOCAL else T0 + n
+        kc = np.zeros((2, slots, 128), np.uint16); vc = np.zeros_like(kc)
+        orc.cache_append(kind, kc, vc, 0, k[:T0], v[:T0])
+        for i in range(n):
+            orc.cache_append(kind, kc, vc, T0 + i, k[T0 + i:T0 + i + 1], v[T0 + i:T0 + i + 1])
+            d = orc.decode_from_cache(lay, kc, vc, T0 + i, q[i])
+            np.testing.assert_allclose(block[i], d, rtol=0, atol=1e-12)
+
+
+def test_full_attention_pair_count_matches_pages(golden_bytes):
+    # about 1.7e10 attention computations per full layer at 131K [P4 第二招]: n^2
+    val, tol, _ = golden_bytes["full_attention_pairs_131k"]
+    n = 131072
+    assert abs(n * n - val) <= tol * val
