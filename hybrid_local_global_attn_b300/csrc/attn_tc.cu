@@ -1,0 +1,432 @@
+// attn_tc.cu -- tensor-core (tcgen05 / TMEM) attention for a block of query
+// tokens: speculative verify and causal chunked prefill.
+//
+// What it computes: the query at position q sees the cached keys before the
+// block start c0 that fall in its key set, plus the block's own keys up to q
+// (causal inside the block) -- the parallel verify pass of a 16-token draft
+// ("深度拆解Muse Glimmer，24 GB显存跑30 B Agent，Meta到底做了什么？", section 04;
+// "Meta开源30B模型Muse Glimmer：一张显卡跑本地Agent的实战解析", section
+// "第三招") and chunked prompt processing, full attention that stays quadratic
+// in global layers ("Tomas Koutsky 解释了 Meta 如何在 24 GB 的容量内容纳 Muse
+// Glimmer", section "长上下文仍然带来计算开销").  Key sets: [q-2047, q] with
+// RoPE (local; operands pre-rotated by rope_stage) or [0, q] without RoPE
+// (global, operands read straight from the cache and the block).
+//
+// Tiling: a CTA owns 16 consecutive query positions of one KV group.  Their
+// 16 positions x 16 query heads form two M = 128 tiles (8 positions x 16
+// heads each, rows r = 16 * position + head), so every K/V tile loaded into
+// shared memory feeds 256 query rows.  Key tiles hold 128 keys and are aligned
+// to c0, so a tile never straddles the cache and the block.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax of tile A (thread = one row = one TMEM lane)
+//   warps 4-7  softmax of tile B
+//   warp 8     TMA producer (Q once; K and V in a 2-deep ring)
+//   warp 9     TMEM owner and single-thread MMA issuer
+// TMEM (512 columns): S_A, S_B (fp32 128 cols each; P overwrites the first
+// 64 columns as packed bf16), O_A, O_B (fp32 128 cols each).
+// Per key tile: S = Q K^T (M128 N128 K16 x 8), softmax in registers with a
+// lazily rescaled running max (rescale only when the max grows by more than
+// 2^8), P back to TMEM, O += P V (A from TMEM, V as an MN-major operand).
+// Splits (verify): the cache part is cut across CTAs; each writes (o/l, lse)
+// and the combine kernel merges them.
+#include "mg_internal.h"
+#include "mg_ptx.cuh"
+
+namespace mg {
+
+namespace {
+
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct TileInfo {
+  int32_t c0, qa, qz;     // block start, first and last valid query position
+  int32_t ncache, nnew;   // tiles from the cache part / the block part
+  int32_t u_begin, v_lo;  // first cache tile index (from c0 down), first block tile
+};
+
+__device__ __forceinline__ int32_t tile_kp0(const TileInfo &ti, int t) {
+  if (t < ti.ncache) return ti.c0 - kTcKeys * (ti.u_begin + t + 1);
+  return ti.c0 + kTcKeys * (ti.v_lo + (t - ti.ncache));
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tq,
+                   const __grid_constant__ CUtensorMap tka, const __grid_constant__ CUtensorMap tva,
+                   const __grid_constant__ CUtensorMap tkb,
+                   const __grid_constant__ CUtensorMap tvb) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_flag;
+  __shared__ uint32_t tmem_base_slot;
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase;                        // 2 x 32 KB
+  const uint32_t sKV = sbase + 2 * kTcQBytes;       // stage s: K at +64K*s, V at +64K*s+32K
+  const uint32_t sBar = sKV + kTcStages * 2 * kTcTileBytes;
+  // barrier addresses
+  const uint32_t bar_q = sBar;
+  const uint32_t bar_kf = sBar + 8;                        // [2]
+  const uint32_t bar_vf = bar_kf + 8 * kTcStages;          // [2]
+  const uint32_t bar_ke = bar_vf + 8 * kTcStages;          // [2] stage empty
+  const uint32_t bar_s = bar_ke + 8 * kTcStages;           // [2] S ready (A, B)
+  const uint32_t bar_p = bar_s + 16;                       // [2] P ready
+  const uint32_t bar_o = bar_p + 16;                       // [2] O final
+  const uint32_t bar_done = bar_o + 16;                    // all MMAs retired
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x % p.splits;
+  const int qb = p.qblocks - 1 - static_cast<int>(blockIdx.x / p.splits);  // heavy blocks first
+  const bool local = (p.kind == 0);
+
+  // ------------------------------------------------------ tile schedule ----
+  TileInfo ti;
+  ti.c0 = p.pos0[b];
+  const bool bad = ti.c0 < 0 || static_cast<int64_t>(ti.c0) + p.n > p.max_len ||
+                   (!p.staged && ti.c0 > p.slots);
+  ti.qa = ti.c0 + kTcPosPerCta * qb;
+  ti.qz = min(ti.qa + kTcPosPerCta - 1, ti.c0 + p.n - 1);
+  ti.ncache = ti.nnew = ti.u_begin = ti.v_lo = 0;
+  if (!bad) {
+    const int32_t lo = local ? max(0, ti.qa - p.window + 1) : 0;
+    const int32_t U = ti.c0 > lo ? (ti.c0 - lo + kTcKeys - 1) / kTcKeys : 0;
+    ti.u_begin = static_cast<int32_t>(static_cast<int64_t>(split) * U / p.splits);
+    const int32_t u_end = static_cast<int32_t>(static_cast<int64_t>(split + 1) * U / p.splits);
+    ti.ncache = u_end - ti.u_begin;
+    if (split == p.splits - 1) {
+      ti.v_lo = local ? max(0, ti.qa - p.window + 1 - ti.c0) / kTcKeys : 0;
+      const int32_t v_hi = (ti.qz - ti.c0) / kTcKeys;
+      ti.nnew = v_hi - ti.v_lo + 1;
+    }
+  }
+  const int ntiles = ti.ncache + ti.nnew;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    if (bad && split == 0 && qb == 0) set_err(p.err, MG_DERR_POSITION);
+    mbar_init(bar_q, 1);
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(bar_kf + 8 * i, 1);
+      mbar_init(bar_vf + 8 * i, 1);
+      mbar_init(bar_ke + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_s + 8 * i, 1);
+      mbar_init(bar_p + 8 * i, 128);
+      mbar_init(bar_o + 8 * i, 1);
+    }
+    mbar_init(bar_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&tmem_base_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------- producer ----
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tka);
+      tma_prefetch_desc(&tva);
+      tma_prefetch_desc(&tkb);
+      tma_prefetch_desc(&tvb);
+      const int32_t q_t0 = kTcPosPerCta * qb;  // position index within the block
+      mbar_arrive_expect_tx(bar_q, 2 * kTcQBytes);
+      for (int m = 0; m < 2; ++m) {
+        for (int x = 0; x < 2; ++x) {
+          tma_load_4d(sQ + m * kTcQBytes + x * (kTcQBytes / 2), &tq, bar_q, 64 * x, kGroup * g,
+                      q_t0 + kTcPosPerTile * m, b);
+        }
+      }
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t % kTcStages;
+        if (t >= kTcStages &&
+            !mbar_wait(bar_ke + 8 * st, ((t / kTcStages) - 1) & 1, &abort_flag)) {
+          abort_flag = 1;
+          set_err(p.err, MG_DERR_TIMEOUT);
+          break;
+        }
+        const int32_t kp0 = tile_kp0(ti, t);
+        const uint32_t dk = sKV + st * 2 * kTcTileBytes;
+        const uint32_t dv = dk + kTcTileBytes;
+        const bool from_cache = t < ti.ncache;
+        mbar_arrive_expect_tx(bar_kf + 8 * st, kTcTileBytes);
+        mbar_arrive_expect_tx(bar_vf + 8 * st, kTcTileBytes);
+        if (p.staged) {
+          const int32_t row = kp0 - ti.c0 + kWindow;
+          for (int x = 0; x < 2; ++x)
+            tma_load_3d(dk + x * (kTcTileBytes / 2), &tka, bar_kf + 8 * st, 64 * x, row,
+                        b * kHkv + g);
+          for (int x = 0; x < 2; ++x)
+            tma_load_3d(dv + x * (kTcTileBytes / 2), &tva, bar_vf + 8 * st, 64 * x, row,
+                        b * kHkv + g);
+        } else if (from_cache) {
+          for (int x = 0; x < 2; ++x)
+            tma_load_3d(dk + x * (kTcTileBytes / 2), &tka, bar_kf + 8 * st, 64 * x, kp0,
+                        b * kHkv + g);
+          for (int x = 0; x < 2; ++x)
+            tma_load_3d(dv + x * (kTcTileBytes / 2), &tva, bar_vf + 8 * st, 64 * x, kp0,
+                        b * kHkv + g);
+        } else {
+          const int32_t row = kp0 - ti.c0;
+          for (int x = 0; x < 2; ++x)
+            tma_load_4d(dk + x * (kTcTileBytes / 2), &tkb, bar_kf + 8 * st, 64 * x, g, row, b);
+          for (int x = 0; x < 2; ++x)
+            tma_load_4d(dv + x * (kTcTileBytes / 2), &tvb, bar_vf + 8 * st, 64 * x, g, row, b);
+        }
+        ++issued;
+      }
+      // no copies may be in flight when the CTA retires
+      (void)mbar_wait(bar_q, 0, nullptr);
+      for (int t = max(0, issued - kTcStages); t < issued; ++t) {
+        (void)mbar_wait(bar_kf + 8 * (t % kTcStages), (t / kTcStages) & 1, nullptr);
+        (void)mbar_wait(bar_vf + 8 * (t % kTcStages), (t / kTcStages) & 1, nullptr);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------ MMA issuer ----
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t tS[2] = {tbase, tbase + 128};
+      const uint32_t tO[2] = {tbase + 256, tbase + 384};
+      bool ok = mbar_wait(bar_q, 0, &abort_flag);
+      tc_fence_after();
+      auto qk = [&](int m, int st) {
+        const uint32_t qs = sQ + m * kTcQBytes;
+        const uint32_t ks = sKV + st * 2 * kTcTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32;
+          mma_ss(tS[m], smem_desc_sw128(qs + off, 16, 1024), smem_desc_sw128(ks + off, 16, 1024),
+                 kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto pv = [&](int m, int st, bool first) {
+        const uint32_t vs = sKV + st * 2 * kTcTileBytes + kTcTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_ts(tO[m], tS[m] + 8 * kk, smem_desc_sw128(vs + kk * 2048, kTcTileBytes / 2, 1024),
+                 kIdescPV, (first && kk == 0) ? 0u : 1u);
+        }
+      };
+      for (int t = 0; ok && t <= ntiles; ++t) {
+        const int st = t % kTcStages;
+        const int pst = (t + kTcStages - 1) % kTcStages;  // stage of tile t-1
+        if (t < ntiles) {
+          ok = mbar_wait(bar_kf + 8 * st, (t / kTcStages) & 1, &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        if (t > 0) {
+          ok = mbar_wait(bar_p, (t - 1) & 1, &abort_flag) &&
+               mbar_wait(bar_vf + 8 * pst, ((t - 1) / kTcStages) & 1, &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          pv(0, pst, t == 1);
+          if (t == ntiles) mma_commit(bar_o);
+        }
+        if (t < ntiles) {
+          qk(0, st);
+          mma_commit(bar_s);
+        }
+        if (t > 0) {
+          ok = mbar_wait(bar_p + 8, (t - 1) & 1, &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          pv(1, pst, t == 1);
+          mma_commit(bar_ke + 8 * pst);
+          if (t == ntiles) mma_commit(bar_o + 8);
+        }
+        if (t < ntiles) {
+          qk(1, st);
+          mma_commit(bar_s + 8);
+        }
+      }
+      if (!ok) {
+        abort_flag = 1;
+        set_err(p.err, MG_DERR_TIMEOUT);
+      }
+      // every MMA issued must retire before TMEM is released
+      mma_commit(bar_done);
+      (void)mbar_wait(bar_done, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------- softmax warps ----
+    const int m = warp >> 2;                     // query tile 0 (A) or 1 (B)
+    const int r = (warp & 3) * 32 + lane;        // row = TMEM lane
+    const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + lane_bits + m * 128;
+    const uint32_t tO = tbase + lane_bits + 256 + m * 128;
+    const int32_t tloc = kTcPosPerCta * qb + kTcPosPerTile * m + (r >> 4);  // index in block
+    const int32_t qp = ti.qa + kTcPosPerTile * m + (r >> 4);  // this row's position
+    const int h = kGroup * g + (r & 15);
+    const bool row_valid = tloc < p.n;  // rows past the block are padding
+    const float sl2 = p.scale_log2;
+    const int32_t wlo = local ? qp - p.window + 1 : INT32_MIN;  // lowest key in the window
+    float mrow = -INFINITY, lrow = 0.f;
+    bool ok = true;
+
+    for (int t = 0; t < ntiles; ++t) {
+      // tcgen05.ld/st below are warp-collective: the whole warp goes on or stops
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s + 8 * m, t & 1, &abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int32_t kp0 = tile_kp0(ti, t);
+      const bool need_mask = (kp0 < 0) || (kp0 + kTcKeys - 1 > ti.qa) ||
+                             (local && kp0 < ti.qz - p.window + 1);
+      // pass 1: row max of the raw scores
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + 32 * c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int32_t kp = kp0 + 32 * c + j;
+          const bool keep = !need_mask || (kp >= 0 && kp <= qp && kp >= wlo);
+          if (keep) mx = fmaxf(mx, __uint_as_float(v[j]));
+        }
+      }
+      const float mt = mx * sl2;  // scale > 0, so it commutes with max
+      float alpha = 1.f;
+      if (mt > mrow + kRescaleThreshold || (mrow == -INFINITY && mt != -INFINITY)) {
+        if (mrow != -INFINITY) alpha = fast_exp2(mrow - mt);
+        mrow = mt;
+      }
+      lrow *= alpha;
+      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + 32 * c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+          tmem_st32(tO + 32 * c, v);
+        }
+        tmem_wait_st();
+      }
+      const float muse = (mrow == -INFINITY) ? 0.f : mrow;
+      // pass 2: P = 2^(s*scale*log2e - m), packed to bf16 over S's first half
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + 32 * c, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int32_t kp = kp0 + 32 * c + j;
+          float e0 = fast_exp2(fmaf(__uint_as_float(v[j]), sl2, -muse));
+          float e1 = fast_exp2(fmaf(__uint_as_float(v[j + 1]), sl2, -muse));
+          if (need_mask) {
+            if (!(kp >= 0 && kp <= qp && kp >= wlo)) e0 = 0.f;
+            if (!(kp + 1 >= 0 && kp + 1 <= qp && kp + 1 >= wlo)) e1 = 0.f;
+          }
+          lrow += e0 + e1;
+          pk[j >> 1] = pack_bf16x2(e0, e1);
+        }
+        tmem_st16(tS + 16 * c, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_p + 8 * m);
+    }
+
+    // ----------------------------------------------------------- epilogue ----
+    if (ok && ntiles > 0) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_o + 8 * m, 0, &abort_flag))) ok = false;
+      tc_fence_after();
+    }
+    if (!ok) {
+      abort_flag = 1;
+      set_err(p.err, MG_DERR_TIMEOUT);
+    }
+    const bool have = ok && ntiles > 0 && lrow > 0.f;
+    const float inv = have ? 1.f / lrow : 0.f;
+    const size_t orow = (static_cast<size_t>(b) * p.n + tloc) * kHq + h;
+    if (p.splits == 1) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        if (ok && ntiles > 0) {
+          tmem_ld32(tO + 32 * c, v);
+          tmem_wait_ld();
+        }
+        if (row_valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD + 32 * c);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16x2(have ? __uint_as_float(v[8 * q4 + 0]) * inv : 0.f,
+                              have ? __uint_as_float(v[8 * q4 + 1]) * inv : 0.f);
+            w.y = pack_bf16x2(have ? __uint_as_float(v[8 * q4 + 2]) * inv : 0.f,
+                              have ? __uint_as_float(v[8 * q4 + 3]) * inv : 0.f);
+            w.z = pack_bf16x2(have ? __uint_as_float(v[8 * q4 + 4]) * inv : 0.f,
+                              have ? __uint_as_float(v[8 * q4 + 5]) * inv : 0.f);
+            w.w = pack_bf16x2(have ? __uint_as_float(v[8 * q4 + 6]) * inv : 0.f,
+                              have ? __uint_as_float(v[8 * q4 + 7]) * inv : 0.f);
+            dst[q4] = w;
+          }
+        }
+      }
+    } else {
+      const size_t pr = orow * p.splits + split;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        if (ok && ntiles > 0) {
+          tmem_ld32(tO + 32 * c, v);
+          tmem_wait_ld();
+        }
+        if (row_valid) {
+          float4 *dst = reinterpret_cast<float4 *>(p.part_o + pr * kD + 32 * c);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 w;
+            w.x = have ? __uint_as_float(v[4 * q4 + 0]) * inv : 0.f;
+            w.y = have ? __uint_as_float(v[4 * q4 + 1]) * inv : 0.f;
+            w.z = have ? __uint_as_float(v[4 * q4 + 2]) * inv : 0.f;
+            w.w = have ? __uint_as_float(v[4 * q4 + 3]) * inv : 0.f;
+            dst[q4] = w;
+          }
+        }
+      }
+      if (row_valid) p.part_lse[pr] = have ? mrow + __log2f(lrow) : -INFINITY;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+cudaError_t launch_attn_tc(const TcParams &p, const CUtensorMap &tq, const CUtensorMap &tka,
+                           const CUtensorMap &tva, const CUtensorMap &tkb, const CUtensorMap &tvb,
+                           cudaStream_t s) {
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>(p.qblocks * p.splits), kHkv, static_cast<unsigned>(p.batch));
+  attn_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(p, tq, tka, tva, tkb, tvb);
+  return cudaGetLastError();
+}
+
+}  // namespace mg

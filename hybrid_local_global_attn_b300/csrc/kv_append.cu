@@ -1,0 +1,58 @@
+// kv_append.cu -- write new K/V rows into a layer's cache, verbatim.
+//
+// Local layers keep a 2048-slot ring (slot = pos mod 2048, the oldest entry
+// is reused), global layers a linear cache (slot = pos); see "Tomas Koutsky
+// 解释了 Meta 如何在 24 GB 的容量内容纳 Muse Glimmer", section
+// "窄缓存为长上下文留出空间" (evict or cyclically reuse stale entries).
+// Pure data movement: one thread moves one 16-byte chunk of K and of V.
+#include "mg_internal.h"
+#include "mg_ptx.cuh"
+
+namespace mg {
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  const int b = blockIdx.y;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = static_cast<int64_t>(p.n) * (kHkv * 16);
+  if (idx >= total) return;
+  const int32_t t = static_cast<int32_t>(idx >> 5);  // token within the call
+  const int g = static_cast<int>(idx >> 4) & 1;      // KV head
+  const int c = static_cast<int>(idx & 15);          // 16-byte chunk of the row
+  const int32_t pos0 = p.pos0[b];
+  if (pos0 < 0) {
+    if (idx == 0) set_err(p.err, MG_DERR_POSITION);
+    return;
+  }
+  // A ring keeps only the last `slots` tokens of this call; skipping the
+  // earlier ones gives the same final state as appending one at a time and
+  // avoids two writers racing for one slot.
+  if (p.kind == 0 && t < p.n - p.slots) return;
+  const int64_t pos = static_cast<int64_t>(pos0) + t;
+  int64_t slot;
+  if (p.kind == 0) {
+    slot = pos % p.slots;
+  } else {
+    if (pos >= p.slots) {
+      set_err(p.err, MG_DERR_POSITION);
+      return;
+    }
+    slot = pos;
+  }
+  const size_t src = ((static_cast<size_t>(b) * p.n + t) * kHkv + g) * kD + c * 8;
+  const size_t dst = ((static_cast<size_t>(b) * kHkv + g) * p.slots + slot) * kD + c * 8;
+  const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src));
+  const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src));
+  *reinterpret_cast<uint4 *>(p.k_cache + dst) = kv;
+  *reinterpret_cast<uint4 *>(p.v_cache + dst) = vv;
+}
+
+cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(p.n) * (kHkv * 16);
+  const int64_t blocks = (total + 255) / 256;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(p.batch));
+  kv_append_kernel<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mg

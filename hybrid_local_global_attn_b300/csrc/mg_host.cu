@@ -1,0 +1,455 @@
+// mg_host.cu -- the C ABI of libmg (declared in include/mg.h): argument
+// checks, workspace layout, TMA descriptors and kernel launches.
+//
+// The library keeps no device state and never allocates: every buffer comes
+// from the caller.  Host-side rejections return a status and launch nothing.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "mg_internal.h"
+
+namespace mg {
+namespace {
+
+constexpr int kNumSms = 148;  // B300
+
+// ------------------------------------------------------ TMA descriptors ----
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Small cache of encoded descriptors keyed by (address, shape, box): decode
+// steps re-use the same caches and buffers, and encoding is pure host work.
+struct MapKey {
+  const void *base;
+  uint32_t rank;
+  uint64_t dims[4];
+  uint32_t box[4];
+  bool operator==(const MapKey &o) const {
+    return base == o.base && rank == o.rank && std::memcmp(dims, o.dims, sizeof dims) == 0 &&
+           std::memcmp(box, o.box, sizeof box) == 0;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kMapCache = 512;
+MapEntry g_maps[kMapCache];
+std::mutex g_map_mu;
+
+// bf16 tensor, contiguous rows of 128 elements; strides derive from dims.
+bool make_map(CUtensorMap *out, const void *base, uint32_t rank, const uint64_t *dims,
+              const uint32_t *box) {
+  MapKey key{};
+  key.base = base;
+  key.rank = rank;
+  for (uint32_t i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+  }
+  size_t h = reinterpret_cast<uintptr_t>(base) >> 8;
+  for (uint32_t i = 0; i < rank; ++i) h = h * 1000003u ^ (dims[i] * 31u + box[i]);
+  MapEntry &e = g_maps[h % kMapCache];
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (e.used && e.key == key) {
+      *out = e.map;
+      return true;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t gdim[4], gstride[3];
+  cuuint32_t gbox[4], estr[4] = {1, 1, 1, 1};
+  uint64_t stride = 2;
+  for (uint32_t i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    gbox[i] = box[i];
+    if (i > 0) gstride[i - 1] = stride;
+    stride *= dims[i];
+  }
+  CUtensorMap m;
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), gdim,
+                  gstride, gbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    e.key = key;
+    e.map = m;
+    e.used = true;
+  }
+  *out = m;
+  return true;
+}
+
+// KV-like tensor [outer][rows][128] read in boxes of `box_rows` x 64 dims.
+bool map_rows(CUtensorMap *m, const void *base, uint64_t rows, uint64_t outer, uint32_t box_rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(kD), rows, outer};
+  const uint32_t box[3] = {64, box_rows, 1};
+  return make_map(m, base, 3, dims, box);
+}
+
+// ---------------------------------------------------------------- RoPE ----
+RopeTurns rope_turns(float theta) {
+  static std::mutex mu;
+  static float last_theta = -1.f;
+  static RopeTurns last;
+  std::lock_guard<std::mutex> lk(mu);
+  if (theta != last_theta) {
+    for (int i = 0; i < 64; ++i) {
+      const double w = std::pow(static_cast<double>(theta), -2.0 * i / 128.0);
+      const double t = w / (2.0 * M_PI);  // turns per position, < 1
+      last.turn[i] = static_cast<uint64_t>(std::ldexp(t, 64));
+    }
+    last_theta = theta;
+  }
+  return last;
+}
+
+// ---------------------------------------------------------- validation ----
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_layer(const mg_layer *L) {
+  if (L == nullptr) return MG_ERR_INVALID;
+  if (L->kind != MG_LOCAL && L->kind != MG_GLOBAL) return MG_ERR_INVALID;
+  if (!(L->scale > 0.f) || !std::isfinite(L->scale)) return MG_ERR_UNSUPPORTED;
+  if (L->kind == MG_LOCAL) {
+    if (L->window != kWindow) return MG_ERR_UNSUPPORTED;
+    if (!(L->rope_theta > 1.f) || !std::isfinite(L->rope_theta)) return MG_ERR_UNSUPPORTED;
+  } else if (L->window != 0) {
+    return MG_ERR_UNSUPPORTED;
+  }
+  return MG_OK;
+}
+
+int check_cache(const mg_layer *L, const mg_cache *C) {
+  if (C == nullptr || C->k == nullptr || C->v == nullptr) return MG_ERR_INVALID;
+  if (C->batch < 1 || C->slots < 1) return MG_ERR_INVALID;
+  if (L->kind == MG_LOCAL && C->slots != kWindow) return MG_ERR_UNSUPPORTED;
+  if (!aligned16(C->k) || !aligned16(C->v)) return MG_ERR_INVALID;
+  return MG_OK;
+}
+
+int splits_decode(int32_t kind, int32_t batch, int32_t max_len) {
+  const int64_t n_slots = kind == MG_LOCAL ? std::min<int64_t>(max_len, kWindow) : max_len;
+  const int64_t tiles = (n_slots + kDecTile - 1) / kDecTile;
+  int64_t s = (2 * kNumSms) / (static_cast<int64_t>(batch) * kHkv);
+  s = std::max<int64_t>(1, std::min<int64_t>(s, tiles));
+  return static_cast<int>(std::min<int64_t>(s, kDecMaxSplits));
+}
+
+int splits_verify(int32_t kind, int32_t batch, int32_t max_len) {
+  const int64_t keys = kind == MG_LOCAL ? std::min<int64_t>(max_len, kWindow) : max_len;
+  const int64_t tiles = (keys + kTcKeys - 1) / kTcKeys;
+  int64_t s = kNumSms / (static_cast<int64_t>(batch) * kHkv);
+  s = std::max<int64_t>(1, std::min<int64_t>(s, tiles));
+  return static_cast<int>(std::min<int64_t>(s, kTcMaxSplits));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t part_o, part_lse, qs, ks, vs, total;
+  int splits, R;
+};
+
+// Returns false for arguments no layout exists for.
+bool ws_layout(int32_t op, const mg_layer *L, int32_t batch, int32_t n, int32_t max_len,
+               WsLayout *w) {
+  std::memset(w, 0, sizeof *w);
+  if (L == nullptr || batch < 1 || n < 1 || max_len < 1) return false;
+  size_t off = 0;
+  const bool local = L->kind == MG_LOCAL;
+  if (op == MG_OP_DECODE) {
+    if (n != 1) return false;
+    w->splits = splits_decode(L->kind, batch, max_len);
+    const size_t rows = static_cast<size_t>(batch) * kHq;
+    w->part_o = off;
+    off = align256(off + rows * w->splits * kD * sizeof(float));
+    w->part_lse = off;
+    off = align256(off + rows * w->splits * sizeof(float));
+  } else if (op == MG_OP_VERIFY || op == MG_OP_PREFILL) {
+    if (op == MG_OP_VERIFY && n > MG_VERIFY_MAX) return false;
+    w->splits = op == MG_OP_VERIFY ? splits_verify(L->kind, batch, max_len) : 1;
+    if (w->splits > 1) {
+      const size_t rows = static_cast<size_t>(batch) * n * kHq;
+      w->part_o = off;
+      off = align256(off + rows * w->splits * kD * sizeof(float));
+      w->part_lse = off;
+      off = align256(off + rows * w->splits * sizeof(float));
+    }
+    if (local) {
+      w->R = kWindow + n;
+      w->qs = off;
+      off = align256(off + static_cast<size_t>(batch) * n * kHq * kD * 2);
+      w->ks = off;
+      off = align256(off + static_cast<size_t>(batch) * kHkv * w->R * kD * 2);
+      w->vs = off;
+      off = align256(off + static_cast<size_t>(batch) * kHkv * w->R * kD * 2);
+    }
+  } else {
+    return false;
+  }
+  w->total = off;
+  return true;
+}
+
+int launch_status(cudaError_t e) { return e == cudaSuccess ? MG_OK : MG_ERR_CUDA; }
+
+template <typename T>
+T *at(void *base, size_t off) {
+  return reinterpret_cast<T *>(static_cast<uint8_t *>(base) + off);
+}
+
+}  // namespace
+}  // namespace mg
+
+using namespace mg;
+
+extern "C" {
+
+size_t mg_cache_bytes(int32_t kind, int32_t batch, int32_t capacity) {
+  if (batch < 0) return 0;
+  int64_t slots;
+  if (kind == MG_LOCAL) slots = kWindow;
+  else if (kind == MG_GLOBAL) {
+    if (capacity < 0) return 0;
+    slots = capacity;
+  } else return 0;
+  return static_cast<size_t>(2) * batch * kHkv * slots * kD * 2;
+}
+
+size_t mg_workspace_bytes(int32_t op, const mg_layer *layer, int32_t batch, int32_t n,
+                          int32_t max_len) {
+  if (check_layer(layer) != MG_OK) return static_cast<size_t>(-1);
+  WsLayout w;
+  if (!ws_layout(op, layer, batch, n, max_len, &w)) return static_cast<size_t>(-1);
+  return w.total;
+}
+
+const char *mg_status_str(int status) {
+  switch (status) {
+    case MG_OK: return "ok";
+    case MG_ERR_INVALID: return "invalid argument";
+    case MG_ERR_UNSUPPORTED: return "unsupported shape or layer parameters";
+    case MG_ERR_CAPACITY: return "max_len beyond the cache capacity";
+    case MG_ERR_WORKSPACE: return "workspace too small";
+    case MG_ERR_CUDA: return "CUDA launch or driver call failed";
+    default: return "unknown status";
+  }
+}
+
+int mg_layer_kind(int32_t l) {
+  if (l < 0 || l >= 52) return -1;
+  return (l % 4 == 3) ? MG_GLOBAL : MG_LOCAL;
+}
+
+int mg_kv_append(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos0, int32_t n,
+                 const void *k_new, const void *v_new, uint32_t *d_err, void *stream) {
+  int st = check_layer(layer);
+  if (st != MG_OK) return st;
+  if ((st = check_cache(layer, cache)) != MG_OK) return st;
+  if (n < 0 || d_pos0 == nullptr || d_err == nullptr) return MG_ERR_INVALID;
+  if (n == 0) return MG_OK;
+  if (k_new == nullptr || v_new == nullptr || !aligned16(k_new) || !aligned16(v_new))
+    return MG_ERR_INVALID;
+  AppendParams p;
+  p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  p.k_cache = static_cast<__nv_bfloat16 *>(cache->k);
+  p.v_cache = static_cast<__nv_bfloat16 *>(cache->v);
+  p.pos0 = d_pos0;
+  p.err = d_err;
+  p.batch = cache->batch;
+  p.n = n;
+  p.slots = cache->slots;
+  p.kind = layer->kind;
+  return launch_status(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
+}
+
+int mg_attn_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
+                   int32_t max_len, const void *q, void *o, void *ws, size_t ws_bytes,
+                   uint32_t *d_err, void *stream) {
+  int st = check_layer(layer);
+  if (st != MG_OK) return st;
+  if ((st = check_cache(layer, cache)) != MG_OK) return st;
+  if (d_pos == nullptr || d_err == nullptr || q == nullptr || o == nullptr) return MG_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(o)) return MG_ERR_INVALID;
+  if (max_len < 1) return MG_ERR_INVALID;
+  if (layer->kind == MG_GLOBAL && max_len > cache->slots) return MG_ERR_CAPACITY;
+  WsLayout w;
+  if (!ws_layout(MG_OP_DECODE, layer, cache->batch, 1, max_len, &w)) return MG_ERR_INVALID;
+  if (ws_bytes < w.total || (w.total > 0 && ws == nullptr)) return MG_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MG_ERR_INVALID;
+  CUtensorMap tk, tv;
+  const uint64_t outer = static_cast<uint64_t>(cache->batch) * kHkv;
+  if (!map_rows(&tk, cache->k, cache->slots, outer, kDecTile) ||
+      !map_rows(&tv, cache->v, cache->slots, outer, kDecTile))
+    return MG_ERR_CUDA;
+  DecodeParams p;
+  p.pos = d_pos;
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.part_o = at<float>(ws, w.part_o);
+  p.part_lse = at<float>(ws, w.part_lse);
+  p.err = d_err;
+  p.batch = cache->batch;
+  p.slots = cache->slots;
+  p.kind = layer->kind;
+  p.splits = w.splits;
+  p.max_len = max_len;
+  p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
+  p.rope = rope_turns(layer->kind == MG_LOCAL ? layer->rope_theta : 10000.f);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(p, tk, tv, s);
+  if (e != cudaSuccess) return MG_ERR_CUDA;
+  CombineParams c;
+  c.part_o = p.part_o;
+  c.part_lse = p.part_lse;
+  c.o = static_cast<__nv_bfloat16 *>(o);
+  c.rows = cache->batch * kHq;
+  c.splits = w.splits;
+  return launch_status(launch_combine(c, s));
+}
+
+}  // extern "C"
+
+namespace mg {
+namespace {
+
+// Shared body of verify and prefill.
+int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
+                    const int32_t *d_pos0, int32_t n, int32_t max_len, const void *q,
+                    const void *k_new, const void *v_new, void *o, void *ws, size_t ws_bytes,
+                    uint32_t *d_err, cudaStream_t s) {
+  int st = check_layer(layer);
+  if (st != MG_OK) return st;
+  if ((st = check_cache(layer, cache)) != MG_OK) return st;
+  if (d_pos0 == nullptr || d_err == nullptr || q == nullptr || o == nullptr ||
+      k_new == nullptr || v_new == nullptr)
+    return MG_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k_new) || !aligned16(v_new))
+    return MG_ERR_INVALID;
+  if (n < 1) return MG_ERR_INVALID;
+  if (op == MG_OP_VERIFY && n > MG_VERIFY_MAX) return MG_ERR_UNSUPPORTED;
+  if (max_len < n) return MG_ERR_INVALID;
+  // the cache must hold every position before the block
+  if (layer->kind == MG_GLOBAL && static_cast<int64_t>(max_len) - n > cache->slots)
+    return MG_ERR_CAPACITY;
+  WsLayout w;
+  if (!ws_layout(op, layer, cache->batch, n, max_len, &w)) return MG_ERR_INVALID;
+  if (ws_bytes < w.total || (w.total > 0 && ws == nullptr)) return MG_ERR_WORKSPACE;
+  if (w.total > 0 && !aligned16(ws)) return MG_ERR_INVALID;
+  const int32_t B = cache->batch;
+  const bool local = layer->kind == MG_LOCAL;
+  const uint64_t outer = static_cast<uint64_t>(B) * kHkv;
+
+  const void *qsrc = q;
+  CUtensorMap tq, tka, tva, tkb, tvb;
+  if (local) {
+    StageParams sp;
+    sp.pos0 = d_pos0;
+    sp.q = static_cast<const __nv_bfloat16 *>(q);
+    sp.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    sp.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    sp.k_cache = static_cast<const __nv_bfloat16 *>(cache->k);
+    sp.v_cache = static_cast<const __nv_bfloat16 *>(cache->v);
+    sp.qs = at<__nv_bfloat16>(ws, w.qs);
+    sp.ks = at<__nv_bfloat16>(ws, w.ks);
+    sp.vs = at<__nv_bfloat16>(ws, w.vs);
+    sp.err = d_err;
+    sp.batch = B;
+    sp.n = n;
+    sp.R = w.R;
+    sp.max_len = max_len;
+    sp.rope = rope_turns(layer->rope_theta);
+    if (launch_rope_stage(sp, s) != cudaSuccess) return MG_ERR_CUDA;
+    qsrc = sp.qs;
+    if (!map_rows(&tka, sp.ks, w.R, outer, kTcKeys) || !map_rows(&tva, sp.vs, w.R, outer, kTcKeys))
+      return MG_ERR_CUDA;
+    tkb = tka;
+    tvb = tva;
+  } else {
+    if (!map_rows(&tka, cache->k, cache->slots, outer, kTcKeys) ||
+        !map_rows(&tva, cache->v, cache->slots, outer, kTcKeys))
+      return MG_ERR_CUDA;
+    const uint64_t dims[4] = {static_cast<uint64_t>(kD), kHkv, static_cast<uint64_t>(n),
+                              static_cast<uint64_t>(B)};
+    const uint32_t box[4] = {64, 1, kTcKeys, 1};
+    if (!make_map(&tkb, k_new, 4, dims, box) || !make_map(&tvb, v_new, 4, dims, box))
+      return MG_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(kD), kHq, static_cast<uint64_t>(n),
+                              static_cast<uint64_t>(B)};
+    const uint32_t box[4] = {64, kGroup, kTcPosPerTile, 1};
+    if (!make_map(&tq, qsrc, 4, dims, box)) return MG_ERR_CUDA;
+  }
+  TcParams p;
+  p.pos0 = d_pos0;
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.part_o = w.splits > 1 ? at<float>(ws, w.part_o) : nullptr;
+  p.part_lse = w.splits > 1 ? at<float>(ws, w.part_lse) : nullptr;
+  p.err = d_err;
+  p.batch = B;
+  p.n = n;
+  p.kind = layer->kind;
+  p.window = local ? kWindow : 0;
+  p.staged = local ? 1 : 0;
+  p.splits = w.splits;
+  p.qblocks = (n + kTcPosPerCta - 1) / kTcPosPerCta;
+  p.max_len = max_len;
+  p.slots = cache->slots;
+  p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
+  if (launch_attn_tc(p, tq, tka, tva, tkb, tvb, s) != cudaSuccess) return MG_ERR_CUDA;
+  if (w.splits > 1) {
+    CombineParams c;
+    c.part_o = p.part_o;
+    c.part_lse = p.part_lse;
+    c.o = p.o;
+    c.rows = B * n * kHq;
+    c.splits = w.splits;
+    return launch_status(launch_combine(c, s));
+  }
+  return MG_OK;
+}
+
+}  // namespace
+}  // namespace mg
+
+extern "C" {
+
+int mg_attn_verify(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos0, int32_t n,
+                   int32_t max_len, const void *q, const void *k_new, const void *v_new, void *o,
+                   void *ws, size_t ws_bytes, uint32_t *d_err, void *stream) {
+  return block_attention(MG_OP_VERIFY, layer, cache, d_pos0, n, max_len, q, k_new, v_new, o, ws,
+                         ws_bytes, d_err, static_cast<cudaStream_t>(stream));
+}
+
+int mg_attn_prefill(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos0,
+                    int32_t n, int32_t max_len, const void *q, const void *k_new,
+                    const void *v_new, void *o, void *ws, size_t ws_bytes, uint32_t *d_err,
+                    void *stream) {
+  return block_attention(MG_OP_PREFILL, layer, cache, d_pos0, n, max_len, q, k_new, v_new, o, ws,
+                         ws_bytes, d_err, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

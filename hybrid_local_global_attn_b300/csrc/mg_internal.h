@@ -1,0 +1,111 @@
+// mg_internal.h -- constants and kernel parameter blocks shared by the host
+// entry points and the kernels of libmg (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mg.h"
+
+namespace mg {
+
+// Shape fixed by the model: 32 query heads, 2 KV heads, head dim 128, a
+// 2048-token window for local layers.
+constexpr int kHq = 32;
+constexpr int kHkv = 2;
+constexpr int kD = 128;
+constexpr int kGroup = kHq / kHkv;  // 16 query heads per KV head
+constexpr int kWindow = 2048;
+constexpr int kRowBytes = kD * 2;   // one bf16 head row
+
+// Every pipeline wait gives up after this much wall time (ns).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Decode (split-KV flash-decode on mma.sync):
+constexpr int kDecTile = 64;              // keys per pipeline stage
+constexpr int kDecStages = 3;             // TMA ring depth (2 CTAs per SM)
+constexpr int kDecWarps = 4;              // consumer warps, 16 keys each per stage
+constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one TMA producer warp
+constexpr int kDecStageBytes = 2 * kDecTile * kRowBytes;  // K + V
+constexpr int kDecSmem = kDecStages * kDecStageBytes + 1024 /*align*/ + 256 /*barriers*/ +
+                         64 * 8 /*rope turns*/;
+constexpr int kDecMaxSplits = 296;
+
+// tcgen05 attention (verify + prefill): 2 query tiles of 128 rows
+// (8 positions x 16 heads each), key tiles of 128.
+constexpr int kTcRows = 128;
+constexpr int kTcKeys = 128;
+constexpr int kTcPosPerTile = kTcRows / kGroup;   // 8
+constexpr int kTcPosPerCta = 2 * kTcPosPerTile;   // 16
+constexpr int kTcStages = 2;
+constexpr int kTcTileBytes = kTcKeys * kRowBytes;  // 32 KB (two 64-dim boxes)
+constexpr int kTcQBytes = kTcRows * kRowBytes;     // 32 KB per query tile
+constexpr int kTcSmem = 2 * kTcQBytes + kTcStages * 2 * kTcTileBytes + 1024 + 256;
+constexpr int kTcThreads = 320;  // warps 0-3 softmax A, 4-7 softmax B, 8 TMA, 9 MMA
+constexpr int kTcMaxSplits = 160;
+
+struct RopeTurns {
+  uint64_t turn[64];  // w_i / (2 pi) in 0.64 fixed point, w_i = theta^(-2i/128)
+};
+
+struct AppendParams {
+  const __nv_bfloat16 *k_new, *v_new;  // [B][n][2][128]
+  __nv_bfloat16 *k_cache, *v_cache;    // [B][2][slots][128]
+  const int32_t *pos0;
+  uint32_t *err;
+  int32_t batch, n, slots, kind;
+};
+
+struct DecodeParams {
+  const int32_t *pos;
+  const __nv_bfloat16 *q;  // [B][32][128]
+  float *part_o;           // [B][32][splits][128]
+  float *part_lse;         // [B][32][splits]   (log2 domain)
+  uint32_t *err;
+  int32_t batch, slots, kind, splits, max_len;
+  float scale_log2;        // softmax scale * log2(e)
+  RopeTurns rope;
+};
+
+struct CombineParams {
+  const float *part_o;    // [rows][splits][128]
+  const float *part_lse;  // [rows][splits]
+  __nv_bfloat16 *o;       // [rows][128]
+  int32_t rows, splits;
+};
+
+struct StageParams {
+  const int32_t *pos0;
+  const __nv_bfloat16 *q;                 // [B][n][32][128]
+  const __nv_bfloat16 *k_new, *v_new;     // [B][n][2][128]
+  const __nv_bfloat16 *k_cache, *v_cache; // ring [B][2][2048][128]
+  __nv_bfloat16 *qs;                      // [B][n][32][128]  rotated q
+  __nv_bfloat16 *ks, *vs;                 // [B][2][R][128]  rows = pos - c0 + 2048
+  uint32_t *err;
+  int32_t batch, n, R, max_len;
+  RopeTurns rope;
+};
+
+struct TcParams {
+  const int32_t *pos0;
+  __nv_bfloat16 *o;  // direct output [B][n][32][128] (splits == 1)
+  float *part_o;     // [B*n*32][splits][128] (splits > 1)
+  float *part_lse;   // [B*n*32][splits]
+  uint32_t *err;
+  int32_t batch, n, kind, window, staged, splits, qblocks, max_len, slots;
+  float scale_log2;
+};
+
+// Kernel launchers (defined next to each kernel).
+cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                          cudaStream_t s);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
+cudaError_t launch_rope_stage(const StageParams &p, cudaStream_t s);
+cudaError_t launch_attn_tc(const TcParams &p, const CUtensorMap &tq, const CUtensorMap &tka,
+                           const CUtensorMap &tva, const CUtensorMap &tkb, const CUtensorMap &tvb,
+                           cudaStream_t s);
+
+}  // namespace mg

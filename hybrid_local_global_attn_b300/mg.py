@@ -1,0 +1,167 @@
+"""ctypes binding of libmg (the C ABI in ``include/mg.h``).
+
+Argument marshalling only: every step of the attention path runs in the CUDA
+kernels of ``libmg.so``.  Functions keep the C names; tensors are torch
+tensors on the GPU (bf16 data, int32 positions, uint32 error word), the
+stream defaults to torch's current stream.  There is no CPU fallback: the
+import fails if the library has not been built, and a call on a machine
+without a GPU fails in the library.
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmg.so")
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python -m hybrid_local_global_attn_b300.build` (nvcc, sm_103a)")
+lib = ctypes.CDLL(LIB_PATH)
+
+HQ, HKV, D = 32, 2, 128
+WINDOW = 2048
+VERIFY_MAX = 16
+N_LAYERS = 52
+LOCAL, GLOBAL = 0, 1
+OP_DECODE, OP_VERIFY, OP_PREFILL = 0, 1, 2
+DERR_POSITION, DERR_TIMEOUT = 1, 2
+ROPE_THETA = 10000.0
+SCALE = 1.0 / math.sqrt(D)
+
+
+class mg_layer(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float), ("scale", ctypes.c_float)]
+
+
+class mg_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("batch", ctypes.c_int32), ("slots", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_LP = ctypes.POINTER(mg_layer)
+_CP = ctypes.POINTER(mg_cache)
+lib.mg_cache_bytes.argtypes = [_i32, _i32, _i32]
+lib.mg_cache_bytes.restype = ctypes.c_size_t
+lib.mg_workspace_bytes.argtypes = [_i32, _LP, _i32, _i32, _i32]
+lib.mg_workspace_bytes.restype = ctypes.c_size_t
+lib.mg_status_str.argtypes = [ctypes.c_int]
+lib.mg_status_str.restype = ctypes.c_char_p
+lib.mg_layer_kind.argtypes = [_i32]
+lib.mg_layer_kind.restype = ctypes.c_int
+lib.mg_kv_append.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P]
+lib.mg_attn_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, _P, _P]
+lib.mg_attn_verify.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+lib.mg_attn_prefill.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+for _f in (lib.mg_kv_append, lib.mg_attn_decode, lib.mg_attn_verify, lib.mg_attn_prefill):
+    _f.restype = ctypes.c_int
+
+
+class MgError(RuntimeError):
+    def __init__(self, status):
+        self.status = status
+        super().__init__(f"libmg: {mg_status_str(status)} (status {status})")
+
+
+def mg_status_str(status: int) -> str:
+    return lib.mg_status_str(int(status)).decode()
+
+
+def mg_cache_bytes(kind: int, batch: int, capacity: int) -> int:
+    return int(lib.mg_cache_bytes(kind, batch, capacity))
+
+
+def mg_layer_kind(l: int) -> int:
+    return int(lib.mg_layer_kind(l))
+
+
+def make_layer(kind: int, rope_theta: float = ROPE_THETA, scale: float = SCALE) -> mg_layer:
+    return mg_layer(int(kind), WINDOW if kind == LOCAL else 0,
+                    float(rope_theta) if kind == LOCAL else 0.0, float(scale))
+
+
+def mg_workspace_bytes(op: int, layer: mg_layer, batch: int, n: int, max_len: int) -> int:
+    v = int(lib.mg_workspace_bytes(op, ctypes.byref(layer), batch, n, max_len))
+    if v == ctypes.c_size_t(-1).value:
+        raise MgError(1)
+    return v
+
+
+class KVCache:
+    """One layer's cache: k and v bf16 [batch][2][slots][128] on the GPU."""
+
+    def __init__(self, kind: int, batch: int, capacity: int = 0, device="cuda"):
+        self.kind = kind
+        self.batch = batch
+        self.slots = WINDOW if kind == LOCAL else int(capacity)
+        self.k = torch.zeros((batch, HKV, self.slots, D), dtype=torch.bfloat16, device=device)
+        self.v = torch.zeros_like(self.k)
+        self.struct = mg_cache(self.k.data_ptr(), self.v.data_ptr(), batch, self.slots)
+
+    def nbytes(self) -> int:
+        return self.k.numel() * 2 + self.v.numel() * 2
+
+
+def _ptr(t, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous() or (dtype is not None and t.dtype != dtype):
+        raise TypeError(f"expected a contiguous CUDA tensor of {dtype}, got {t.dtype} "
+                        f"on {t.device} (contiguous={t.is_contiguous()})")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _call(fn, *args):
+    rc = fn(*args)
+    if rc != 0:
+        raise MgError(rc)
+
+
+def mg_kv_append(layer, cache: KVCache, pos0, k_new, v_new, err, stream=None):
+    _call(lib.mg_kv_append, ctypes.byref(layer), ctypes.byref(cache.struct), _ptr(pos0, torch.int32),
+          int(k_new.shape[1]), _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
+          _ptr(err, torch.int32), _stream(stream))
+
+
+def mg_attn_decode(layer, cache: KVCache, pos, max_len, q, o, ws, err, stream=None):
+    _call(lib.mg_attn_decode, ctypes.byref(layer), ctypes.byref(cache.struct), _ptr(pos, torch.int32),
+          int(max_len), _ptr(q, torch.bfloat16), _ptr(o, torch.bfloat16), _ptr(ws),
+          ws.numel() * ws.element_size() if ws is not None else 0, _ptr(err, torch.int32),
+          _stream(stream))
+
+
+def mg_attn_verify(layer, cache: KVCache, pos0, max_len, q, k_new, v_new, o, ws, err, stream=None):
+    _call(lib.mg_attn_verify, ctypes.byref(layer), ctypes.byref(cache.struct), _ptr(pos0, torch.int32),
+          int(q.shape[1]), int(max_len), _ptr(q, torch.bfloat16), _ptr(k_new, torch.bfloat16),
+          _ptr(v_new, torch.bfloat16), _ptr(o, torch.bfloat16), _ptr(ws),
+          ws.numel() * ws.element_size() if ws is not None else 0, _ptr(err, torch.int32),
+          _stream(stream))
+
+
+def mg_attn_prefill(layer, cache: KVCache, pos0, max_len, q, k_new, v_new, o, ws, err, stream=None):
+    _call(lib.mg_attn_prefill, ctypes.byref(layer), ctypes.byref(cache.struct), _ptr(pos0, torch.int32),
+          int(q.shape[1]), int(max_len), _ptr(q, torch.bfloat16), _ptr(k_new, torch.bfloat16),
+          _ptr(v_new, torch.bfloat16), _ptr(o, torch.bfloat16), _ptr(ws),
+          ws.numel() * ws.element_size() if ws is not None else 0, _ptr(err, torch.int32),
+          _stream(stream))
+
+
+def workspace(op, layer, batch, n, max_len, device="cuda"):
+    """Caller-side workspace allocation (torch) of the size libmg asks for."""
+    nbytes = mg_workspace_bytes(op, layer, batch, n, max_len)
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def error_word(device="cuda"):
+    """Device error word (int32 view of the C uint32), zeroed."""
+    return torch.zeros(1, dtype=torch.int32, device=device)

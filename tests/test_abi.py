@@ -1,0 +1,136 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol,
+its byte model matches the figures the pages print, and host-side argument
+checks reject bad calls before touching CUDA.  No GPU needed.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "mg.h")
+GIB = 1024 ** 3
+MIB = 1024 ** 2
+
+
+@pytest.fixture(scope="module")
+def mg():
+    from hybrid_local_global_attn_b300 import build
+    build.build()
+    from hybrid_local_global_attn_b300 import mg as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mg_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(mg):
+    names = declared_functions()
+    assert {"mg_kv_append", "mg_attn_decode", "mg_attn_verify", "mg_attn_prefill",
+            "mg_cache_bytes", "mg_workspace_bytes", "mg_status_str"} <= set(names)
+    for n in names:
+        assert hasattr(mg.lib, n), n
+        assert ctypes.cast(getattr(mg.lib, n), ctypes.c_void_p).value
+
+
+def test_byte_model_matches_pages(mg, golden_bytes):
+    gb = golden_bytes
+    per_tok = mg.mg_cache_bytes(mg.GLOBAL, 1, 1)
+    assert per_tok == gb["kv_bytes_per_token_layer"][0] == 1024
+    T = 131072
+    kinds = [mg.mg_layer_kind(l) for l in range(52)]
+    assert kinds.count(mg.GLOBAL) == 13 and kinds.count(mg.LOCAL) == 39
+    assert all((k == mg.GLOBAL) == (l % 4 == 3) for l, k in enumerate(kinds))
+    glob = sum(mg.mg_cache_bytes(k, 1, T) for k in kinds if k == mg.GLOBAL)
+    loc = sum(mg.mg_cache_bytes(k, 1, T) for k in kinds if k == mg.LOCAL)
+    assert glob / GIB == gb["global_kv_gib"][0]          # 1.625 GiB exactly
+    v, tol, _ = gb["local_kv_mib"]
+    assert abs(loc / MIB - v) <= tol * v                  # 78 MiB
+    v, tol, _ = gb["hybrid_kv_gib"]
+    assert abs((glob + loc) / GIB - v) <= tol * v         # ~1.70 GiB
+    v, tol, _ = gb["all_global_kv_gib"]
+    allg = 52 * mg.mg_cache_bytes(mg.GLOBAL, 1, T)
+    assert abs(allg / GIB - v) <= tol * v                 # 6.5 GiB
+    # MHA: 32 KV heads instead of 2
+    assert 32 // mg.HKV == gb["mha_factor"][0]
+    assert (glob + loc) * 16 / GIB > gb["mha_kv_gib_at_least"][0]
+    assert mg.mg_cache_bytes(mg.LOCAL, 3, 999999) == 3 * mg.mg_cache_bytes(mg.LOCAL, 1, 0)
+    assert mg.mg_cache_bytes(7, 1, 10) == 0 and mg.mg_cache_bytes(mg.GLOBAL, 1, -1) == 0
+
+
+def test_status_strings_and_kinds(mg):
+    assert mg.mg_status_str(0) == "ok"
+    for s in range(1, 6):
+        assert mg.mg_status_str(s) not in ("ok", "unknown status")
+    assert mg.mg_layer_kind(-1) == -1 and mg.mg_layer_kind(52) == -1
+
+
+def test_workspace_sizes(mg):
+    L = mg.make_layer(mg.LOCAL)
+    G = mg.make_layer(mg.GLOBAL)
+    for op, n in ((mg.OP_DECODE, 1), (mg.OP_VERIFY, 16), (mg.OP_PREFILL, 4096)):
+        for lay in (L, G):
+            w = mg.mg_workspace_bytes(op, lay, 2, n, 40000)
+            assert w >= 0
+    assert mg.mg_workspace_bytes(mg.OP_PREFILL, G, 1, 4096, 32768) == 0  # global prefill: none
+    assert mg.mg_workspace_bytes(mg.OP_DECODE, G, 1, 1, 131073) > 0
+    with pytest.raises(mg.MgError):
+        mg.mg_workspace_bytes(mg.OP_VERIFY, G, 1, 17, 1000)     # block > 16
+    with pytest.raises(mg.MgError):
+        mg.mg_workspace_bytes(mg.OP_DECODE, G, 0, 1, 1000)      # batch 0
+    bad = mg.mg_layer(mg.LOCAL, 1024, 1e4, mg.SCALE)             # window != 2048
+    with pytest.raises(mg.MgError):
+        mg.mg_workspace_bytes(mg.OP_DECODE, bad, 1, 1, 100)
+
+
+def _raw_call_status(mg, fn, *args):
+    return fn(*args)
+
+
+def test_host_side_rejections_launch_nothing(mg):
+    """Bad arguments come back as a status before any CUDA call (so this runs
+    without a GPU).  Pointers are fake but never dereferenced on the host."""
+    lib = mg.lib
+    fake = ctypes.c_void_p(0x1000)
+    cache = mg.mg_cache(0x10000, 0x20000, 1, 2048)
+    L = mg.make_layer(mg.LOCAL)
+    G = mg.make_layer(mg.GLOBAL)
+    by = ctypes.byref
+    # null layer / cache / positions
+    assert lib.mg_kv_append(None, by(cache), fake, 1, fake, fake, fake, None) == 1
+    assert lib.mg_kv_append(by(L), None, fake, 1, fake, fake, fake, None) == 1
+    assert lib.mg_kv_append(by(L), by(cache), None, 1, fake, fake, fake, None) == 1
+    assert lib.mg_kv_append(by(L), by(cache), fake, -1, fake, fake, fake, None) == 1
+    # n == 0 is a no-op
+    assert lib.mg_kv_append(by(L), by(cache), fake, 0, fake, fake, fake, None) == 0
+    # local layer with a cache that is not a 2048-slot ring
+    c2 = mg.mg_cache(0x10000, 0x20000, 1, 4096)
+    assert lib.mg_kv_append(by(L), by(c2), fake, 1, fake, fake, fake, None) == 2
+    # window / theta / scale out of range
+    for bad in (mg.mg_layer(mg.LOCAL, 4096, 1e4, mg.SCALE), mg.mg_layer(mg.LOCAL, 2048, 0.0, mg.SCALE),
+                mg.mg_layer(mg.GLOBAL, 2048, 0.0, mg.SCALE), mg.mg_layer(mg.GLOBAL, 0, 0.0, -1.0),
+                mg.mg_layer(5, 0, 0.0, mg.SCALE)):
+        assert lib.mg_attn_decode(by(bad), by(cache), fake, 10, fake, fake, fake, 1 << 30,
+                                  fake, None) in (1, 2)
+    # global decode past capacity
+    gc = mg.mg_cache(0x10000, 0x20000, 1, 1000)
+    assert lib.mg_attn_decode(by(G), by(gc), fake, 1001, fake, fake, fake, 1 << 30, fake, None) == 3
+    # workspace too small
+    need = mg.mg_workspace_bytes(mg.OP_DECODE, G, 1, 1, 1000)
+    assert lib.mg_attn_decode(by(G), by(gc), fake, 1000, fake, fake, fake, need - 1, fake, None) == 4
+    # misaligned tensor pointer
+    assert lib.mg_attn_decode(by(G), by(gc), fake, 1000, ctypes.c_void_p(0x1002), fake, fake,
+                              1 << 30, fake, None) == 1
+    # verify block longer than 16
+    assert lib.mg_attn_verify(by(G), by(gc), fake, 17, 1017, fake, fake, fake, fake, fake, 1 << 30,
+                              fake, None) == 2
+    # verify / prefill: cache too short for the positions before the block
+    assert lib.mg_attn_prefill(by(G), by(gc), fake, 100, 1101, fake, fake, fake, fake, fake, 1 << 30,
+                               fake, None) == 3
+    assert lib.mg_attn_prefill(by(G), by(gc), fake, 0, 10, fake, fake, fake, fake, fake, 1 << 30,
+                               fake, None) == 1

@@ -1,0 +1,126 @@
+"""Decode attention on the GPU against the fp64 oracle: ragged positions
+around tile and ring boundaries, mixed batches, the 256-step two-layer
+decode across the ring wrap with the cache checked bit for bit after every
+step, and sampled checks at 32K and 128K context."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import bits_of, cache_expected, check_err, compare, oracle_kind
+from hybrid_local_global_attn_b300 import synth
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mg():
+    from hybrid_local_global_attn_b300 import mg as m
+    return m
+
+
+def fill_for_decode(mg, kind, k, v, positions, capacity):
+    """Cache whose state is what appending positions 0..p_b gives (for the
+    ring: the last 2048 of them).  Returns the cache."""
+    B = k.shape[0]
+    cache = mg.KVCache(kind, B, capacity)
+    lay = mg.make_layer(kind)
+    err = mg.error_word()
+    if kind == 1:
+        n = k.shape[1]
+        pos0 = [0] * B
+    else:
+        n = 2048
+        pos0 = [max(0, p - 2047) for p in positions]
+    kn = torch.stack([k[b, p:p + n] for b, p in enumerate(pos0)]).cuda().contiguous()
+    vn = torch.stack([v[b, p:p + n] for b, p in enumerate(pos0)]).cuda().contiguous()
+    mg.mg_kv_append(lay, cache, torch.tensor(pos0, dtype=torch.int32, device="cuda"), kn, vn, err)
+    torch.cuda.synchronize()
+    check_err(err)
+    return cache
+
+
+def decode_once(mg, kind, cache, positions, q, max_len):
+    lay = mg.make_layer(kind)
+    B = q.shape[0]
+    ws = mg.workspace(mg.OP_DECODE, lay, B, 1, max_len)
+    o = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    err = mg.error_word()
+    mg.mg_attn_decode(lay, cache, torch.tensor(positions, dtype=torch.int32, device="cuda"), max_len,
+                      q.cuda().contiguous(), o, ws, err)
+    torch.cuda.synchronize()
+    return o, err
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+@pytest.mark.parametrize("positions", [[0, 1, 63], [64, 65, 127], [2046, 2047, 2048],
+                                       [3000, 4095, 4100], [129, 2500, 63]])
+def test_decode_ragged_positions(mg, kind, positions):
+    B = len(positions)
+    T = max(max(0, p - 2047) for p in positions) + 2048 if kind == 0 else max(positions) + 1
+    k, v = synth.history(B, T, 7, 2 if kind == 0 else 3)
+    q = synth.queries(B, 1, 7, 2 if kind == 0 else 3)[:, 0]
+    cache = fill_for_decode(mg, kind, k, v, positions, capacity=T)
+    max_len = max(positions) + 1
+    o, err = decode_once(mg, kind, cache, positions, q, max_len)
+    check_err(err)
+    lay = orc.layer(oracle_kind(kind))
+    for b, p in enumerate(positions):
+        ref = orc.attention(lay, k[b, :p + 1], v[b, :p + 1], [p], q[b:b + 1])[0]
+        compare(o[b], ref, f"kind {kind} b {b} p {p}")
+
+
+def test_decode_position_beyond_max_len_is_flagged(mg):
+    k, v = synth.history(2, 300, 8, 3)
+    q = synth.queries(2, 1, 8, 3)[:, 0]
+    cache = fill_for_decode(mg, 1, k, v, [100, 299], capacity=300)
+    o, err = decode_once(mg, 1, cache, [100, 299], q, max_len=200)  # 299 >= max_len
+    check_err(err, mg.DERR_POSITION)
+    ref = orc.attention(orc.layer(orc.GLOBAL), k[0, :101], v[0, :101], [100], q[:1])[0]
+    compare(o[0], ref, "valid sequence next to a rejected one")
+    assert float(o[1].float().abs().max()) == 0.0
+
+
+def test_pr1_two_layer_decode_across_ring_wrap(mg):
+    """One local (window 2048, RoPE 1e4) and one global layer, batch 1, seed 0:
+    cache pre-filled for positions 0..1999, then 256 single-token steps at
+    p = 2000..2255 (append, then decode), every output compared with the
+    oracle and both caches compared bit for bit after every step."""
+    seed, P0, steps = 0, 2000, 256
+    T = P0 + steps
+    layers = [(0, 0), (1, 3)]  # (kind, layer index for the seed)
+    state = []
+    for kind, li in layers:
+        k, v = synth.history(1, T, seed, li)
+        q = synth.queries(1, steps, seed, li)
+        cache = mg.KVCache(kind, 1, T)
+        lay = mg.make_layer(kind)
+        err = mg.error_word()
+        mg.mg_kv_append(lay, cache, torch.tensor([0], dtype=torch.int32, device="cuda"),
+                        k[:, :P0].cuda().contiguous(), v[:, :P0].cuda().contiguous(), err)
+        ws = mg.workspace(mg.OP_DECODE, lay, 1, 1, T)
+        exp_k = np.zeros((2, cache.slots, 128), np.uint16)
+        exp_v = np.zeros_like(exp_k)
+        orc.cache_append(oracle_kind(kind), exp_k, exp_v, 0, k[0, :P0], v[0, :P0])
+        state.append(dict(kind=kind, k=k, v=v, q=q, cache=cache, lay=lay, err=err, ws=ws,
+                          kd=k.cuda(), vd=v.cuda(), qd=q.cuda(), exp_k=exp_k, exp_v=exp_v,
+                          olay=orc.layer(oracle_kind(kind))))
+    o = torch.empty((1, 32, 128), dtype=torch.bfloat16, device="cuda")
+    worst = 0.0
+    for i in range(steps):
+        p = P0 + i
+        pos = torch.tensor([p], dtype=torch.int32, device="cuda")
+        for s in state:
+            mg.mg_kv_append(s["lay"], s["cache"], pos, s["kd"][:, p:p + 1].contiguous(),
+                            s["vd"][:, p:p + 1].contiguous(), s["err"])
+            mg.mg_attn_decode(s["lay"], s["cache"], pos, T, s["qd"][:, i].contiguous(), o, s["ws"],
+                              s["err"])
+            orc.cache_append(oracle_kind(s["kind"]), s["exp_k"], s["exp_v"], p, s["k"][0, p:p + 1],
+                             s["v"][0, p:p + 1])
+            ref = orc.attention(s["olay"], s["k"][0, :p + 1], s["v"][0, :p + 1], [p], s["q"][:, i])[0]
+            err_abs, _, _ = compare(o[0], ref, f"kind {s['kind']} step {i} p {p}")
+            worst = max(worst, err_abs)
+            assert np.array_equal(bits_of(s["cache"].k[0]), s["exp_k"]), f"K cache step {i}"
+            assert np.array_equal(bits_of(s["cache"].v[0]), s["exp_v"]), f"V cache step {i}"
+    for s in state:
+        check_err(s["err"])
