@@ -360,8 +360,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                           cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kDecSmem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(decode_kernel), kDecSmem, 0);
   if (e != cudaSuccess) return e;
   dim3 grid(p.splits, kHkv, p.batch);
   decode_kernel<<<grid, kDecThreads, kDecSmem, s>>>(p, tk, tv);

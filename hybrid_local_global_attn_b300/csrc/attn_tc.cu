@@ -421,8 +421,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 cudaError_t launch_attn_tc(const TcParams &p, const CUtensorMap &tq, const CUtensorMap &tka,
                            const CUtensorMap &tva, const CUtensorMap &tkb, const CUtensorMap &tvb,
                            cudaStream_t s) {
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(attn_tc_kernel), kTcSmem, 1);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.qblocks * p.splits), kHkv, static_cast<unsigned>(p.batch));
   attn_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(p, tq, tka, tva, tkb, tvb);

@@ -108,6 +108,24 @@ bool map_rows(CUtensorMap *m, const void *base, uint64_t rows, uint64_t outer, u
   return make_map(m, base, 3, dims, box);
 }
 
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id) {
+  static std::mutex mu;
+  static uint64_t done[4] = {0, 0, 0, 0};  // bit d: set on device d
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || kernel_id < 0 || kernel_id >= 4) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[kernel_id] & (1ull << dev)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[kernel_id] |= 1ull << dev;
+  return e;
+}
+
+namespace {
+
 // ---------------------------------------------------------------- RoPE ----
 RopeTurns rope_turns(float theta) {
   static std::mutex mu;

@@ -98,6 +98,10 @@ struct TcParams {
   float scale_log2;
 };
 
+// Sets the kernel's dynamic shared-memory limit once per device (so that no
+// attribute call happens while a stream is being captured into a graph).
+cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id);
+
 // Kernel launchers (defined next to each kernel).
 cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
