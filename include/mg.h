@@ -153,6 +153,31 @@ int mg_attn_decode(const mg_layer *layer, const mg_cache *cache,
                    void *stream);
 
 /*
+ * Decode attention without a workspace argument, for callers that cannot
+ * allocate device memory: for example a plugin inside a host framework that
+ * owns every device buffer and gives plugins none, or a serving loop that
+ * must not call cudaMalloc on its hot path and has no spare buffer to lend.
+ * The pages have no counterpart to this; it is a packaging of
+ * mg_attn_decode, with the same arguments minus ws / ws_bytes and the same
+ * results.
+ *
+ * The split partials live in a fixed device array of MG_NOALLOC_SCRATCH_BYTES
+ * inside libmg.so (held by every GPU that loads the library until the process
+ * exits).  A call whose mg_workspace_bytes(MG_OP_DECODE, layer, batch, 1,
+ * max_len) exceeds it returns MG_ERR_WORKSPACE and launches nothing (at the
+ * default split counts this is batch above ~250).  The array is shared by
+ * all calls on a device and keeps the last call's contents; nothing in it
+ * has to start at zero.  Calls that overlap on the GPU (e.g. on two streams)
+ * race on it.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress, that device current); make that first call
+ * before any stream capture.
+ */
+#define MG_NOALLOC_SCRATCH_BYTES (4u << 20)
+int mg_attn_decode_noalloc(const mg_layer *layer, const mg_cache *cache,
+                           const int32_t *d_pos, int32_t max_len, const void *q,
+                           void *o, uint32_t *d_err, void *stream);
+
+/*
  * Parallel verify of a speculative draft block [P1 §04; P4 "第三招"]:
  * n (1..16) consecutive query tokens at positions p0[b] .. p0[b]+n-1 in
  * one pass.  Query i sees the cached keys before p0 inside its window plus
