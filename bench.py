@@ -6,7 +6,7 @@ RoPE, 13 global), batch 1.  A 131072-token prompt is prefilled in
 8192-token chunks through every layer (prefill + append), the 16-token
 speculative verify runs against the 131072-token cache, then decode steps
 run at positions 131072, 131073, ...  One timed step = one decode token
-through all 52 layers (append + split-KV decode + combine), replayed from a
+through all 52 layers (fused append + split-KV decode, then combine), replayed from a
 CUDA graph of the C-ABI calls.  The headline value is decode attention HBM
 throughput (algorithmic K/V + q/o bytes / time); prefill TFLOP/s and the
 verify numbers are measured in the same run and reported beside it.
@@ -322,17 +322,19 @@ def leg_verify(wl):
     e1.record()
     e1.synchronize()
     ms = e0.elapsed_time(e1) / reps
+    # the 13 global-layer verify calls back to back from one graph
     glob = [l for l in range(N_LAYERS) if wl.kinds[l] == mg.GLOBAL]
-    evs = []
-    for r in range(3):
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
         for l in glob:
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
             one(l)
-            b.record()
-            evs.append((a, b))
-    torch.cuda.synchronize()
-    g_ms = statistics.mean(a.elapsed_time(b) for a, b in evs[len(glob):])
+    g2.replay()
+    e0.record()
+    for _ in range(reps):
+        g2.replay()
+    e1.record()
+    e1.synchronize()
+    g_ms = e0.elapsed_time(e1) / (reps * len(glob))
     assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after verify"
     nbytes = sum(verify_layer_bytes(k, PROMPT, 16) for k in wl.kinds)
     flops = sum(verify_layer_flops(k, PROMPT, 16) for k in wl.kinds)
@@ -379,8 +381,8 @@ def run_gpu(args, rank, world):
 
     def decode_step():
         for l in range(N_LAYERS):
-            mg.mg_kv_append(layers[l], caches[l], pos_cur, k_cur[l], v_cur[l], err)
-            mg.mg_attn_decode(layers[l], caches[l], pos_cur, cap, q_cur[l], o_cur[l], ws_dec[l], err)
+            mg.mg_append_decode(layers[l], caches[l], pos_cur, cap, q_cur[l], k_cur[l], v_cur[l],
+                                o_cur[l], ws_dec[l], err)
 
     def stage(i):
         pos_cur.fill_(PROMPT + i)
@@ -394,7 +396,7 @@ def run_gpu(args, rank, world):
     g_dec = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_dec):
         decode_step()
-    launches_per_step = 3 * N_LAYERS  # append + decode + combine per layer
+    launches_per_step = 2 * N_LAYERS  # fused append+decode, then combine, per layer
     for i in range(W):
         stage(i)
         g_dec.replay()
@@ -529,6 +531,70 @@ def run_gpu(args, rank, world):
     return 0
 
 
+def run_micro():
+    """Per-call cost of each entry point inside a CUDA graph of back-to-back
+    calls (warm, launch gaps included): 39 local-layer decodes, 13
+    global-layer decodes at 131072 keys, one-token appends.  Prints one JSON
+    line; used to see where a decode step's time goes."""
+    import torch
+    from hybrid_local_global_attn_b300 import mg
+    dev = torch.device("cuda", 0)
+    err = mg.error_word()
+    bf = torch.bfloat16
+    T = PROMPT + 64
+    out = {}
+
+    def timed(fn, reps=20):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3  # us per graph
+
+    for kind, n_layers, name in ((mg.LOCAL, 39, "local"), (mg.GLOBAL, 13, "global")):
+        lay = mg.make_layer(kind)
+        caches = [mg.KVCache(kind, 1, T) for _ in range(n_layers)]
+        for c in caches:
+            c.k.normal_()
+            c.v.normal_()
+        q = torch.randn((n_layers, 1, 32, 128), device=dev).to(bf)
+        kn = torch.randn((n_layers, 1, 1, 2, 128), device=dev).to(bf)
+        vn = torch.randn_like(kn)
+        o = torch.empty_like(q)
+        ws = [mg.workspace(mg.OP_DECODE, lay, 1, 1, T) for _ in range(n_layers)]
+        pos = torch.tensor([PROMPT], dtype=torch.int32, device=dev)
+
+        def dec():
+            for l in range(n_layers):
+                mg.mg_attn_decode(lay, caches[l], pos, T, q[l], o[l], ws[l], err)
+
+        def appdec():
+            for l in range(n_layers):
+                mg.mg_append_decode(lay, caches[l], pos, T, q[l], kn[l], vn[l], o[l], ws[l], err)
+
+        def app():
+            for l in range(n_layers):
+                mg.mg_kv_append(lay, caches[l], pos, kn[l], vn[l], err)
+
+        out[f"{name}_decode_us"] = timed(dec) / n_layers
+        out[f"{name}_append_decode_us"] = timed(appdec) / n_layers
+        out[f"{name}_append_us"] = timed(app) / n_layers
+        del caches
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error word {int(err.item()):#x}"
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def run_ncu_case(name):
     """Small, self-contained launches of one kernel for ncu captures: inputs
     larger than L2 where the kernel streams memory, a few GB at most."""
@@ -595,7 +661,11 @@ def main():
                     help="random: fill caches without attention (profiling runs only)")
     ap.add_argument("--ncu-case", default=None,
                     help="decode_global | verify_global | prefill_global | prefill_local")
+    ap.add_argument("--micro", action="store_true",
+                    help="per-call cost of each entry point in graphs of back-to-back calls")
     args = ap.parse_args()
+    if args.micro:
+        return run_micro()
     if args.ncu_case:
         return run_ncu_case(args.ncu_case)
     if args.warmup < 3:

@@ -84,6 +84,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int qb = p.qblocks - 1 - static_cast<int>(blockIdx.x / p.splits);  // heavy blocks first
   const bool local = (p.kind == 0);
 
+  pdl_wait();  // positions, block K/V and (local) staged operands come from earlier kernels
+  pdl_launch_dependents();
+
   // ------------------------------------------------------ tile schedule ----
   TileInfo ti;
   ti.c0 = p.pos0[b];
@@ -286,20 +289,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t kp0 = tile_kp0(ti, t);
       const bool need_mask = (kp0 < 0) || (kp0 + kTcKeys - 1 > ti.qa) ||
                              (local && kp0 < ti.qz - p.window + 1);
-      // pass 1: row max of the raw scores
-      float mx = -INFINITY;
+      // The whole S row (128 fp32) in registers: four loads in flight, one wait.
+      uint32_t v[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, v[c]);
+      tmem_wait_ld();
+      if (need_mask) {
+        // keys kp0 + j are visible for j in [jlo, jhi]; the rest become -inf
+        const int32_t jlo = max(max(wlo, 0), kp0) - kp0;
+        const int32_t jhi = qp - kp0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int32_t jj = 32 * c + j;
+            v[c][j] = (jj < jlo || jj > jhi) ? 0xff800000u : v[c][j];
+          }
+      }
+      float mx4[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + 32 * c, v);
-        tmem_wait_ld();
+        float a = __uint_as_float(v[c][0]), b2 = __uint_as_float(v[c][1]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int32_t kp = kp0 + 32 * c + j;
-          const bool keep = !need_mask || (kp >= 0 && kp <= qp && kp >= wlo);
-          if (keep) mx = fmaxf(mx, __uint_as_float(v[j]));
+        for (int j = 2; j < 32; j += 2) {
+          a = fmaxf(a, __uint_as_float(v[c][j]));
+          b2 = fmaxf(b2, __uint_as_float(v[c][j + 1]));
         }
+        mx4[c] = fmaxf(a, b2);
       }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float mt = mx * sl2;  // scale > 0, so it commutes with max
       float alpha = 1.f;
       if (mt > mrow + kRescaleThreshold || (mrow == -INFINITY && mt != -INFINITY)) {
@@ -307,39 +325,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mrow = mt;
       }
       lrow *= alpha;
-      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + 32 * c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-          tmem_st32(tO + 32 * c, v);
-        }
-        tmem_wait_st();
-      }
       const float muse = (mrow == -INFINITY) ? 0.f : mrow;
-      // pass 2: P = 2^(s*scale*log2e - m), packed to bf16 over S's first half
+      // P = 2^(s*scale*log2e - m), packed to bf16 over the first half of S
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + 32 * c, v);
-        tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          const int32_t kp = kp0 + 32 * c + j;
-          float e0 = fast_exp2(fmaf(__uint_as_float(v[j]), sl2, -muse));
-          float e1 = fast_exp2(fmaf(__uint_as_float(v[j + 1]), sl2, -muse));
-          if (need_mask) {
-            if (!(kp >= 0 && kp <= qp && kp >= wlo)) e0 = 0.f;
-            if (!(kp + 1 >= 0 && kp + 1 <= qp && kp + 1 >= wlo)) e1 = 0.f;
-          }
-          lrow += e0 + e1;
+          const float e0 = fast_exp2(fmaf(__uint_as_float(v[c][j]), sl2, -muse));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(v[c][j + 1]), sl2, -muse));
+          ls[(j >> 1) & 3] += e0 + e1;
           pk[j >> 1] = pack_bf16x2(e0, e1);
         }
         tmem_st16(tS + 16 * c, pk);
+      }
+      lrow += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // Rare: the running max grew by more than 2^8 -- rescale O in TMEM.  O
+      // is stable here (its last update was committed before this S tile)
+      // and the next P.V waits for this warp's arrival below.
+      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o32[32];
+          tmem_ld32(tO + 32 * c, o32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o32[j] = __float_as_uint(__uint_as_float(o32[j]) * alpha);
+          tmem_st32(tO + 32 * c, o32);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -424,8 +438,7 @@ cudaError_t launch_attn_tc(const TcParams &p, const CUtensorMap &tq, const CUten
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(attn_tc_kernel), kTcSmem, 1);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.qblocks * p.splits), kHkv, static_cast<unsigned>(p.batch));
-  attn_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(p, tq, tka, tva, tkb, tvb);
-  return cudaGetLastError();
+  return launch_pdl(attn_tc_kernel, grid, dim3(kTcThreads), kTcSmem, s, p, tq, tka, tva, tkb, tvb);
 }
 
 }  // namespace mg

@@ -11,6 +11,8 @@
 namespace mg {
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  pdl_wait();  // positions and rows may come from the previous kernel
+  pdl_launch_dependents();
   const int b = blockIdx.y;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = static_cast<int64_t>(p.n) * (kHkv * 16);
@@ -51,8 +53,7 @@ cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s) {
   const int64_t blocks = (total + 255) / 256;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(p.batch));
-  kv_append_kernel<<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, grid, dim3(256), 0, s, p);
 }
 
 }  // namespace mg

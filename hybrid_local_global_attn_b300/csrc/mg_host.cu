@@ -120,6 +120,8 @@ cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id) {
   std::lock_guard<std::mutex> lk(mu);
   if (done[kernel_id] & (1ull << dev)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && kernel_id == 2)  // the local decode kernel runs 16-CTA clusters
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[kernel_id] |= 1ull << dev;
   return e;
 }
@@ -137,6 +139,10 @@ RopeTurns rope_turns(float theta) {
       const double w = std::pow(static_cast<double>(theta), -2.0 * i / 128.0);
       const double t = w / (2.0 * M_PI);  // turns per position, < 1
       last.turn[i] = static_cast<uint64_t>(std::ldexp(t, 64));
+      for (int k = 0; k < 6; ++k) {
+        const double a = static_cast<double>(kRopeSteps[k]) * w;
+        last.step[k][i] = make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+      }
     }
     last_theta = theta;
   }
@@ -199,12 +205,17 @@ bool ws_layout(int32_t op, const mg_layer *L, int32_t batch, int32_t n, int32_t 
   const bool local = L->kind == MG_LOCAL;
   if (op == MG_OP_DECODE) {
     if (n != 1) return false;
-    w->splits = splits_decode(L->kind, batch, max_len);
-    const size_t rows = static_cast<size_t>(batch) * kHq;
-    w->part_o = off;
-    off = align256(off + rows * w->splits * kD * sizeof(float));
-    w->part_lse = off;
-    off = align256(off + rows * w->splits * sizeof(float));
+    if (local) {
+      // one cluster per (sequence, KV head) merges in shared memory: no workspace
+      w->splits = kDecLocalSplits;
+    } else {
+      w->splits = splits_decode(L->kind, batch, max_len);
+      const size_t rows = static_cast<size_t>(batch) * kHq;
+      w->part_o = off;
+      off = align256(off + rows * w->splits * kD * sizeof(float));
+      w->part_lse = off;
+      off = align256(off + rows * w->splits * sizeof(float));
+    }
   } else if (op == MG_OP_VERIFY || op == MG_OP_PREFILL) {
     if (op == MG_OP_VERIFY && n > MG_VERIFY_MAX) return false;
     w->splits = op == MG_OP_VERIFY ? splits_verify(L->kind, batch, max_len) : 1;
@@ -304,20 +315,22 @@ int mg_kv_append(const mg_layer *layer, const mg_cache *cache, const int32_t *d_
   return launch_status(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
 }
 
-int mg_attn_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
-                   int32_t max_len, const void *q, void *o, void *ws, size_t ws_bytes,
-                   uint32_t *d_err, void *stream) {
+static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
+                       int32_t max_len, const void *q, const void *k_new, const void *v_new,
+                       void *o, void *ws, size_t ws_bytes, uint32_t *d_err, void *stream) {
   int st = check_layer(layer);
   if (st != MG_OK) return st;
   if ((st = check_cache(layer, cache)) != MG_OK) return st;
   if (d_pos == nullptr || d_err == nullptr || q == nullptr || o == nullptr) return MG_ERR_INVALID;
   if (!aligned16(q) || !aligned16(o)) return MG_ERR_INVALID;
+  if ((k_new == nullptr) != (v_new == nullptr)) return MG_ERR_INVALID;
+  if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return MG_ERR_INVALID;
   if (max_len < 1) return MG_ERR_INVALID;
   if (layer->kind == MG_GLOBAL && max_len > cache->slots) return MG_ERR_CAPACITY;
   WsLayout w;
   if (!ws_layout(MG_OP_DECODE, layer, cache->batch, 1, max_len, &w)) return MG_ERR_INVALID;
   if (ws_bytes < w.total || (w.total > 0 && ws == nullptr)) return MG_ERR_WORKSPACE;
-  if (!aligned16(ws)) return MG_ERR_INVALID;
+  if (w.total > 0 && !aligned16(ws)) return MG_ERR_INVALID;
   CUtensorMap tk, tv;
   const uint64_t outer = static_cast<uint64_t>(cache->batch) * kHkv;
   if (!map_rows(&tk, cache->k, cache->slots, outer, kDecTile) ||
@@ -326,8 +339,14 @@ int mg_attn_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *
   DecodeParams p;
   p.pos = d_pos;
   p.q = static_cast<const __nv_bfloat16 *>(q);
-  p.part_o = at<float>(ws, w.part_o);
-  p.part_lse = at<float>(ws, w.part_lse);
+  p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  p.k_cache = static_cast<__nv_bfloat16 *>(cache->k);
+  p.v_cache = static_cast<__nv_bfloat16 *>(cache->v);
+  const bool local = layer->kind == MG_LOCAL;
+  p.part_o = local ? nullptr : at<float>(ws, w.part_o);
+  p.part_lse = local ? nullptr : at<float>(ws, w.part_lse);
+  p.o = static_cast<__nv_bfloat16 *>(o);
   p.err = d_err;
   p.batch = cache->batch;
   p.slots = cache->slots;
@@ -335,10 +354,11 @@ int mg_attn_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *
   p.splits = w.splits;
   p.max_len = max_len;
   p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
-  p.rope = rope_turns(layer->kind == MG_LOCAL ? layer->rope_theta : 10000.f);
+  p.rope = rope_turns(local ? layer->rope_theta : 10000.f);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_decode(p, tk, tv, s);
   if (e != cudaSuccess) return MG_ERR_CUDA;
+  if (local) return MG_OK;  // the cluster wrote o itself
   CombineParams c;
   c.part_o = p.part_o;
   c.part_lse = p.part_lse;
@@ -346,6 +366,21 @@ int mg_attn_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *
   c.rows = cache->batch * kHq;
   c.splits = w.splits;
   return launch_status(launch_combine(c, s));
+}
+
+int mg_attn_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
+                   int32_t max_len, const void *q, void *o, void *ws, size_t ws_bytes,
+                   uint32_t *d_err, void *stream) {
+  return decode_impl(layer, cache, d_pos, max_len, q, nullptr, nullptr, o, ws, ws_bytes, d_err,
+                     stream);
+}
+
+int mg_append_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
+                     int32_t max_len, const void *q, const void *k_new, const void *v_new, void *o,
+                     void *ws, size_t ws_bytes, uint32_t *d_err, void *stream) {
+  if (k_new == nullptr || v_new == nullptr) return MG_ERR_INVALID;
+  return decode_impl(layer, cache, d_pos, max_len, q, k_new, v_new, o, ws, ws_bytes, d_err,
+                     stream);
 }
 
 }  // extern "C"

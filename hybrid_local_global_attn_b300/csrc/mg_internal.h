@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "mg.h"
 
 namespace mg {
@@ -32,6 +34,7 @@ constexpr int kDecStageBytes = 2 * kDecTile * kRowBytes;  // K + V
 constexpr int kDecSmem = kDecStages * kDecStageBytes + 1024 /*align*/ + 256 /*barriers*/ +
                          64 * 8 /*rope turns*/;
 constexpr int kDecMaxSplits = 296;
+constexpr int kDecLocalSplits = 16;  // one 16-CTA cluster per (sequence, KV head)
 
 // tcgen05 attention (verify + prefill): 2 query tiles of 128 rows
 // (8 positions x 16 heads each), key tiles of 128.
@@ -48,7 +51,12 @@ constexpr int kTcMaxSplits = 160;
 
 struct RopeTurns {
   uint64_t turn[64];  // w_i / (2 pi) in 0.64 fixed point, w_i = theta^(-2i/128)
+  // (cos, sin) of d * w_i for the key-position steps d a decode thread takes
+  // between its keys: d = 8, 64, 72, and the same minus 2048 (across the
+  // ring's wrap point), computed in double on the host.
+  float2 step[6][64];
 };
+constexpr int kRopeSteps[6] = {8, 64, 72, 8 - kWindow, 64 - kWindow, 72 - kWindow};
 
 struct AppendParams {
   const __nv_bfloat16 *k_new, *v_new;  // [B][n][2][128]
@@ -61,8 +69,14 @@ struct AppendParams {
 struct DecodeParams {
   const int32_t *pos;
   const __nv_bfloat16 *q;  // [B][32][128]
-  float *part_o;           // [B][32][splits][128]
+  // Optional fused append of the query token's own K/V ([B][1][2][128]):
+  // when k_new != nullptr the CTA whose split holds the token's slot writes
+  // it into the cache before reading that tile.
+  const __nv_bfloat16 *k_new, *v_new;
+  __nv_bfloat16 *k_cache, *v_cache;
+  float *part_o;           // [B][32][splits][128]  (global layers)
   float *part_lse;         // [B][32][splits]   (log2 domain)
+  __nv_bfloat16 *o;        // [B][32][128]: written directly by local layers
   uint32_t *err;
   int32_t batch, slots, kind, splits, max_len;
   float scale_log2;        // softmax scale * log2(e)
@@ -97,6 +111,26 @@ struct TcParams {
   int32_t batch, n, kind, window, staged, splits, qblocks, max_len, slots;
   float scale_log2;
 };
+
+// Launch with programmatic stream serialization, so the kernel may be
+// scheduled while the previous kernel in the stream drains; every kernel of
+// the library calls pdl_wait() before reading anything an earlier kernel
+// wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Sets the kernel's dynamic shared-memory limit once per device (so that no
 // attribute call happens while a stream is being captured into a graph).

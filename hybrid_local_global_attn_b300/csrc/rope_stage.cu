@@ -37,6 +37,8 @@ __device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, int32_t pos, int i
 }  // namespace
 
 __global__ void __launch_bounds__(256) rope_stage_kernel(const __grid_constant__ StageParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t n_kv = static_cast<int64_t>(p.batch) * kHkv * p.R * 8;
   const int64_t n_q = static_cast<int64_t>(p.batch) * p.n * kHq * 8;
@@ -95,8 +97,7 @@ cudaError_t launch_rope_stage(const StageParams &p, cudaStream_t s) {
   const int64_t blocks = (total + 255) / 256;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  rope_stage_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(rope_stage_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, p);
 }
 
 }  // namespace mg

@@ -55,9 +55,11 @@ lib.mg_layer_kind.argtypes = [_i32]
 lib.mg_layer_kind.restype = ctypes.c_int
 lib.mg_kv_append.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P]
 lib.mg_attn_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, _P, _P]
+lib.mg_append_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_verify.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_prefill.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
-for _f in (lib.mg_kv_append, lib.mg_attn_decode, lib.mg_attn_verify, lib.mg_attn_prefill):
+for _f in (lib.mg_kv_append, lib.mg_attn_decode, lib.mg_append_decode, lib.mg_attn_verify,
+           lib.mg_attn_prefill):
     _f.restype = ctypes.c_int
 
 
@@ -136,6 +138,14 @@ def mg_kv_append(layer, cache: KVCache, pos0, k_new, v_new, err, stream=None):
 def mg_attn_decode(layer, cache: KVCache, pos, max_len, q, o, ws, err, stream=None):
     _call(lib.mg_attn_decode, ctypes.byref(layer), ctypes.byref(cache.struct), _ptr(pos, torch.int32),
           int(max_len), _ptr(q, torch.bfloat16), _ptr(o, torch.bfloat16), _ptr(ws),
+          ws.numel() * ws.element_size() if ws is not None else 0, _ptr(err, torch.int32),
+          _stream(stream))
+
+
+def mg_append_decode(layer, cache: KVCache, pos, max_len, q, k_new, v_new, o, ws, err, stream=None):
+    _call(lib.mg_append_decode, ctypes.byref(layer), ctypes.byref(cache.struct),
+          _ptr(pos, torch.int32), int(max_len), _ptr(q, torch.bfloat16), _ptr(k_new, torch.bfloat16),
+          _ptr(v_new, torch.bfloat16), _ptr(o, torch.bfloat16), _ptr(ws),
           ws.numel() * ws.element_size() if ws is not None else 0, _ptr(err, torch.int32),
           _stream(stream))
 

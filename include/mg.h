@@ -153,6 +153,20 @@ int mg_attn_decode(const mg_layer *layer, const mg_cache *cache,
                    void *stream);
 
 /*
+ * Append + decode in one pass: the same result as mg_kv_append of the query
+ * token's own K/V (n = 1 at pos[b]) followed by mg_attn_decode, with the
+ * append folded into the decode kernel (the CTA that reads the token's slot
+ * writes it first).  Same arguments as mg_attn_decode plus
+ *   k_new, v_new : bf16 [batch][1][2][128] (device)
+ * Global layers flag a position >= slots (MG_DERR_POSITION) and skip it,
+ * as mg_kv_append does.
+ */
+int mg_append_decode(const mg_layer *layer, const mg_cache *cache,
+                     const int32_t *d_pos, int32_t max_len, const void *q,
+                     const void *k_new, const void *v_new, void *o, void *ws,
+                     size_t ws_bytes, uint32_t *d_err, void *stream);
+
+/*
  * Decode attention without a workspace argument, for callers that cannot
  * allocate device memory: for example a plugin inside a host framework that
  * owns every device buffer and gives plugins none, or a serving loop that

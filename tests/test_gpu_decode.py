@@ -81,11 +81,13 @@ def test_decode_position_beyond_max_len_is_flagged(mg):
     assert float(o[1].float().abs().max()) == 0.0
 
 
-def test_pr1_two_layer_decode_across_ring_wrap(mg):
+@pytest.mark.parametrize("fused", [False, True])
+def test_pr1_two_layer_decode_across_ring_wrap(mg, fused):
     """One local (window 2048, RoPE 1e4) and one global layer, batch 1, seed 0:
     cache pre-filled for positions 0..1999, then 256 single-token steps at
-    p = 2000..2255 (append, then decode), every output compared with the
-    oracle and both caches compared bit for bit after every step."""
+    p = 2000..2255 (append, then decode -- as two calls, or fused in
+    mg_append_decode), every output compared with the oracle and both caches
+    compared bit for bit after every step."""
     seed, P0, steps = 0, 2000, 256
     T = P0 + steps
     layers = [(0, 0), (1, 3)]  # (kind, layer index for the seed)
@@ -111,10 +113,14 @@ def test_pr1_two_layer_decode_across_ring_wrap(mg):
         p = P0 + i
         pos = torch.tensor([p], dtype=torch.int32, device="cuda")
         for s in state:
-            mg.mg_kv_append(s["lay"], s["cache"], pos, s["kd"][:, p:p + 1].contiguous(),
-                            s["vd"][:, p:p + 1].contiguous(), s["err"])
-            mg.mg_attn_decode(s["lay"], s["cache"], pos, T, s["qd"][:, i].contiguous(), o, s["ws"],
-                              s["err"])
+            kn, vn = s["kd"][:, p:p + 1].contiguous(), s["vd"][:, p:p + 1].contiguous()
+            if fused:
+                mg.mg_append_decode(s["lay"], s["cache"], pos, T, s["qd"][:, i].contiguous(), kn, vn,
+                                    o, s["ws"], s["err"])
+            else:
+                mg.mg_kv_append(s["lay"], s["cache"], pos, kn, vn, s["err"])
+                mg.mg_attn_decode(s["lay"], s["cache"], pos, T, s["qd"][:, i].contiguous(), o,
+                                  s["ws"], s["err"])
             orc.cache_append(oracle_kind(s["kind"]), s["exp_k"], s["exp_v"], p, s["k"][0, p:p + 1],
                              s["v"][0, p:p + 1])
             ref = orc.attention(s["olay"], s["k"][0, :p + 1], s["v"][0, :p + 1], [p], s["q"][:, i])[0]
@@ -124,3 +130,42 @@ def test_pr1_two_layer_decode_across_ring_wrap(mg):
             assert np.array_equal(bits_of(s["cache"].v[0]), s["exp_v"]), f"V cache step {i}"
     for s in state:
         check_err(s["err"])
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_append_decode_mixed_batch(mg, kind):
+    """Fused append + decode for a batch whose sequences sit at different
+    positions (some below the window, one right at the ring wrap)."""
+    positions = [5, 2047, 2048, 3001]
+    B = len(positions)
+    T = max(positions) + 1
+    k, v = synth.history(B, T, 9, 2 if kind == 0 else 3)
+    q = synth.queries(B, 1, 9, 2 if kind == 0 else 3)[:, 0]
+    # cache holding positions < p_b (ring: the last 2048 of them)
+    cache = mg.KVCache(kind, B, T)
+    lay = mg.make_layer(kind)
+    err = mg.error_word()
+    for b, p in enumerate(positions):
+        lo = max(0, p - 2048) if kind == 0 else 0
+        one = mg.KVCache(kind, 1, T)
+        mg.mg_kv_append(lay, one, torch.tensor([lo], dtype=torch.int32, device="cuda"),
+                        k[b:b + 1, lo:p].cuda().contiguous(), v[b:b + 1, lo:p].cuda().contiguous(), err)
+        cache.k[b].copy_(one.k[0])
+        cache.v[b].copy_(one.v[0])
+    kn = torch.stack([k[b, p:p + 1] for b, p in enumerate(positions)]).cuda().contiguous()
+    vn = torch.stack([v[b, p:p + 1] for b, p in enumerate(positions)]).cuda().contiguous()
+    ws = mg.workspace(mg.OP_DECODE, lay, B, 1, T)
+    o = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    mg.mg_append_decode(lay, cache, torch.tensor(positions, dtype=torch.int32, device="cuda"), T,
+                        q.cuda().contiguous(), kn, vn, o, ws, err)
+    torch.cuda.synchronize()
+    check_err(err)
+    olay = orc.layer(oracle_kind(kind))
+    for b, p in enumerate(positions):
+        ref = orc.attention(olay, k[b, :p + 1], v[b, :p + 1], [p], q[b:b + 1])[0]
+        compare(o[b], ref, f"kind {kind} b {b} p {p}")
+        lo = max(0, p - 2047) if kind == 0 else 0
+        kc, vc = cache_expected(kind, cache.slots, k[b], v[b], [(lo, p + 1 - lo)])
+        # slots never written stay zero on both sides
+        assert np.array_equal(bits_of(cache.k[b]), kc), f"K cache b {b}"
+        assert np.array_equal(bits_of(cache.v[b]), vc), f"V cache b {b}"
