@@ -42,6 +42,24 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+def max_over_ranks(x, device, world):
+    """Largest value of x over all ranks: the job takes as long as its
+    slowest rank.  world == 1 returns x unchanged."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, seconds, world):
+    """Whole-job throughput: every rank processes units_per_rank (weak
+    scaling, independent replicas) within the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -417,14 +435,10 @@ def run_gpu(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = clk.stop()
-    dec_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([dec_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dec_ms = float(t.item())
+    dec_ms = max_over_ranks(e0.elapsed_time(e1), dev, world)
     dec_bytes = sum(decode_layer_bytes(kinds[l], PROMPT + i) for i in range(W, W + K)
                     for l in range(N_LAYERS))
-    gbs = dec_bytes * world / (dec_ms / 1e3) / 1e9
+    gbs = job_throughput(dec_bytes, dec_ms / 1e3, world) / 1e9
     assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after decode"
     log(f"decode: {dec_ms / K * 1e3:.1f} us/step, {gbs:.1f} GB/s, clocks {clocks}")
 
@@ -473,14 +487,10 @@ def run_gpu(args, rank, world):
         g_dec.replay()
         h_o.copy_(o_cur, non_blocking=True)
         torch.cuda.current_stream().synchronize()
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev, world)
     e2e_bytes = sum(decode_layer_bytes(kinds[l], PROMPT + i) for i in range(W + K, W + K + ee)
                     for l in range(N_LAYERS))
-    e2e_gbs = e2e_bytes * world / e2e_s / 1e9
+    e2e_gbs = job_throughput(e2e_bytes, e2e_s, world) / 1e9
     h2d = 4 + N_LAYERS * (32 * 128 * 2 + 2 * 2 * 128 * 2)
     d2h = N_LAYERS * 32 * 128 * 2
     assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after e2e"
