@@ -72,11 +72,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t bar_q = sBar;
   const uint32_t bar_kf = sBar + 8;                        // [2]
   const uint32_t bar_vf = bar_kf + 8 * kTcStages;          // [2]
-  const uint32_t bar_ke = bar_vf + 8 * kTcStages;          // [2] stage empty
-  const uint32_t bar_s = bar_ke + 8 * kTcStages;           // [2] S ready (A, B)
+  const uint32_t bar_ke = bar_vf + 8 * kTcStages;          // [2] K stage free
+  const uint32_t bar_ve = bar_ke + 8 * kTcStages;          // [2] V stage free
+  const uint32_t bar_s = bar_ve + 8 * kTcStages;           // [2] S ready (A, B)
   const uint32_t bar_p = bar_s + 16;                       // [2] P ready
   const uint32_t bar_o = bar_p + 16;                       // [2] O final
   const uint32_t bar_done = bar_o + 16;                    // all MMAs retired
+  const uint32_t bar_turn = bar_done + 8;                  // [2] softmax turn of tile A / B
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y, b = blockIdx.z;
@@ -117,6 +119,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar_kf + 8 * i, 1);
       mbar_init(bar_vf + 8 * i, 1);
       mbar_init(bar_ke + 8 * i, 1);
+      mbar_init(bar_ve + 8 * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s + 8 * i, 1);
@@ -124,6 +127,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar_o + 8 * i, 1);
     }
     mbar_init(bar_done, 1);
+    mbar_init(bar_turn, 128);      // tile A may start: the 128 threads of B arrive
+    mbar_init(bar_turn + 8, 128);  // tile B may start: the 128 threads of A arrive
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -154,6 +159,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int st = t % kTcStages;
+        // K of tile t reuses the stage of tile t-2 once both tiles' S = Q K^T
+        // of it have run; V waits for both P.V instead
         if (t >= kTcStages &&
             !mbar_wait(bar_ke + 8 * st, ((t / kTcStages) - 1) & 1, &abort_flag)) {
           abort_flag = 1;
@@ -164,30 +171,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t dk = sKV + st * 2 * kTcTileBytes;
         const uint32_t dv = dk + kTcTileBytes;
         const bool from_cache = t < ti.ncache;
-        mbar_arrive_expect_tx(bar_kf + 8 * st, kTcTileBytes);
-        mbar_arrive_expect_tx(bar_vf + 8 * st, kTcTileBytes);
-        if (p.staged) {
-          const int32_t row = kp0 - ti.c0 + kWindow;
-          for (int x = 0; x < 2; ++x)
-            tma_load_3d(dk + x * (kTcTileBytes / 2), &tka, bar_kf + 8 * st, 64 * x, row,
-                        b * kHkv + g);
-          for (int x = 0; x < 2; ++x)
-            tma_load_3d(dv + x * (kTcTileBytes / 2), &tva, bar_vf + 8 * st, 64 * x, row,
-                        b * kHkv + g);
-        } else if (from_cache) {
-          for (int x = 0; x < 2; ++x)
-            tma_load_3d(dk + x * (kTcTileBytes / 2), &tka, bar_kf + 8 * st, 64 * x, kp0,
-                        b * kHkv + g);
-          for (int x = 0; x < 2; ++x)
-            tma_load_3d(dv + x * (kTcTileBytes / 2), &tva, bar_vf + 8 * st, 64 * x, kp0,
-                        b * kHkv + g);
-        } else {
-          const int32_t row = kp0 - ti.c0;
-          for (int x = 0; x < 2; ++x)
-            tma_load_4d(dk + x * (kTcTileBytes / 2), &tkb, bar_kf + 8 * st, 64 * x, g, row, b);
-          for (int x = 0; x < 2; ++x)
-            tma_load_4d(dv + x * (kTcTileBytes / 2), &tvb, bar_vf + 8 * st, 64 * x, g, row, b);
+        // one 128-key tile of K (dst dk, barrier kf) or V (dv, vf)
+        auto load_tile = [&](bool is_v) {
+          const uint32_t dst = is_v ? dv : dk;
+          const uint32_t fb = (is_v ? bar_vf : bar_kf) + 8 * st;
+          const CUtensorMap *ma = is_v ? &tva : &tka;
+          const CUtensorMap *mb = is_v ? &tvb : &tkb;
+          mbar_arrive_expect_tx(fb, kTcTileBytes);
+          for (int x = 0; x < 2; ++x) {
+            const uint32_t d = dst + x * (kTcTileBytes / 2);
+            if (p.staged)
+              tma_load_3d(d, ma, fb, 64 * x, kp0 - ti.c0 + kWindow, b * kHkv + g);
+            else if (from_cache)
+              tma_load_3d(d, ma, fb, 64 * x, kp0, b * kHkv + g);
+            else
+              tma_load_4d(d, mb, fb, 64 * x, g, kp0 - ti.c0, b);
+          }
+        };
+        load_tile(false);
+        if (t >= kTcStages &&
+            !mbar_wait(bar_ve + 8 * st, ((t / kTcStages) - 1) & 1, &abort_flag)) {
+          abort_flag = 1;
+          set_err(p.err, MG_DERR_TIMEOUT);
+          ++issued;  // the K copy of this tile is in flight
+          break;
         }
+        load_tile(true);
         ++issued;
       }
       // no copies may be in flight when the CTA retires
@@ -222,37 +231,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  kIdescPV, (first && kk == 0) ? 0u : 1u);
         }
       };
-      for (int t = 0; ok && t <= ntiles; ++t) {
-        const int st = t % kTcStages;
-        const int pst = (t + kTcStages - 1) % kTcStages;  // stage of tile t-1
-        if (t < ntiles) {
-          ok = mbar_wait(bar_kf + 8 * st, (t / kTcStages) & 1, &abort_flag);
-          if (!ok) break;
+      // Step k of query tile m issues O_m += P_m(k-1) V(k-1) (k > 0) and then
+      // S_m = Q_m K(k)^T (k < ntiles).  The two tiles advance independently:
+      // whichever tile's P is ready goes first, so one slow softmax does not
+      // hold back the other tile's MMAs.  A K/V stage is released after both
+      // tiles have issued their P.V on it.
+      int step[2] = {0, 0};
+      uint64_t idle_since = 0;
+      while (ok && (step[0] <= ntiles || step[1] <= ntiles)) {
+        bool progressed = false;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int k = step[m];
+          if (k > ntiles) continue;
+          const int st = k % kTcStages;
+          const int pst = (k + kTcStages - 1) % kTcStages;  // stage of tile k-1
+          if (k < ntiles && !mbar_test(bar_kf + 8 * st, (k / kTcStages) & 1)) continue;
+          if (k > 0 && !(mbar_test(bar_p + 8 * m, (k - 1) & 1) &&
+                         mbar_test(bar_vf + 8 * pst, ((k - 1) / kTcStages) & 1)))
+            continue;
           tc_fence_after();
+          if (k > 0) {
+            pv(m, pst, k == 1);
+            if (k == ntiles) mma_commit(bar_o + 8 * m);
+            if (step[1 - m] > k) mma_commit(bar_ve + 8 * pst);  // both P.V(k-1) issued
+          }
+          if (k < ntiles) {
+            qk(m, st);
+            mma_commit(bar_s + 8 * m);
+            if (step[1 - m] > k) mma_commit(bar_ke + 8 * st);  // both Q K(k)^T issued
+          }
+          step[m] = k + 1;
+          progressed = true;
         }
-        if (t > 0) {
-          ok = mbar_wait(bar_p, (t - 1) & 1, &abort_flag) &&
-               mbar_wait(bar_vf + 8 * pst, ((t - 1) / kTcStages) & 1, &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          pv(0, pst, t == 1);
-          if (t == ntiles) mma_commit(bar_o);
-        }
-        if (t < ntiles) {
-          qk(0, st);
-          mma_commit(bar_s);
-        }
-        if (t > 0) {
-          ok = mbar_wait(bar_p + 8, (t - 1) & 1, &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          pv(1, pst, t == 1);
-          mma_commit(bar_ke + 8 * pst);
-          if (t == ntiles) mma_commit(bar_o + 8);
-        }
-        if (t < ntiles) {
-          qk(1, st);
-          mma_commit(bar_s + 8);
+        if (progressed) {
+          idle_since = 0;
+        } else {
+          const uint64_t now = global_ns();
+          if (idle_since == 0) idle_since = now;
+          if (abort_flag || now - idle_since > kWaitLimitNs) ok = false;
         }
       }
       if (!ok) {
@@ -280,8 +297,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
 
     for (int t = 0; t < ntiles; ++t) {
+      // The two tiles' softmax passes take turns (A(t), B(t), A(t+1), ...):
+      // run side by side they slow each other down and then leave the tensor
+      // core with both tiles' MMAs at once; in turn, one tile's softmax
+      // overlaps the other tile's MMAs.
+      const bool my_turn = (m == 0) ? (t == 0 || mbar_wait(bar_turn, (t - 1) & 1, &abort_flag))
+                                    : mbar_wait(bar_turn + 8, t & 1, &abort_flag);
       // tcgen05.ld/st below are warp-collective: the whole warp goes on or stops
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_s + 8 * m, t & 1, &abort_flag))) {
+      if (!__all_sync(0xffffffffu, my_turn && mbar_wait(bar_s + 8 * m, t & 1, &abort_flag))) {
         ok = false;
         break;
       }
@@ -358,6 +381,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_p + 8 * m);
+      mbar_arrive(bar_turn + 8 * (1 - m));  // the other tile's turn
     }
 
     // ----------------------------------------------------------- epilogue ----
