@@ -157,6 +157,20 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<kLocal>::kMinBlocks)
   if (warp == kDecWarps && lane == 0) {
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
+    // Warm L2 with the first tiles this CTA will stream while the previous
+    // kernel is still running.  The range is what the split gets when the
+    // query sits at max_len - 1 (local: fixed 128-slot pieces); only a
+    // prefetch -- the loads that feed the math come after pdl_wait().
+    int32_t c = kLocal ? kWindow / kDecLocalSplits : (p.max_len + p.splits - 1) / p.splits;
+    c = (c + kDecTile - 1) / kDecTile * kDecTile;
+    const int32_t first = split * c;
+    const int32_t upto = min(min(first + (kLocal ? c : kDecPrefetchTiles * kDecTile), first + c),
+                             kLocal ? p.slots : min(p.max_len, p.slots));
+    for (int32_t row = first; row < upto; row += kDecTile)
+      for (int x = 0; x < 2; ++x) {
+        tma_prefetch_l2_3d(&tk, 64 * x, row, b * kHkv + g);
+        tma_prefetch_l2_3d(&tv, 64 * x, row, b * kHkv + g);
+      }
   }
   __syncthreads();
   // First half of a cluster barrier whose wait (before the first store into

@@ -34,6 +34,7 @@ constexpr int kDecStageBytes = 2 * kDecTile * kRowBytes;  // K + V
 constexpr int kDecSmem = kDecStages * kDecStageBytes + 1024 /*align*/ + 256 /*barriers*/ +
                          64 * 8 /*rope turns*/;
 constexpr int kDecMaxSplits = 296;
+constexpr int kDecPrefetchTiles = 8;  // L2-prefetched tiles per global-layer CTA
 constexpr int kDecLocalSplits = 16;  // one 16-CTA cluster per (sequence, KV head)
 
 // tcgen05 attention (verify + prefill): 2 query tiles of 128 rows
