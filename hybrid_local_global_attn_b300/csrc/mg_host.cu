@@ -129,17 +129,25 @@ cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id) {
 namespace {
 
 // ---------------------------------------------------------------- RoPE ----
-RopeTurns rope_turns(float theta) {
+// w_i = theta^(-2i/128) as 0.64 fixed-point turns per position, and the
+// (cos, sin) of the slot steps the local kernel takes between a thread's
+// keys, all from double precision.
+struct RopeTables {
+  uint64_t turn[64];
+  float2 step[3][64];
+};
+
+RopeTables rope_tables(float theta) {
   static std::mutex mu;
   static float last_theta = -1.f;
-  static RopeTurns last;
+  static RopeTables last;
   std::lock_guard<std::mutex> lk(mu);
   if (theta != last_theta) {
     for (int i = 0; i < 64; ++i) {
       const double w = std::pow(static_cast<double>(theta), -2.0 * i / 128.0);
       const double t = w / (2.0 * M_PI);  // turns per position, < 1
       last.turn[i] = static_cast<uint64_t>(std::ldexp(t, 64));
-      for (int k = 0; k < 6; ++k) {
+      for (int k = 0; k < 3; ++k) {
         const double a = static_cast<double>(kRopeSteps[k]) * w;
         last.step[k][i] = make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
       }
@@ -147,6 +155,13 @@ RopeTurns rope_turns(float theta) {
     last_theta = theta;
   }
   return last;
+}
+
+RopeTurns rope_turns(float theta) {
+  const RopeTables t = rope_tables(theta);
+  RopeTurns r;
+  std::memcpy(r.turn, t.turn, sizeof r.turn);
+  return r;
 }
 
 // ---------------------------------------------------------- validation ----
@@ -207,7 +222,7 @@ bool ws_layout(int32_t op, const mg_layer *L, int32_t batch, int32_t n, int32_t 
     if (n != 1) return false;
     if (local) {
       // one cluster per (sequence, KV head) merges in shared memory: no workspace
-      w->splits = kDecLocalSplits;
+      w->splits = kLocCluster;
     } else {
       w->splits = splits_decode(L->kind, batch, max_len);
       const size_t rows = static_cast<size_t>(batch) * kHq;
@@ -216,6 +231,10 @@ bool ws_layout(int32_t op, const mg_layer *L, int32_t batch, int32_t n, int32_t 
       w->part_lse = off;
       off = align256(off + rows * w->splits * sizeof(float));
     }
+  } else if (op == MG_OP_VERIFY && local) {
+    // the ring kernel: one cluster per (sequence, KV head, token), no workspace
+    if (n > MG_VERIFY_MAX) return false;
+    w->splits = kLocCluster;
   } else if (op == MG_OP_VERIFY || op == MG_OP_PREFILL) {
     if (op == MG_OP_VERIFY && n > MG_VERIFY_MAX) return false;
     w->splits = op == MG_OP_VERIFY ? splits_verify(L->kind, batch, max_len) : 1;
@@ -247,6 +266,32 @@ int launch_status(cudaError_t e) { return e == cudaSuccess ? MG_OK : MG_ERR_CUDA
 template <typename T>
 T *at(void *base, size_t off) {
   return reinterpret_cast<T *>(static_cast<uint8_t *>(base) + off);
+}
+
+// Local layers, decode and verify: the ring kernel, n query tokens per
+// sequence starting at d_pos; block rows (k_new, v_new) optional.
+cudaError_t launch_local(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
+                         int32_t n, int32_t max_len, const void *q, const void *k_new,
+                         const void *v_new, bool write_new, void *o, uint32_t *d_err,
+                         const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s) {
+  LocalParams p;
+  p.pos = d_pos;
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  p.k_cache = static_cast<__nv_bfloat16 *>(cache->k);
+  p.v_cache = static_cast<__nv_bfloat16 *>(cache->v);
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.err = d_err;
+  p.batch = cache->batch;
+  p.n = n;
+  p.max_len = max_len;
+  p.write_new = write_new ? 1 : 0;
+  p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
+  const RopeTables t = rope_tables(layer->rope_theta);
+  std::memcpy(p.turn, t.turn, sizeof p.turn);
+  std::memcpy(p.step, t.step, sizeof p.step);
+  return launch_local_attn(p, tk, tv, s);
 }
 
 }  // namespace
@@ -336,6 +381,10 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   if (!map_rows(&tk, cache->k, cache->slots, outer, kDecTile) ||
       !map_rows(&tv, cache->v, cache->slots, outer, kDecTile))
     return MG_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (layer->kind == MG_LOCAL)
+    return launch_status(launch_local(layer, cache, d_pos, 1, max_len, q, k_new, v_new,
+                                      k_new != nullptr, o, d_err, tk, tv, s));
   DecodeParams p;
   p.pos = d_pos;
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -343,22 +392,16 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
   p.k_cache = static_cast<__nv_bfloat16 *>(cache->k);
   p.v_cache = static_cast<__nv_bfloat16 *>(cache->v);
-  const bool local = layer->kind == MG_LOCAL;
-  p.part_o = local ? nullptr : at<float>(ws, w.part_o);
-  p.part_lse = local ? nullptr : at<float>(ws, w.part_lse);
-  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.part_o = at<float>(ws, w.part_o);
+  p.part_lse = at<float>(ws, w.part_lse);
   p.err = d_err;
   p.batch = cache->batch;
   p.slots = cache->slots;
-  p.kind = layer->kind;
   p.splits = w.splits;
   p.max_len = max_len;
   p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
-  p.rope = rope_turns(local ? layer->rope_theta : 10000.f);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_decode(p, tk, tv, s);
   if (e != cudaSuccess) return MG_ERR_CUDA;
-  if (local) return MG_OK;  // the cluster wrote o itself
   CombineParams c;
   c.part_o = p.part_o;
   c.part_lse = p.part_lse;
@@ -415,6 +458,14 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
   const bool local = layer->kind == MG_LOCAL;
   const uint64_t outer = static_cast<uint64_t>(B) * kHkv;
 
+  if (local && op == MG_OP_VERIFY) {
+    CUtensorMap tk, tv;
+    if (!map_rows(&tk, cache->k, cache->slots, outer, kDecTile) ||
+        !map_rows(&tv, cache->v, cache->slots, outer, kDecTile))
+      return MG_ERR_CUDA;
+    return launch_status(launch_local(layer, cache, d_pos0, n, max_len, q, k_new, v_new, false, o,
+                                      d_err, tk, tv, s));
+  }
   const void *qsrc = q;
   CUtensorMap tq, tka, tva, tkb, tvb;
   if (local) {

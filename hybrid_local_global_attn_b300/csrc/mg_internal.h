@@ -35,7 +35,12 @@ constexpr int kDecSmem = kDecStages * kDecStageBytes + 1024 /*align*/ + 256 /*ba
                          64 * 8 /*rope turns*/;
 constexpr int kDecMaxSplits = 296;
 constexpr int kDecPrefetchTiles = 8;  // L2-prefetched tiles per global-layer CTA
-constexpr int kDecLocalSplits = 16;  // one 16-CTA cluster per (sequence, KV head)
+
+// Local layers (ring attention for up to 16 query tokens): one 16-CTA cluster
+// per (sequence, KV head, group of query tokens), 128 ring slots per CTA.
+constexpr int kLocCluster = 16;
+constexpr int kMaxLocalTokens = 16;
+constexpr int kLocMaxTpc = 6;  // query tokens one CTA takes in turn
 
 // tcgen05 attention (verify + prefill): 2 query tiles of 128 rows
 // (8 positions x 16 heads each), key tiles of 128.
@@ -52,12 +57,9 @@ constexpr int kTcMaxSplits = 160;
 
 struct RopeTurns {
   uint64_t turn[64];  // w_i / (2 pi) in 0.64 fixed point, w_i = theta^(-2i/128)
-  // (cos, sin) of d * w_i for the key-position steps d a decode thread takes
-  // between its keys: d = 8, 64, 72, and the same minus 2048 (across the
-  // ring's wrap point), computed in double on the host.
-  float2 step[6][64];
 };
-constexpr int kRopeSteps[6] = {8, 64, 72, 8 - kWindow, 64 - kWindow, 72 - kWindow};
+// Slot steps between the keys one thread of the local kernel rotates.
+constexpr int kRopeSteps[3] = {8, 64, 72};
 
 struct AppendParams {
   const __nv_bfloat16 *k_new, *v_new;  // [B][n][2][128]
@@ -67,7 +69,7 @@ struct AppendParams {
   int32_t batch, n, slots, kind;
 };
 
-struct DecodeParams {
+struct DecodeParams {  // global layers
   const int32_t *pos;
   const __nv_bfloat16 *q;  // [B][32][128]
   // Optional fused append of the query token's own K/V ([B][1][2][128]):
@@ -75,13 +77,29 @@ struct DecodeParams {
   // it into the cache before reading that tile.
   const __nv_bfloat16 *k_new, *v_new;
   __nv_bfloat16 *k_cache, *v_cache;
-  float *part_o;           // [B][32][splits][128]  (global layers)
+  float *part_o;           // [B][32][splits][128]
   float *part_lse;         // [B][32][splits]   (log2 domain)
-  __nv_bfloat16 *o;        // [B][32][128]: written directly by local layers
   uint32_t *err;
-  int32_t batch, slots, kind, splits, max_len;
+  int32_t batch, slots, splits, max_len;
   float scale_log2;        // softmax scale * log2(e)
-  RopeTurns rope;
+};
+
+struct LocalParams {  // local layers, n <= kMaxLocalTokens query tokens
+  const int32_t *pos;  // [B]: position of query token 0
+  const __nv_bfloat16 *q;  // [B][n][32][128]
+  // The block's own K/V ([B][n][2][128]); query i sees tokens 0..i of it in
+  // place of the ring rows of their slots.  nullptr: the ring already holds
+  // every position the queries see (decode after mg_kv_append).
+  const __nv_bfloat16 *k_new, *v_new;
+  __nv_bfloat16 *k_cache, *v_cache;  // ring [B][2][2048][128]
+  __nv_bfloat16 *o;                  // [B][n][32][128]
+  uint32_t *err;
+  int32_t batch, n, max_len;
+  int32_t tpc;         // query tokens per CTA (1..kLocMaxTpc)
+  int32_t write_new;   // 1: also store the block rows into the ring (fused append, n == 1)
+  float scale_log2;
+  uint64_t turn[64];   // as in RopeTurns
+  float2 step[3][64];  // (cos, sin) of kRopeSteps[k] * w_i, from double
 };
 
 struct CombineParams {
@@ -141,6 +159,9 @@ cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id);
 cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                           cudaStream_t s);
+// picks p.tpc itself
+cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtensorMap &tv,
+                              cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 cudaError_t launch_rope_stage(const StageParams &p, cudaStream_t s);
 cudaError_t launch_attn_tc(const TcParams &p, const CUtensorMap &tq, const CUtensorMap &tka,
