@@ -21,9 +21,9 @@
 //    b = p mod 2048.  Since R(p)^T R(j) = R(j - p), the score
 //    <R(p) q, R(j) k> equals <R(b) q, R(s) k> (s <= b) or
 //    <R(b + 2048) q, R(s) k> (s > b).  So keys are rotated by their slot's
-//    angle -- a table each CTA computes before the dependency wait, while
-//    the previous kernel is still running -- and each query is rotated
-//    twice, by R(b) and R(b + 2048).
+//    angle -- each thread computes the angles of its keys into registers
+//    before the dependency wait, while the previous kernel is still
+//    running -- and each query is rotated twice, by R(b) and R(b + 2048).
 //  * The draft block's own tokens (verify) are a separate 16-row tile
 //    handled by the cluster's first CTA: query p0+i scores block token
 //    k <= i as <R(i) q, R(k) k_k> (= <R(p0+i) q, R(p0+k) k_k>), and the
@@ -41,8 +41,9 @@
 //    memory once, by the first token.
 //  * Cluster merge: CTA r owns head r of the group; every CTA pushes its
 //    normalised partial row and its log-sum-exp for each query into the
-//    owner's shared memory (st.shared::cluster), and after one cluster
-//    barrier the owner writes the bf16 outputs.
+//    owner's shared memory with st.async, whose bytes complete on the
+//    owner's mbarrier; the owner merges as soon as its own inbox is full
+//    (no cluster-wide barrier at the end) and writes the bf16 outputs.
 #include <mutex>
 
 #include "mg_internal.h"
@@ -61,7 +62,6 @@ constexpr int kLocTiles = kPiece / kDecTile;      // 2 tiles of 64 slots
 constexpr int kBlk = kMaxLocalTokens;             // rows of the block tile
 constexpr int kTileSmem = kLocTiles * kDecStageBytes;  // K + V of the piece
 constexpr int kBlkSmem = 2 * kBlk * kRowBytes;         // K + V of the block
-constexpr int kTableSmem = 32 * kCons * 8;        // float2 per (entry, consumer thread)
 constexpr int kBlkTabSmem = kBlk * 64 * 8;        // (cos, sin) of k w_i, k < 16
 constexpr int kQRow = kD + 8;                     // padded bf16 row of a rotated query
 constexpr int kQRotSmem = 3 * kGroup * kQRow * 2;  // R(b) q, R(b + 2048) q, R(i) q
@@ -72,8 +72,7 @@ constexpr int kRedSmem = 2 * kLocWarps * kGroup * 4;
 constexpr int kConstSmem = 64 * 8 + 64 * 8;       // turns, step of 8 slots
 constexpr int kInboxPerToken = (kLocCluster * kD + kLocCluster) * 4;  // o rows, then lse
 constexpr int kOffBlk = kTileSmem;
-constexpr int kOffTable = kOffBlk + kBlkSmem;
-constexpr int kOffBlkTab = kOffTable + kTableSmem;
+constexpr int kOffBlkTab = kOffBlk + kBlkSmem;
 constexpr int kOffQRot = kOffBlkTab + kBlkTabSmem;
 constexpr int kOffP = kOffQRot + (kQRotSmem + 255) / 256 * 256;
 constexpr int kOffQAng = kOffP + (kPSmem + 255) / 256 * 256;
@@ -98,20 +97,42 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+// Remote store into another CTA's shared memory that completes its bytes on
+// that CTA's mbarrier (both addresses from mapa).
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "f"(a), "f"(b), "r"(bar)
+               : "memory");
 }
-__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr),
+               "f"(a), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred P;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, P;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (kWaitLimitNs) for phase `parity` of an mbarrier completed by
+// other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
 }
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -141,7 +162,6 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   __shared__ int abort_flag;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  float2 *table = reinterpret_cast<float2 *>(smem + kOffTable);
   float2 *blktab = reinterpret_cast<float2 *>(smem + kOffBlkTab);  // [16 k][64 freq]
   uint32_t *pmat = reinterpret_cast<uint32_t *>(smem + kOffP);  // [16 rows][kPRow/2] bf16 pairs
   float2 *qang = reinterpret_cast<float2 *>(smem + kOffQAng);  // [2 versions][64]
@@ -154,6 +174,7 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   const uint32_t blk_base = smem_base + kOffBlk;    // K box 0/1 (2 KB each), then V
   const uint32_t qrot_base = smem_base + kOffQRot;  // [3 versions][16 rows][kQRow] bf16
   const uint32_t bar_full = smem_u32(smem + kOffBars);  // 2 tiles
+  const uint32_t bar_inbox = bar_full + 8 * kLocTiles;   // the pushes into this CTA's inbox
 
   const int nq = (p.n + p.tpc - 1) / p.tpc;  // token groups per sequence
   const int g = blockIdx.y;
@@ -176,7 +197,10 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int t = 0; t < kLocTiles; ++t) mbar_init(bar_full + 8 * t, 1);
+    mbar_init(bar_inbox, 1);
     fence_mbar_init();
+    // every CTA of the cluster pushes one row and one lse per query token
+    mbar_arrive_expect_tx(bar_inbox, cnt * kInboxPerToken);
   }
   if (threadIdx.x < 64) {
     turns[threadIdx.x] = p.turn[threadIdx.x];
@@ -192,19 +216,19 @@ __global__ void __launch_bounds__(kLocThreads, 1)
       }
   }
   __syncthreads();
+  // Slot angles of this thread's 2 keys (slots sb and sb + 8) at its 16
+  // frequencies, kept in registers until the keys are rotated: entry
+  // 16 sel + f.
+  float2 tab[32];
   {
-    // Slot angles of this thread's 2 keys (slots sb and sb + 8) at its 16
-    // frequencies: entry (sel, f) at table[(16 sel + f) * kCons + tid].
     const int tid = threadIdx.x;
     const int32_t sb = s0 + th * kDecTile + ws * 16 + gr;
 #pragma unroll
     for (int f = 0; f < 16; ++f) {
       const int fr = freq_of(f, tq);
-      float2 a;
-      rope_cos_sin(sb, turns[fr], a.x, a.y);
+      rope_cos_sin(sb, turns[fr], tab[f].x, tab[f].y);
       const float2 r = step8[fr];
-      table[f * kCons + tid] = a;
-      table[(16 + f) * kCons + tid] = make_float2(a.x * r.x - a.y * r.y, a.y * r.x + a.x * r.y);
+      tab[16 + f] = make_float2(tab[f].x * r.x - tab[f].y * r.y, tab[f].y * r.x + tab[f].x * r.y);
     }
     if (blk_here) {  // R(k) for the block offsets k = 0..15
       for (int e = tid; e < kBlk * 64; e += kCons) {
@@ -412,8 +436,7 @@ __global__ void __launch_bounds__(kLocThreads, 1)
 #pragma unroll
                 for (int sel = 0; sel < 2; ++sel) {
                   const int j = 16 * sel + 4 * ks + 2 * h8;
-                  rot_pair(lo[ks][2 * sel + h8], hi[ks][2 * sel + h8], table[j * kCons + tid],
-                           table[(j + 1) * kCons + tid]);
+                  rot_pair(lo[ks][2 * sel + h8], hi[ks][2 * sel + h8], tab[j], tab[j + 1]);
                 }
               if (cnt > 1) {  // later queries read the rotated keys (this warp's own rows)
                 const uint32_t off = sw128(k_row, 2 * ks + k_chi);
@@ -598,18 +621,20 @@ __global__ void __launch_bounds__(kLocThreads, 1)
         }
       }
       // ------------ push this query's partial rows to the CTAs that own them ----
-      if (t == 0) cluster_wait();  // every CTA of the cluster runs
+      if (t == 0) cluster_wait();  // every CTA of the cluster runs, its inbox barrier is set
       const uint32_t box_s = inbox_s + t * kInboxPerToken;
+      const uint32_t bar0 = map_to_rank(bar_inbox, gr), bar1 = map_to_rank(bar_inbox, gr + 8);
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
         const int d = 16 * warp + 8 * n + 2 * tq;
-        st_cluster_f32x2(map_to_rank(box_s + 4 * (my_rank * kD + d), gr), oacc[n][0], oacc[n][1]);
-        st_cluster_f32x2(map_to_rank(box_s + 4 * (my_rank * kD + d), gr + 8), oacc[n][2],
-                         oacc[n][3]);
+        const uint32_t a = box_s + 4 * (my_rank * kD + d);
+        st_async_f32x2(map_to_rank(a, gr), oacc[n][0], oacc[n][1], bar0);
+        st_async_f32x2(map_to_rank(a, gr + 8), oacc[n][2], oacc[n][3], bar1);
       }
       if (warp == 0 && tq == 0) {
-        st_cluster_f32(map_to_rank(box_s + 4 * (kLocCluster * kD + my_rank), gr), lse0);
-        st_cluster_f32(map_to_rank(box_s + 4 * (kLocCluster * kD + my_rank), gr + 8), lse1);
+        const uint32_t a = box_s + 4 * (kLocCluster * kD + my_rank);
+        st_async_f32(map_to_rank(a, gr), lse0, bar0);
+        st_async_f32(map_to_rank(a, gr + 8), lse1, bar1);
       }
     }
     // never leave the CTA with copies in flight
@@ -621,8 +646,11 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   }
 
   // ------------- merge the rows this CTA owns (head my_rank of the group) ----
-  cluster_sync_all();  // all pushes have landed; no remote access after this
-  {
+  // Every push into this CTA has landed once its inbox barrier completes;
+  // the CTA reads and writes no other CTA's memory after its own pushes.
+  const bool all_in = mbar_wait_cluster(bar_inbox, 0);
+  if (!all_in && threadIdx.x == 0) set_err(p.err, MG_DERR_TIMEOUT);
+  if (all_in) {
     const int d = threadIdx.x & (kD - 1);
     for (int t = threadIdx.x >> 7; t < cnt; t += kCons / kD) {
       const float *box = inbox + t * (kInboxPerToken / 4);

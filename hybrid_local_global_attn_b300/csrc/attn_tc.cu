@@ -12,19 +12,24 @@
 // RoPE (local; operands pre-rotated by rope_stage) or [0, q] without RoPE
 // (global, operands read straight from the cache and the block).
 //
-// Tiling: a CTA owns 16 consecutive query positions of one KV group.  Their
-// 16 positions x 16 query heads form two M = 128 tiles (8 positions x 16
-// heads each, rows r = 16 * position + head), so every K/V tile loaded into
-// shared memory feeds 256 query rows.  Key tiles hold 128 keys and are aligned
-// to c0, so a tile never straddles the cache and the block.
+// Tiling: a CTA owns 8 consecutive query positions of one KV group: 8
+// positions x 16 query heads form one M = 128 tile (rows r = 16 * position +
+// head).  Key tiles hold 128 keys and are aligned to c0, so a tile never
+// straddles the cache and the block.
+//
+// Two softmax warpgroups take alternate key tiles (even / odd), each with its
+// own S and O in TMEM and its own running max and sum -- two independent
+// online softmaxes over interleaved halves of the keys, merged at the end.
+// So S = Q K^T of tile t + 2 only waits for P.V of tile t, not for the other
+// group's softmax, and the tensor core is fed while either group works.
 //
 // Warp roles (320 threads):
-//   warps 0-3  softmax of tile A (thread = one row = one TMEM lane)
-//   warps 4-7  softmax of tile B
-//   warp 8     TMA producer (Q once; K and V in a 2-deep ring)
+//   warps 0-3  softmax of even key tiles (thread = one row = one TMEM lane)
+//   warps 4-7  softmax of odd key tiles
+//   warp 8     TMA producer (Q once; K and V in a 3-deep ring)
 //   warp 9     TMEM owner and single-thread MMA issuer
-// TMEM (512 columns): S_A, S_B (fp32 128 cols each; P overwrites the first
-// 64 columns as packed bf16), O_A, O_B (fp32 128 cols each).
+// TMEM (512 columns): S_0, S_1 (fp32 128 cols each; P overwrites the first
+// 64 columns as packed bf16), O_0, O_1 (fp32 128 cols each).
 // Per key tile: S = Q K^T (M128 N128 K16 x 8), softmax in registers with a
 // lazily rescaled running max (rescale only when the max grows by more than
 // 2^8), P back to TMEM, O += P V (A from TMEM, V as an MN-major operand).
@@ -65,20 +70,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase;                        // 2 x 32 KB
-  const uint32_t sKV = sbase + 2 * kTcQBytes;       // stage s: K at +64K*s, V at +64K*s+32K
+  const uint32_t sQ = sbase;                        // 32 KB
+  const uint32_t sKV = sbase + kTcQBytes;           // stage s: K at +64K*s, V at +64K*s+32K
   const uint32_t sBar = sKV + kTcStages * 2 * kTcTileBytes;
   // barrier addresses
   const uint32_t bar_q = sBar;
-  const uint32_t bar_kf = sBar + 8;                        // [2]
-  const uint32_t bar_vf = bar_kf + 8 * kTcStages;          // [2]
-  const uint32_t bar_ke = bar_vf + 8 * kTcStages;          // [2] K stage free
-  const uint32_t bar_ve = bar_ke + 8 * kTcStages;          // [2] V stage free
-  const uint32_t bar_s = bar_ve + 8 * kTcStages;           // [2] S ready (A, B)
+  const uint32_t bar_kf = sBar + 8;                        // [3] K full
+  const uint32_t bar_vf = bar_kf + 8 * kTcStages;          // [3] V full
+  const uint32_t bar_ke = bar_vf + 8 * kTcStages;          // [3] K stage free
+  const uint32_t bar_ve = bar_ke + 8 * kTcStages;          // [3] V stage free
+  const uint32_t bar_s = bar_ve + 8 * kTcStages;           // [2] S ready (group 0, 1)
   const uint32_t bar_p = bar_s + 16;                       // [2] P ready
   const uint32_t bar_o = bar_p + 16;                       // [2] O final
   const uint32_t bar_done = bar_o + 16;                    // all MMAs retired
-  const uint32_t bar_turn = bar_done + 8;                  // [2] softmax turn of tile A / B
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y, b = blockIdx.z;
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
   const int ntiles = ti.ncache + ti.nnew;
+  const int n_grp[2] = {(ntiles + 1) / 2, ntiles / 2};  // key tiles of group 0 / 1
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -127,8 +132,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar_o + 8 * i, 1);
     }
     mbar_init(bar_done, 1);
-    mbar_init(bar_turn, 128);      // tile A may start: the 128 threads of B arrive
-    mbar_init(bar_turn + 8, 128);  // tile B may start: the 128 threads of A arrive
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -149,18 +152,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tkb);
       tma_prefetch_desc(&tvb);
       const int32_t q_t0 = kTcPosPerCta * qb;  // position index within the block
-      mbar_arrive_expect_tx(bar_q, 2 * kTcQBytes);
-      for (int m = 0; m < 2; ++m) {
-        for (int x = 0; x < 2; ++x) {
-          tma_load_4d(sQ + m * kTcQBytes + x * (kTcQBytes / 2), &tq, bar_q, 64 * x, kGroup * g,
-                      q_t0 + kTcPosPerTile * m, b);
-        }
-      }
+      mbar_arrive_expect_tx(bar_q, kTcQBytes);
+      for (int x = 0; x < 2; ++x)
+        tma_load_4d(sQ + x * (kTcQBytes / 2), &tq, bar_q, 64 * x, kGroup * g, q_t0, b);
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int st = t % kTcStages;
-        // K of tile t reuses the stage of tile t-2 once both tiles' S = Q K^T
-        // of it have run; V waits for both P.V instead
+        // K of tile t reuses the stage of tile t-3 once S = Q K^T of it has
+        // run; V waits for its P.V instead
         if (t >= kTcStages &&
             !mbar_wait(bar_ke + 8 * st, ((t / kTcStages) - 1) & 1, &abort_flag)) {
           abort_flag = 1;
@@ -209,68 +208,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer ----
     if (lane == 0 && ntiles > 0) {
-      const uint32_t tS[2] = {tbase, tbase + 128};
-      const uint32_t tO[2] = {tbase + 256, tbase + 384};
       bool ok = mbar_wait(bar_q, 0, &abort_flag);
       tc_fence_after();
-      auto qk = [&](int m, int st) {
-        const uint32_t qs = sQ + m * kTcQBytes;
+      // S_{t&1} = Q K(t)^T
+      auto qk = [&](int t) -> bool {
+        const int st = t % kTcStages;
+        if (!mbar_wait(bar_kf + 8 * st, (t / kTcStages) & 1, &abort_flag)) return false;
+        tc_fence_after();
         const uint32_t ks = sKV + st * 2 * kTcTileBytes;
+        const uint32_t tS = tbase + 128 * (t & 1);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32;
-          mma_ss(tS[m], smem_desc_sw128(qs + off, 16, 1024), smem_desc_sw128(ks + off, 16, 1024),
+          mma_ss(tS, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(ks + off, 16, 1024),
                  kIdescQK, kk > 0 ? 1u : 0u);
         }
+        mma_commit(bar_s + 8 * (t & 1));
+        mma_commit(bar_ke + 8 * st);
+        return true;
       };
-      auto pv = [&](int m, int st, bool first) {
+      // O_{t&1} += P(t) V(t), P from the first half of S_{t&1}
+      auto pv = [&](int t) -> bool {
+        const int st = t % kTcStages, e = t & 1;
+        if (!mbar_wait(bar_p + 8 * e, (t >> 1) & 1, &abort_flag)) return false;
+        if (!mbar_wait(bar_vf + 8 * st, (t / kTcStages) & 1, &abort_flag)) return false;
+        tc_fence_after();
         const uint32_t vs = sKV + st * 2 * kTcTileBytes + kTcTileBytes;
+        const uint32_t tS = tbase + 128 * e, tO = tbase + 256 + 128 * e;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tO[m], tS[m] + 8 * kk, smem_desc_sw128(vs + kk * 2048, kTcTileBytes / 2, 1024),
-                 kIdescPV, (first && kk == 0) ? 0u : 1u);
+          mma_ts(tO, tS + 8 * kk, smem_desc_sw128(vs + kk * 2048, kTcTileBytes / 2, 1024), kIdescPV,
+                 (t < 2 && kk == 0) ? 0u : 1u);
         }
+        mma_commit(bar_ve + 8 * st);
+        if (t + 2 >= ntiles) mma_commit(bar_o + 8 * e);  // the group's last tile
+        return true;
       };
-      // Step k of query tile m issues O_m += P_m(k-1) V(k-1) (k > 0) and then
-      // S_m = Q_m K(k)^T (k < ntiles).  The two tiles advance independently:
-      // whichever tile's P is ready goes first, so one slow softmax does not
-      // hold back the other tile's MMAs.  A K/V stage is released after both
-      // tiles have issued their P.V on it.
-      int step[2] = {0, 0};
-      uint64_t idle_since = 0;
-      while (ok && (step[0] <= ntiles || step[1] <= ntiles)) {
-        bool progressed = false;
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const int k = step[m];
-          if (k > ntiles) continue;
-          const int st = k % kTcStages;
-          const int pst = (k + kTcStages - 1) % kTcStages;  // stage of tile k-1
-          if (k < ntiles && !mbar_test(bar_kf + 8 * st, (k / kTcStages) & 1)) continue;
-          if (k > 0 && !(mbar_test(bar_p + 8 * m, (k - 1) & 1) &&
-                         mbar_test(bar_vf + 8 * pst, ((k - 1) / kTcStages) & 1)))
-            continue;
-          tc_fence_after();
-          if (k > 0) {
-            pv(m, pst, k == 1);
-            if (k == ntiles) mma_commit(bar_o + 8 * m);
-            if (step[1 - m] > k) mma_commit(bar_ve + 8 * pst);  // both P.V(k-1) issued
-          }
-          if (k < ntiles) {
-            qk(m, st);
-            mma_commit(bar_s + 8 * m);
-            if (step[1 - m] > k) mma_commit(bar_ke + 8 * st);  // both Q K(k)^T issued
-          }
-          step[m] = k + 1;
-          progressed = true;
-        }
-        if (progressed) {
-          idle_since = 0;
-        } else {
-          const uint64_t now = global_ns();
-          if (idle_since == 0) idle_since = now;
-          if (abort_flag || now - idle_since > kWaitLimitNs) ok = false;
-        }
+      // Issue order: S(0), S(1), then P.V(t) and S(t+2) for t = 0, 1, ...
+      // S(t+2) reuses the TMEM of S(t) = P(t), so it goes after P.V(t); the
+      // MMAs of one thread run in issue order.
+      ok = ok && qk(0);
+      if (ntiles > 1) ok = ok && qk(1);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        ok = pv(t);
+        if (ok && t + 2 < ntiles) ok = qk(t + 2);
       }
       if (!ok) {
         abort_flag = 1;
@@ -282,13 +263,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------- softmax warps ----
-    const int m = warp >> 2;                     // query tile 0 (A) or 1 (B)
+    const int e = warp >> 2;                     // group: even (0) or odd (1) key tiles
     const int r = (warp & 3) * 32 + lane;        // row = TMEM lane
     const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tbase + lane_bits + m * 128;
-    const uint32_t tO = tbase + lane_bits + 256 + m * 128;
-    const int32_t tloc = kTcPosPerCta * qb + kTcPosPerTile * m + (r >> 4);  // index in block
-    const int32_t qp = ti.qa + kTcPosPerTile * m + (r >> 4);  // this row's position
+    const uint32_t tS = tbase + lane_bits + 128 * e;
+    const uint32_t tO = tbase + lane_bits + 256 + 128 * e;
+    const int32_t tloc = kTcPosPerCta * qb + (r >> 4);  // index in block
+    const int32_t qp = ti.qa + (r >> 4);                // this row's position
     const int h = kGroup * g + (r & 15);
     const bool row_valid = tloc < p.n;  // rows past the block are padding
     const float sl2 = p.scale_log2;
@@ -296,15 +277,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float mrow = -INFINITY, lrow = 0.f;
     bool ok = true;
 
-    for (int t = 0; t < ntiles; ++t) {
-      // The two tiles' softmax passes take turns (A(t), B(t), A(t+1), ...):
-      // run side by side they slow each other down and then leave the tensor
-      // core with both tiles' MMAs at once; in turn, one tile's softmax
-      // overlaps the other tile's MMAs.
-      const bool my_turn = (m == 0) ? (t == 0 || mbar_wait(bar_turn, (t - 1) & 1, &abort_flag))
-                                    : mbar_wait(bar_turn + 8, t & 1, &abort_flag);
+    for (int u = 0; u < n_grp[e]; ++u) {
+      const int t = 2 * u + e;  // key tile
       // tcgen05.ld/st below are warp-collective: the whole warp goes on or stops
-      if (!__all_sync(0xffffffffu, my_turn && mbar_wait(bar_s + 8 * m, t & 1, &abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s + 8 * e, u & 1, &abort_flag))) {
         ok = false;
         break;
       }
@@ -329,16 +305,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             v[c][j] = (jj < jlo || jj > jhi) ? 0xff800000u : v[c][j];
           }
       }
+      // row max: three-input max, four independent chains
       float mx4[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float a = __uint_as_float(v[c][0]), b2 = __uint_as_float(v[c][1]);
+        float a = fmax3(__uint_as_float(v[c][0]), __uint_as_float(v[c][1]),
+                        __uint_as_float(v[c][2]));
 #pragma unroll
-        for (int j = 2; j < 32; j += 2) {
-          a = fmaxf(a, __uint_as_float(v[c][j]));
-          b2 = fmaxf(b2, __uint_as_float(v[c][j + 1]));
-        }
-        mx4[c] = fmaxf(a, b2);
+        for (int j = 3; j < 31; j += 2)
+          a = fmax3(a, __uint_as_float(v[c][j]), __uint_as_float(v[c][j + 1]));
+        mx4[c] = fmaxf(a, __uint_as_float(v[c][31]));
       }
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float mt = mx * sl2;  // scale > 0, so it commutes with max
@@ -349,25 +325,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       lrow *= alpha;
       const float muse = (mrow == -INFINITY) ? 0.f : mrow;
-      // P = 2^(s*scale*log2e - m), packed to bf16 over the first half of S
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(s*scale*log2e - m), packed to bf16 over the first half of S;
+      // the scaling and the row sum run as packed f32x2 operations
+      const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-muse, -muse);
+      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};  // (0.0f, 0.0f)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          const float e0 = fast_exp2(fmaf(__uint_as_float(v[c][j]), sl2, -muse));
-          const float e1 = fast_exp2(fmaf(__uint_as_float(v[c][j + 1]), sl2, -muse));
-          ls[(j >> 1) & 3] += e0 + e1;
+          const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(v[c][j]), __uint_as_float(v[c][j + 1])),
+                                        sc2, nm2);
+          float x0, x1;
+          f32x2_split(x2, x0, x1);
+          const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+          ls2[(j >> 1) & 3] = add_f32x2(ls2[(j >> 1) & 3], f32x2(e0, e1));
           pk[j >> 1] = pack_bf16x2(e0, e1);
         }
         tmem_st16(tS + 16 * c, pk);
       }
-      lrow += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      {
+        const uint64_t t2 = add_f32x2(add_f32x2(ls2[0], ls2[1]), add_f32x2(ls2[2], ls2[3]));
+        float a0, a1;
+        f32x2_split(t2, a0, a1);
+        lrow += a0 + a1;
+      }
       // Rare: the running max grew by more than 2^8 -- rescale O in TMEM.  O
-      // is stable here (its last update was committed before this S tile)
-      // and the next P.V waits for this warp's arrival below.
-      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // is stable here (this group's last P.V was issued before this S tile
+      // and has retired with it) and the next P.V waits for this warp's
+      // arrival below.
+      if (u > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o32[32];
@@ -380,71 +367,70 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_p + 8 * m);
-      mbar_arrive(bar_turn + 8 * (1 - m));  // the other tile's turn
+      mbar_arrive(bar_p + 8 * e);
     }
 
     // ----------------------------------------------------------- epilogue ----
-    if (ok && ntiles > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_o + 8 * m, 0, &abort_flag))) ok = false;
-      tc_fence_after();
-    }
-    if (!ok) {
-      abort_flag = 1;
-      set_err(p.err, MG_DERR_TIMEOUT);
-    }
-    const bool have = ok && ntiles > 0 && lrow > 0.f;
-    const float inv = have ? 1.f / lrow : 0.f;
+    // The two groups' states merge: O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1),
+    // f_e = 2^(m_e - M).  Group e finishes dims 64 e .. 64 e + 63 of its rows.
+    for (int k = 0; k < 2; ++k)
+      if (ok && n_grp[k] > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(bar_o + 8 * k, 0, &abort_flag)))
+        ok = false;
+    tc_fence_after();
+    // (m, l) of both groups, [group][m, l][row], over the Q tile: every MMA
+    // has retired once both groups' O are final
+    float *ml_x = reinterpret_cast<float *>(smem);
+    const bool have_mine = ok && n_grp[e] > 0 && lrow > 0.f;
+    ml_x[(2 * e + 0) * kTcRows + r] = have_mine ? mrow : -INFINITY;
+    ml_x[(2 * e + 1) * kTcRows + r] = have_mine ? lrow : 0.f;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    ok = __all_sync(0xffffffffu, ok && !abort_flag);  // warp-uniform: it gates tcgen05.ld
+    if (!ok && lane == 0) set_err(p.err, MG_DERR_TIMEOUT);
+    const float m0 = ml_x[0 * kTcRows + r], m1 = ml_x[2 * kTcRows + r];
+    const float M = fmaxf(m0, m1);
+    const float f0 = (ok && m0 != -INFINITY) ? fast_exp2(m0 - M) : 0.f;
+    const float f1 = (ok && m1 != -INFINITY) ? fast_exp2(m1 - M) : 0.f;
+    const float L = f0 * ml_x[1 * kTcRows + r] + f1 * ml_x[3 * kTcRows + r];
+    const bool have = ok && L > 0.f;
+    const float w0 = have ? f0 / L : 0.f, w1 = have ? f1 / L : 0.f;
     const size_t orow = (static_cast<size_t>(b) * p.n + tloc) * kHq + h;
-    if (p.splits == 1) {
+    const uint32_t tO0 = tbase + lane_bits + 256, tO1 = tbase + lane_bits + 384;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        if (ok && ntiles > 0) {
-          tmem_ld32(tO + 32 * c, v);
-          tmem_wait_ld();
-        }
-        if (row_valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD + 32 * c);
+    for (int c = 0; c < 2; ++c) {
+      const int d0 = 64 * e + 32 * c;  // first dim of this 32-column chunk
+      // tcgen05.ld is warp-collective: load on CTA-uniform conditions only
+      // (a group without key tiles never wrote its O; its weight is 0)
+      uint32_t a0[32], a1[32];
+      if (ok && n_grp[0] > 0) tmem_ld32(tO0 + d0, a0);
+      if (ok && n_grp[1] > 0) tmem_ld32(tO1 + d0, a1);
+      tmem_wait_ld();
+      float o[32];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(have ? __uint_as_float(v[8 * q4 + 0]) * inv : 0.f,
-                              have ? __uint_as_float(v[8 * q4 + 1]) * inv : 0.f);
-            w.y = pack_bf16x2(have ? __uint_as_float(v[8 * q4 + 2]) * inv : 0.f,
-                              have ? __uint_as_float(v[8 * q4 + 3]) * inv : 0.f);
-            w.z = pack_bf16x2(have ? __uint_as_float(v[8 * q4 + 4]) * inv : 0.f,
-                              have ? __uint_as_float(v[8 * q4 + 5]) * inv : 0.f);
-            w.w = pack_bf16x2(have ? __uint_as_float(v[8 * q4 + 6]) * inv : 0.f,
-                              have ? __uint_as_float(v[8 * q4 + 7]) * inv : 0.f);
-            dst[q4] = w;
-          }
+      for (int j = 0; j < 32; ++j)
+        o[j] = (w0 != 0.f ? __uint_as_float(a0[j]) * w0 : 0.f) +
+               (w1 != 0.f ? __uint_as_float(a1[j]) * w1 : 0.f);
+      if (!row_valid) continue;
+      if (p.splits == 1) {
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD + d0);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 w;
+          w.x = pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]);
+          w.y = pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]);
+          w.z = pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]);
+          w.w = pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]);
+          dst[q4] = w;
         }
+      } else {
+        float4 *dst = reinterpret_cast<float4 *>(p.part_o + (orow * p.splits + split) * kD + d0);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          dst[q4] = make_float4(o[4 * q4 + 0], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
       }
-    } else {
-      const size_t pr = orow * p.splits + split;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        if (ok && ntiles > 0) {
-          tmem_ld32(tO + 32 * c, v);
-          tmem_wait_ld();
-        }
-        if (row_valid) {
-          float4 *dst = reinterpret_cast<float4 *>(p.part_o + pr * kD + 32 * c);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            float4 w;
-            w.x = have ? __uint_as_float(v[4 * q4 + 0]) * inv : 0.f;
-            w.y = have ? __uint_as_float(v[4 * q4 + 1]) * inv : 0.f;
-            w.z = have ? __uint_as_float(v[4 * q4 + 2]) * inv : 0.f;
-            w.w = have ? __uint_as_float(v[4 * q4 + 3]) * inv : 0.f;
-            dst[q4] = w;
-          }
-        }
-      }
-      if (row_valid) p.part_lse[pr] = have ? mrow + __log2f(lrow) : -INFINITY;
     }
+    if (p.splits > 1 && row_valid && e == 0)
+      p.part_lse[orow * p.splits + split] = have ? M + __log2f(L) : -INFINITY;
   }
 
   __syncwarp();

@@ -196,10 +196,11 @@ int splits_decode(int32_t kind, int32_t batch, int32_t max_len) {
   return static_cast<int>(std::min<int64_t>(s, kDecMaxSplits));
 }
 
-int splits_verify(int32_t kind, int32_t batch, int32_t max_len) {
+int splits_verify(int32_t kind, int32_t batch, int32_t n, int32_t max_len) {
   const int64_t keys = kind == MG_LOCAL ? std::min<int64_t>(max_len, kWindow) : max_len;
   const int64_t tiles = (keys + kTcKeys - 1) / kTcKeys;
-  int64_t s = kNumSms / (static_cast<int64_t>(batch) * kHkv);
+  const int64_t qblocks = (n + kTcPosPerCta - 1) / kTcPosPerCta;
+  int64_t s = kNumSms / (static_cast<int64_t>(batch) * kHkv * qblocks);
   s = std::max<int64_t>(1, std::min<int64_t>(s, tiles));
   return static_cast<int>(std::min<int64_t>(s, kTcMaxSplits));
 }
@@ -237,7 +238,7 @@ bool ws_layout(int32_t op, const mg_layer *L, int32_t batch, int32_t n, int32_t 
     w->splits = kLocCluster;
   } else if (op == MG_OP_VERIFY || op == MG_OP_PREFILL) {
     if (op == MG_OP_VERIFY && n > MG_VERIFY_MAX) return false;
-    w->splits = op == MG_OP_VERIFY ? splits_verify(L->kind, batch, max_len) : 1;
+    w->splits = op == MG_OP_VERIFY ? splits_verify(L->kind, batch, n, max_len) : 1;
     if (w->splits > 1) {
       const size_t rows = static_cast<size_t>(batch) * n * kHq;
       w->part_o = off;

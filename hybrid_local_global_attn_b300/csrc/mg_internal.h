@@ -42,17 +42,17 @@ constexpr int kLocCluster = 16;
 constexpr int kMaxLocalTokens = 16;
 constexpr int kLocMaxTpc = 6;  // query tokens one CTA takes in turn
 
-// tcgen05 attention (verify + prefill): 2 query tiles of 128 rows
-// (8 positions x 16 heads each), key tiles of 128.
+// tcgen05 attention (verify + prefill): one query tile of 128 rows
+// (8 positions x 16 heads) per CTA, key tiles of 128.
 constexpr int kTcRows = 128;
 constexpr int kTcKeys = 128;
 constexpr int kTcPosPerTile = kTcRows / kGroup;   // 8
-constexpr int kTcPosPerCta = 2 * kTcPosPerTile;   // 16
-constexpr int kTcStages = 2;
+constexpr int kTcPosPerCta = kTcPosPerTile;       // 8
+constexpr int kTcStages = 3;
 constexpr int kTcTileBytes = kTcKeys * kRowBytes;  // 32 KB (two 64-dim boxes)
-constexpr int kTcQBytes = kTcRows * kRowBytes;     // 32 KB per query tile
-constexpr int kTcSmem = 2 * kTcQBytes + kTcStages * 2 * kTcTileBytes + 1024 + 256;
-constexpr int kTcThreads = 320;  // warps 0-3 softmax A, 4-7 softmax B, 8 TMA, 9 MMA
+constexpr int kTcQBytes = kTcRows * kRowBytes;     // 32 KB
+constexpr int kTcSmem = kTcQBytes + kTcStages * 2 * kTcTileBytes + 1024 + 256;
+constexpr int kTcThreads = 320;  // warps 0-3 / 4-7 softmax of even / odd key tiles, 8 TMA, 9 MMA
 constexpr int kTcMaxSplits = 160;
 
 struct RopeTurns {
