@@ -120,7 +120,7 @@ cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id) {
   std::lock_guard<std::mutex> lk(mu);
   if (done[kernel_id] & (1ull << dev)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && kernel_id == 2)  // the local decode kernel runs 16-CTA clusters
+  if (e == cudaSuccess && kernel_id >= 2)  // the local-layer kernels run 16-CTA clusters
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[kernel_id] |= 1ull << dev;
   return e;
@@ -292,7 +292,7 @@ cudaError_t launch_local(const mg_layer *layer, const mg_cache *cache, const int
   const RopeTables t = rope_tables(layer->rope_theta);
   std::memcpy(p.turn, t.turn, sizeof p.turn);
   std::memcpy(p.step, t.step, sizeof p.step);
-  return launch_local_attn(p, tk, tv, s);
+  return n > 1 ? launch_local_tc(p, tk, tv, s) : launch_local_attn(p, tk, tv, s);
 }
 
 }  // namespace
@@ -460,9 +460,11 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
   const uint64_t outer = static_cast<uint64_t>(B) * kHkv;
 
   if (local && op == MG_OP_VERIFY) {
+    // one token: the mma.sync ring kernel; a block: the tcgen05 ring kernel
+    const uint32_t rows = n == 1 ? kDecTile : kWindow / kLocCluster;
     CUtensorMap tk, tv;
-    if (!map_rows(&tk, cache->k, cache->slots, outer, kDecTile) ||
-        !map_rows(&tv, cache->v, cache->slots, outer, kDecTile))
+    if (!map_rows(&tk, cache->k, cache->slots, outer, rows) ||
+        !map_rows(&tv, cache->v, cache->slots, outer, rows))
       return MG_ERR_CUDA;
     return launch_status(launch_local(layer, cache, d_pos0, n, max_len, q, k_new, v_new, false, o,
                                       d_err, tk, tv, s));

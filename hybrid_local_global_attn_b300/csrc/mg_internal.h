@@ -159,7 +159,10 @@ cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id);
 cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                           cudaStream_t s);
-// picks p.tpc itself
+// single-token ring kernel (picks p.tpc itself) and the tcgen05 ring kernel
+// for draft blocks (8 tokens per CTA)
+cudaError_t launch_local_tc(const LocalParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                            cudaStream_t s);
 cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtensorMap &tv,
                               cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
