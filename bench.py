@@ -636,6 +636,26 @@ def run_ncu_case(name):
             pos = torch.tensor([T - n], dtype=torch.int32, device=dev)
             for _ in range(4):
                 mg.mg_attn_verify(lay, cache, pos, T, q, kn, vn, o, ws, err)
+    elif name in ("decode_local", "verify_local"):
+        # one local layer at context 131072 (a full 2048-slot ring), batch 1
+        T = 131072
+        cache = mg.KVCache(mg.LOCAL, 1, T + 16)
+        cache.k.normal_()
+        cache.v.normal_()
+        lay = mg.make_layer(mg.LOCAL)
+        n = 1 if name == "decode_local" else 16
+        op = mg.OP_DECODE if n == 1 else mg.OP_VERIFY
+        ws = mg.workspace(op, lay, 1, n, T + 16)
+        q = torch.randn((1, n, 32, 128), device=dev).to(bf)
+        kn = torch.randn((1, n, 2, 128), device=dev).to(bf)
+        vn = torch.randn((1, n, 2, 128), device=dev).to(bf)
+        o = torch.empty_like(q)
+        pos = torch.tensor([T], dtype=torch.int32, device=dev)
+        for _ in range(4):
+            if n == 1:
+                mg.mg_append_decode(lay, cache, pos, T + 16, q[:, 0], kn, vn, o[:, 0], ws, err)
+            else:
+                mg.mg_attn_verify(lay, cache, pos, T + 16, q, kn, vn, o, ws, err)
     elif name in ("prefill_global", "prefill_local"):
         kind = mg.GLOBAL if name == "prefill_global" else mg.LOCAL
         c0, n = 28672, 4096  # last 4096-token chunk of a 32768-token prompt
@@ -670,7 +690,8 @@ def main():
     ap.add_argument("--fill", default="prefill", choices=["prefill", "random"],
                     help="random: fill caches without attention (profiling runs only)")
     ap.add_argument("--ncu-case", default=None,
-                    help="decode_global | verify_global | prefill_global | prefill_local")
+                    help="decode_global | verify_global | decode_local | verify_local | "
+                         "prefill_global | prefill_local")
     ap.add_argument("--micro", action="store_true",
                     help="per-call cost of each entry point in graphs of back-to-back calls")
     args = ap.parse_args()
