@@ -4,10 +4,11 @@
 // and lse_s = m_s + log2(l_s) in the base-2 domain.  The exact softmax over
 // the union of the splits is o = sum_s 2^(lse_s - L) o_s / sum_s 2^(lse_s - L)
 // with L = max_s lse_s; splits that saw no key carry lse = -inf and drop out.
-// A separate launch (no inter-CTA waiting).  One CTA of 16 warps per
-// (row, quarter of the 128 dims): warp w takes splits w, w+16, ... with one
-// dim per lane; all of a warp's loads are issued together, each warp merges
-// against its own max, and warp 0 rescales and adds the 16 warp results.
+// A separate launch (no inter-CTA waiting).  Few rows, many splits (global
+// decode): one CTA of 16 warps per (row, quarter of the 128 dims): warp w
+// takes splits w, w+16, ... with one dim per lane; all of a warp's loads are
+// issued together, each warp merges against its own max, and warp 0
+// rescales and adds the 16 warp results.
 #include "mg_internal.h"
 #include "mg_ptx.cuh"
 
@@ -73,8 +74,51 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   }
 }
 
+// Many rows, few splits (verify): one CTA per row, thread d = output dim d.
+// The splits go in chunks of 16 whose loads are all in flight; the chunk
+// maxima rescale the running sums (online log-sum-exp).
+constexpr int kRowChunk = 16;
+constexpr int kRowSplitsMax = 64;  // above this the wide kernel is used
+
+__global__ void __launch_bounds__(kD) combine_rows_kernel(const CombineParams p) {
+  pdl_wait();  // the partials come from the previous kernel
+  pdl_launch_dependents();
+  const int row = blockIdx.x, d = threadIdx.x;
+  const int S = p.splits;
+  const float *lse = p.part_lse + static_cast<size_t>(row) * S;
+  const float *po = p.part_o + static_cast<size_t>(row) * S * kD + d;
+  float m = -INFINITY, den = 0.f, acc = 0.f;
+  for (int s0 = 0; s0 < S; s0 += kRowChunk) {
+    float ls[kRowChunk], v[kRowChunk];
+#pragma unroll
+    for (int k = 0; k < kRowChunk; ++k) {
+      const int s_ = s0 + k;
+      ls[k] = (s_ < S) ? __ldg(lse + s_) : -INFINITY;
+      v[k] = (s_ < S) ? __ldg(po + static_cast<size_t>(s_) * kD) : 0.f;
+    }
+    float mc = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kRowChunk; ++k) mc = fmaxf(mc, ls[k]);
+    if (mc == -INFINITY) continue;  // nothing in this chunk
+    const float mn = fmaxf(m, mc);
+    const float f = (m == -INFINITY) ? 0.f : fast_exp2(m - mn);
+    den *= f;
+    acc *= f;
+    m = mn;
+#pragma unroll
+    for (int k = 0; k < kRowChunk; ++k) {
+      const float w = (ls[k] == -INFINITY) ? 0.f : fast_exp2(ls[k] - m);
+      den += w;
+      acc = fmaf(w, v[k], acc);
+    }
+  }
+  p.o[static_cast<size_t>(row) * kD + d] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
+}
+
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s) {
   if (p.rows <= 0) return cudaSuccess;
+  if (p.splits <= kRowSplitsMax)
+    return launch_pdl(combine_rows_kernel, dim3(p.rows), dim3(kD), 0, s, p);
   return launch_pdl(combine_kernel, dim3(p.rows * kCombineParts), dim3(kCombineWarps * 32), 0, s,
                     p);
 }
