@@ -17,22 +17,27 @@
 // head).  Key tiles hold 128 keys and are aligned to c0, so a tile never
 // straddles the cache and the block.
 //
-// Two softmax warpgroups take alternate key tiles (even / odd), each with its
-// own S and O in TMEM and its own running max and sum -- two independent
-// online softmaxes over interleaved halves of the keys, merged at the end.
-// So S = Q K^T of tile t + 2 only waits for P.V of tile t, not for the other
-// group's softmax, and the tensor core is fed while either group works.
+// Shared-memory bandwidth (128 B/cycle) is the tight resource of a
+// single-CTA tcgen05 pipeline: per 128x128 tile the TMA fill (64 KB), the
+// K operand (32 KB) and the V operand (32 KB) already take ~1000 cycles.  So
+// the query tile lives in TMEM and is the A operand of S = Q K^T, as P is of
+// O += P V; only K and V are read from shared memory.
 //
 // Warp roles (320 threads):
-//   warps 0-3  softmax of even key tiles (thread = one row = one TMEM lane)
-//   warps 4-7  softmax of odd key tiles
-//   warp 8     TMA producer (Q once; K and V in a 3-deep ring)
+//   warps 0-3  softmax of keys 0..63 of every key tile (thread = row = lane)
+//   warps 4-7  softmax of keys 64..127 of the same rows; the two halves
+//              exchange their row maxima once per tile
+//   warp 8     TMA producer (Q once; K in a 2-deep ring, V in a 4-deep ring:
+//              V of a tile is consumed a softmax after its K)
 //   warp 9     TMEM owner and single-thread MMA issuer
-// TMEM (512 columns): S_0, S_1 (fp32 128 cols each; P overwrites the first
-// 64 columns as packed bf16), O_0, O_1 (fp32 128 cols each).
-// Per key tile: S = Q K^T (M128 N128 K16 x 8), softmax in registers with a
-// lazily rescaled running max (rescale only when the max grows by more than
-// 2^8), P back to TMEM, O += P V (A from TMEM, V as an MN-major operand).
+// TMEM (512 columns): S_0, S_1 (double-buffered scores, fp32 128 cols each;
+// P overwrites the first 64 columns as packed bf16), O (fp32 128 cols), Q
+// (bf16 pairs, 64 cols).  S = Q K^T of tile t + 1 runs while the softmax
+// works on tile t.
+// Per key tile: S = Q K^T (M128 N128 K16 x 8, A from TMEM), softmax in
+// registers with a lazily rescaled running max (rescale only when the max
+// grows by more than 2^8), P back to TMEM, O += P V (A from TMEM, V as an
+// MN-major operand).
 // Splits (verify): the cache part is cut across CTAs; each writes (o/l, lse)
 // and the combine kernel merges them.
 #include "mg_internal.h"
@@ -67,22 +72,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_base_slot;
+  __shared__ float red_x[2][kTcRows];  // per tile: the two halves' row maxima
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase;                        // 32 KB
-  const uint32_t sKV = sbase + kTcQBytes;           // stage s: K at +64K*s, V at +64K*s+32K
-  const uint32_t sBar = sKV + kTcStages * 2 * kTcTileBytes;
+  const uint32_t sQ = sbase;                        // 32 KB (copied into TMEM)
+  const uint32_t sK = sbase + kTcQBytes;            // K ring: stage s at +32K*s
+  const uint32_t sV = sK + kTcKStages * kTcTileBytes;  // V ring
+  const uint32_t sBar = sV + kTcVStages * kTcTileBytes;
   // barrier addresses
-  const uint32_t bar_q = sBar;
-  const uint32_t bar_kf = sBar + 8;                        // [3] K full
-  const uint32_t bar_vf = bar_kf + 8 * kTcStages;          // [3] V full
-  const uint32_t bar_ke = bar_vf + 8 * kTcStages;          // [3] K stage free
-  const uint32_t bar_ve = bar_ke + 8 * kTcStages;          // [3] V stage free
-  const uint32_t bar_s = bar_ve + 8 * kTcStages;           // [2] S ready (group 0, 1)
-  const uint32_t bar_p = bar_s + 16;                       // [2] P ready
-  const uint32_t bar_o = bar_p + 16;                       // [2] O final
-  const uint32_t bar_done = bar_o + 16;                    // all MMAs retired
+  const uint32_t bar_q = sBar;                             // Q in shared memory
+  const uint32_t bar_kf = sBar + 8;                        // [kTcKStages] K full
+  const uint32_t bar_ke = bar_kf + 8 * kTcKStages;         // [kTcKStages] K stage free
+  const uint32_t bar_vf = bar_ke + 8 * kTcKStages;         // [kTcVStages] V full
+  const uint32_t bar_ve = bar_vf + 8 * kTcVStages;         // [kTcVStages] V stage free
+  const uint32_t bar_s = bar_ve + 8 * kTcVStages;          // [2] S buffer ready
+  const uint32_t bar_p = bar_s + 16;                       // [2] P ready (256 arrivals)
+  const uint32_t bar_qt = bar_p + 16;                      // Q in TMEM (256 arrivals)
+  const uint32_t bar_o = bar_qt + 8;                       // O final
+  const uint32_t bar_done = bar_o + 8;                     // all MMAs retired
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y, b = blockIdx.z;
@@ -114,23 +122,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
   const int ntiles = ti.ncache + ti.nnew;
-  const int n_grp[2] = {(ntiles + 1) / 2, ntiles / 2};  // key tiles of group 0 / 1
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     if (bad && split == 0 && qb == 0) set_err(p.err, MG_DERR_POSITION);
     mbar_init(bar_q, 1);
-    for (int i = 0; i < kTcStages; ++i) {
+    for (int i = 0; i < kTcKStages; ++i) {
       mbar_init(bar_kf + 8 * i, 1);
-      mbar_init(bar_vf + 8 * i, 1);
       mbar_init(bar_ke + 8 * i, 1);
+    }
+    for (int i = 0; i < kTcVStages; ++i) {
+      mbar_init(bar_vf + 8 * i, 1);
       mbar_init(bar_ve + 8 * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s + 8 * i, 1);
-      mbar_init(bar_p + 8 * i, 128);
-      mbar_init(bar_o + 8 * i, 1);
+      mbar_init(bar_p + 8 * i, 256);
     }
+    mbar_init(bar_qt, 256);
+    mbar_init(bar_o, 1);
     mbar_init(bar_done, 1);
     fence_mbar_init();
   }
@@ -142,6 +152,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_slot;
+  constexpr uint32_t kColO = 256, kColQ = 384;
 
   if (warp == 8) {
     // ------------------------------------------------------- producer ----
@@ -155,25 +166,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive_expect_tx(bar_q, kTcQBytes);
       for (int x = 0; x < 2; ++x)
         tma_load_4d(sQ + x * (kTcQBytes / 2), &tq, bar_q, 64 * x, kGroup * g, q_t0, b);
-      int issued = 0;
+      int issued_k = 0, issued_v = 0;
       for (int t = 0; t < ntiles; ++t) {
-        const int st = t % kTcStages;
-        // K of tile t reuses the stage of tile t-3 once S = Q K^T of it has
-        // run; V waits for its P.V instead
-        if (t >= kTcStages &&
-            !mbar_wait(bar_ke + 8 * st, ((t / kTcStages) - 1) & 1, &abort_flag)) {
-          abort_flag = 1;
-          set_err(p.err, MG_DERR_TIMEOUT);
-          break;
-        }
         const int32_t kp0 = tile_kp0(ti, t);
-        const uint32_t dk = sKV + st * 2 * kTcTileBytes;
-        const uint32_t dv = dk + kTcTileBytes;
         const bool from_cache = t < ti.ncache;
-        // one 128-key tile of K (dst dk, barrier kf) or V (dv, vf)
-        auto load_tile = [&](bool is_v) {
-          const uint32_t dst = is_v ? dv : dk;
-          const uint32_t fb = (is_v ? bar_vf : bar_kf) + 8 * st;
+        // one 128-key tile of K or V into dst, completing on fb
+        auto load_tile = [&](bool is_v, uint32_t dst, uint32_t fb) {
           const CUtensorMap *ma = is_v ? &tva : &tka;
           const CUtensorMap *mb = is_v ? &tvb : &tkb;
           mbar_arrive_expect_tx(fb, kTcTileBytes);
@@ -187,61 +185,70 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tma_load_4d(d, mb, fb, 64 * x, g, kp0 - ti.c0, b);
           }
         };
-        load_tile(false);
-        if (t >= kTcStages &&
-            !mbar_wait(bar_ve + 8 * st, ((t / kTcStages) - 1) & 1, &abort_flag)) {
+        // K of tile t reuses the stage of tile t - kTcKStages once its
+        // S = Q K^T has run; V reuses the stage of tile t - kTcVStages once
+        // its P.V has run
+        const int ks = t % kTcKStages, vs = t % kTcVStages;
+        if (t >= kTcKStages &&
+            !mbar_wait(bar_ke + 8 * ks, ((t / kTcKStages) - 1) & 1, &abort_flag)) {
           abort_flag = 1;
           set_err(p.err, MG_DERR_TIMEOUT);
-          ++issued;  // the K copy of this tile is in flight
           break;
         }
-        load_tile(true);
-        ++issued;
+        load_tile(false, sK + ks * kTcTileBytes, bar_kf + 8 * ks);
+        ++issued_k;
+        if (t >= kTcVStages &&
+            !mbar_wait(bar_ve + 8 * vs, ((t / kTcVStages) - 1) & 1, &abort_flag)) {
+          abort_flag = 1;
+          set_err(p.err, MG_DERR_TIMEOUT);
+          break;
+        }
+        load_tile(true, sV + vs * kTcTileBytes, bar_vf + 8 * vs);
+        ++issued_v;
       }
       // no copies may be in flight when the CTA retires
       (void)mbar_wait(bar_q, 0, nullptr);
-      for (int t = max(0, issued - kTcStages); t < issued; ++t) {
-        (void)mbar_wait(bar_kf + 8 * (t % kTcStages), (t / kTcStages) & 1, nullptr);
-        (void)mbar_wait(bar_vf + 8 * (t % kTcStages), (t / kTcStages) & 1, nullptr);
-      }
+      for (int t = max(0, issued_k - kTcKStages); t < issued_k; ++t)
+        (void)mbar_wait(bar_kf + 8 * (t % kTcKStages), (t / kTcKStages) & 1, nullptr);
+      for (int t = max(0, issued_v - kTcVStages); t < issued_v; ++t)
+        (void)mbar_wait(bar_vf + 8 * (t % kTcVStages), (t / kTcVStages) & 1, nullptr);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer ----
     if (lane == 0 && ntiles > 0) {
-      bool ok = mbar_wait(bar_q, 0, &abort_flag);
-      tc_fence_after();
-      // S_{t&1} = Q K(t)^T
+      bool ok = mbar_wait(bar_qt, 0, &abort_flag);  // Q copied into TMEM by the softmax warps
+      // S_{t&1} = Q K(t)^T, Q from TMEM
       auto qk = [&](int t) -> bool {
-        const int st = t % kTcStages;
-        if (!mbar_wait(bar_kf + 8 * st, (t / kTcStages) & 1, &abort_flag)) return false;
+        const int st = t % kTcKStages;
+        if (!mbar_wait(bar_kf + 8 * st, (t / kTcKStages) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t ks = sKV + st * 2 * kTcTileBytes;
+        const uint32_t ks = sK + st * kTcTileBytes;
         const uint32_t tS = tbase + 128 * (t & 1);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32;
-          mma_ss(tS, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(ks + off, 16, 1024),
-                 kIdescQK, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * (kTcTileBytes / 2) + (kk & 3) * 32;
+          mma_ts(tS, tbase + kColQ + 8 * kk, smem_desc_sw128(ks + off, 16, 1024), kIdescQK,
+                 kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_s + 8 * (t & 1));
         mma_commit(bar_ke + 8 * st);
         return true;
       };
-      // O_{t&1} += P(t) V(t), P from the first half of S_{t&1}
+      // O += P(t) V(t), P from the first half of S_{t&1}
       auto pv = [&](int t) -> bool {
-        const int st = t % kTcStages, e = t & 1;
+        const int st = t % kTcVStages, e = t & 1;
         if (!mbar_wait(bar_p + 8 * e, (t >> 1) & 1, &abort_flag)) return false;
-        if (!mbar_wait(bar_vf + 8 * st, (t / kTcStages) & 1, &abort_flag)) return false;
+        if (!mbar_wait(bar_vf + 8 * st, (t / kTcVStages) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t vs = sKV + st * 2 * kTcTileBytes + kTcTileBytes;
-        const uint32_t tS = tbase + 128 * e, tO = tbase + 256 + 128 * e;
+        const uint32_t vs = sV + st * kTcTileBytes;
+        const uint32_t tS = tbase + 128 * e;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tO, tS + 8 * kk, smem_desc_sw128(vs + kk * 2048, kTcTileBytes / 2, 1024), kIdescPV,
-                 (t < 2 && kk == 0) ? 0u : 1u);
+          mma_ts(tbase + kColO, tS + 8 * kk, smem_desc_sw128(vs + kk * 2048, kTcTileBytes / 2, 1024),
+                 kIdescPV, (t == 0 && kk == 0) ? 0u : 1u);
         }
         mma_commit(bar_ve + 8 * st);
-        if (t + 2 >= ntiles) mma_commit(bar_o + 8 * e);  // the group's last tile
+        if (t == ntiles - 1) mma_commit(bar_o);
         return true;
       };
       // Issue order: S(0), S(1), then P.V(t) and S(t+2) for t = 0, 1, ...
@@ -263,74 +270,103 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------- softmax warps ----
-    const int e = warp >> 2;                     // group: even (0) or odd (1) key tiles
+    const int hh = warp >> 2;                    // half: keys 64 hh .. 64 hh + 63 of each tile
     const int r = (warp & 3) * 32 + lane;        // row = TMEM lane
     const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tbase + lane_bits + 128 * e;
-    const uint32_t tO = tbase + lane_bits + 256 + 128 * e;
+    const uint32_t tL = tbase + lane_bits;       // this lane's column 0
     const int32_t tloc = kTcPosPerCta * qb + (r >> 4);  // index in block
     const int32_t qp = ti.qa + (r >> 4);                // this row's position
     const int h = kGroup * g + (r & 15);
     const bool row_valid = tloc < p.n;  // rows past the block are padding
     const float sl2 = p.scale_log2;
     const int32_t wlo = local ? qp - p.window + 1 : INT32_MIN;  // lowest key in the window
-    float mrow = -INFINITY, lrow = 0.f;
+    float mrow = -INFINITY, lhalf = 0.f;  // running max (same in both halves), this half's sum
     bool ok = true;
 
-    for (int u = 0; u < n_grp[e]; ++u) {
-      const int t = 2 * u + e;  // key tile
-      // tcgen05.ld/st below are warp-collective: the whole warp goes on or stops
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_s + 8 * e, u & 1, &abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int32_t kp0 = tile_kp0(ti, t);
-      const bool need_mask = (kp0 < 0) || (kp0 + kTcKeys - 1 > ti.qa) ||
-                             (local && kp0 < ti.qz - p.window + 1);
-      // The whole S row (128 fp32) in registers: four loads in flight, one wait.
-      uint32_t v[4][32];
+    // Q row r, dims 64 hh .. 64 hh + 63 (swizzled box hh of the Q tile),
+    // into TMEM columns kColQ + 32 hh .. as bf16 pairs
+    if (ntiles > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, &abort_flag));
+      uint32_t qv[32];
+      const uint32_t box = sQ + hh * (kTcQBytes / 2) + r * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, v[c]);
-      tmem_wait_ld();
+      for (int c = 0; c < 8; ++c) {
+        uint32_t a0, a1, a2, a3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                     : "r"(box + ((c ^ (r & 7)) << 4)));
+        qv[4 * c] = a0;
+        qv[4 * c + 1] = a1;
+        qv[4 * c + 2] = a2;
+        qv[4 * c + 3] = a3;
+      }
+      tmem_st32(tL + kColQ + 32 * hh, qv);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_qt);
+    }
+
+    // Every warp runs every tile's two named barriers; after a timeout a warp
+    // keeps doing so without touching TMEM (its results are dropped).
+    for (int t = 0; t < ntiles; ++t) {
+      const int e = t & 1;
+      const uint32_t tS = tL + 128 * e;
+      // tcgen05.ld/st below are warp-collective: the whole warp goes on or stops
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_s + 8 * e, (t >> 1) & 1, &abort_flag));
+      tc_fence_after();
+      const int32_t kp0 = tile_kp0(ti, t) + 64 * hh;  // first key of this half
+      const bool need_mask = (kp0 < 0) || (kp0 + 63 > ti.qa) ||
+                             (local && kp0 < ti.qz - p.window + 1);
+      uint32_t v[2][32];
+      if (ok) {
+        tmem_ld32(tS + 64 * hh, v[0]);
+        tmem_ld32(tS + 64 * hh + 32, v[1]);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[0][j] = v[1][j] = 0xff800000u;
+      }
       if (need_mask) {
         // keys kp0 + j are visible for j in [jlo, jhi]; the rest become -inf
         const int32_t jlo = max(max(wlo, 0), kp0) - kp0;
         const int32_t jhi = qp - kp0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int32_t jj = 32 * c + j;
             v[c][j] = (jj < jlo || jj > jhi) ? 0xff800000u : v[c][j];
           }
       }
-      // row max: three-input max, four independent chains
-      float mx4[4];
+      float mx2[2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float a = fmax3(__uint_as_float(v[c][0]), __uint_as_float(v[c][1]),
                         __uint_as_float(v[c][2]));
 #pragma unroll
         for (int j = 3; j < 31; j += 2)
           a = fmax3(a, __uint_as_float(v[c][j]), __uint_as_float(v[c][j + 1]));
-        mx4[c] = fmaxf(a, __uint_as_float(v[c][31]));
+        mx2[c] = fmaxf(a, __uint_as_float(v[c][31]));
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      // the row's max over both halves (every S value is in registers, so P
+      // may overwrite S after this barrier)
+      red_x[hh][r] = fmaxf(mx2[0], mx2[1]);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const float mx = fmaxf(red_x[0][r], red_x[1][r]);
+      asm volatile("bar.sync 2, 256;" ::: "memory");  // red_x is reused next tile
       const float mt = mx * sl2;  // scale > 0, so it commutes with max
       float alpha = 1.f;
       if (mt > mrow + kRescaleThreshold || (mrow == -INFINITY && mt != -INFINITY)) {
         if (mrow != -INFINITY) alpha = fast_exp2(mrow - mt);
         mrow = mt;
       }
-      lrow *= alpha;
+      lhalf *= alpha;
       const float muse = (mrow == -INFINITY) ? 0.f : mrow;
-      // P = 2^(s*scale*log2e - m), packed to bf16 over the first half of S;
-      // the scaling and the row sum run as packed f32x2 operations
+      // P = 2^(s*scale*log2e - m) as bf16 pairs: keys 64 hh + 2c.. -> column 32 hh + c
       const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-muse, -muse);
-      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};  // (0.0f, 0.0f)
+      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
@@ -342,27 +378,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ls2[(j >> 1) & 3] = add_f32x2(ls2[(j >> 1) & 3], f32x2(e0, e1));
           pk[j >> 1] = pack_bf16x2(e0, e1);
         }
-        tmem_st16(tS + 16 * c, pk);
+        if (ok) tmem_st16(tS + 32 * hh + 16 * c, pk);
       }
       {
         const uint64_t t2 = add_f32x2(add_f32x2(ls2[0], ls2[1]), add_f32x2(ls2[2], ls2[3]));
         float a0, a1;
         f32x2_split(t2, a0, a1);
-        lrow += a0 + a1;
+        lhalf += a0 + a1;
       }
-      // Rare: the running max grew by more than 2^8 -- rescale O in TMEM.  O
-      // is stable here (this group's last P.V was issued before this S tile
-      // and has retired with it) and the next P.V waits for this warp's
-      // arrival below.
-      if (u > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // Rare: the running max grew by more than 2^8 -- rescale O in TMEM
+      // (this half's 64 columns).  S(t) was issued after P.V(t-2), so that
+      // one has retired, but P.V(t-1) may still run: wait for its V stage
+      // release first.  The next P.V waits for this tile's P arrival below.
+      if (ok && t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const int pst = (t - 1) % kTcVStages;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar_ve + 8 * pst, ((t - 1) / kTcVStages) & 1, &abort_flag)) && ok;
+        tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o32[32];
-          tmem_ld32(tO + 32 * c, o32);
+          tmem_ld32(tL + kColO + 64 * hh + 32 * c, o32);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) o32[j] = __float_as_uint(__uint_as_float(o32[j]) * alpha);
-          tmem_st32(tO + 32 * c, o32);
+          tmem_st32(tL + kColO + 64 * hh + 32 * c, o32);
         }
       }
       tmem_wait_st();
@@ -371,66 +411,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     // ----------------------------------------------------------- epilogue ----
-    // The two groups' states merge: O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1),
-    // f_e = 2^(m_e - M).  Group e finishes dims 64 e .. 64 e + 63 of its rows.
-    for (int k = 0; k < 2; ++k)
-      if (ok && n_grp[k] > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(bar_o + 8 * k, 0, &abort_flag)))
-        ok = false;
+    if (ok && ntiles > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_o, 0, &abort_flag))) ok = false;
     tc_fence_after();
-    // (m, l) of both groups, [group][m, l][row], over the Q tile: every MMA
-    // has retired once both groups' O are final
-    float *ml_x = reinterpret_cast<float *>(smem);
-    const bool have_mine = ok && n_grp[e] > 0 && lrow > 0.f;
-    ml_x[(2 * e + 0) * kTcRows + r] = have_mine ? mrow : -INFINITY;
-    ml_x[(2 * e + 1) * kTcRows + r] = have_mine ? lrow : 0.f;
+    // the row sum: both halves' partial sums (same running max)
+    red_x[hh][r] = lhalf;
     asm volatile("bar.sync 1, 256;" ::: "memory");
+    const float lrow = red_x[0][r] + red_x[1][r];
     ok = __all_sync(0xffffffffu, ok && !abort_flag);  // warp-uniform: it gates tcgen05.ld
     if (!ok && lane == 0) set_err(p.err, MG_DERR_TIMEOUT);
-    const float m0 = ml_x[0 * kTcRows + r], m1 = ml_x[2 * kTcRows + r];
-    const float M = fmaxf(m0, m1);
-    const float f0 = (ok && m0 != -INFINITY) ? fast_exp2(m0 - M) : 0.f;
-    const float f1 = (ok && m1 != -INFINITY) ? fast_exp2(m1 - M) : 0.f;
-    const float L = f0 * ml_x[1 * kTcRows + r] + f1 * ml_x[3 * kTcRows + r];
-    const bool have = ok && L > 0.f;
-    const float w0 = have ? f0 / L : 0.f, w1 = have ? f1 / L : 0.f;
+    const bool have = ok && ntiles > 0 && lrow > 0.f;
+    const float inv = have ? 1.f / lrow : 0.f;
     const size_t orow = (static_cast<size_t>(b) * p.n + tloc) * kHq + h;
-    const uint32_t tO0 = tbase + lane_bits + 256, tO1 = tbase + lane_bits + 384;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      const int d0 = 64 * e + 32 * c;  // first dim of this 32-column chunk
-      // tcgen05.ld is warp-collective: load on CTA-uniform conditions only
-      // (a group without key tiles never wrote its O; its weight is 0)
-      uint32_t a0[32], a1[32];
-      if (ok && n_grp[0] > 0) tmem_ld32(tO0 + d0, a0);
-      if (ok && n_grp[1] > 0) tmem_ld32(tO1 + d0, a1);
-      tmem_wait_ld();
-      float o[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        o[j] = (w0 != 0.f ? __uint_as_float(a0[j]) * w0 : 0.f) +
-               (w1 != 0.f ? __uint_as_float(a1[j]) * w1 : 0.f);
+      const int d0 = 64 * hh + 32 * c;  // first dim of this 32-column chunk
+      uint32_t a[32];
+      if (ok && ntiles > 0) {
+        tmem_ld32(tL + kColO + d0, a);
+        tmem_wait_ld();
+      }
       if (!row_valid) continue;
       if (p.splits == 1) {
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD + d0);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           uint4 w;
-          w.x = pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]);
-          w.y = pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]);
-          w.z = pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]);
-          w.w = pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]);
+          w.x = pack_bf16x2(have ? __uint_as_float(a[8 * q4 + 0]) * inv : 0.f,
+                            have ? __uint_as_float(a[8 * q4 + 1]) * inv : 0.f);
+          w.y = pack_bf16x2(have ? __uint_as_float(a[8 * q4 + 2]) * inv : 0.f,
+                            have ? __uint_as_float(a[8 * q4 + 3]) * inv : 0.f);
+          w.z = pack_bf16x2(have ? __uint_as_float(a[8 * q4 + 4]) * inv : 0.f,
+                            have ? __uint_as_float(a[8 * q4 + 5]) * inv : 0.f);
+          w.w = pack_bf16x2(have ? __uint_as_float(a[8 * q4 + 6]) * inv : 0.f,
+                            have ? __uint_as_float(a[8 * q4 + 7]) * inv : 0.f);
           dst[q4] = w;
         }
       } else {
         float4 *dst = reinterpret_cast<float4 *>(p.part_o + (orow * p.splits + split) * kD + d0);
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
-          dst[q4] = make_float4(o[4 * q4 + 0], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+          dst[q4] = make_float4(have ? __uint_as_float(a[4 * q4 + 0]) * inv : 0.f,
+                                have ? __uint_as_float(a[4 * q4 + 1]) * inv : 0.f,
+                                have ? __uint_as_float(a[4 * q4 + 2]) * inv : 0.f,
+                                have ? __uint_as_float(a[4 * q4 + 3]) * inv : 0.f);
       }
     }
-    if (p.splits > 1 && row_valid && e == 0)
-      p.part_lse[orow * p.splits + split] = have ? M + __log2f(L) : -INFINITY;
+    if (p.splits > 1 && row_valid && hh == 0)
+      p.part_lse[orow * p.splits + split] = have ? mrow + __log2f(lrow) : -INFINITY;
   }
 
   __syncwarp();

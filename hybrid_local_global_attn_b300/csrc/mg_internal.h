@@ -48,10 +48,11 @@ constexpr int kTcRows = 128;
 constexpr int kTcKeys = 128;
 constexpr int kTcPosPerTile = kTcRows / kGroup;   // 8
 constexpr int kTcPosPerCta = kTcPosPerTile;       // 8
-constexpr int kTcStages = 3;
+constexpr int kTcKStages = 2;  // K ring (freed by Q.K^T)
+constexpr int kTcVStages = 4;  // V ring (freed by P.V, which comes a softmax later)
 constexpr int kTcTileBytes = kTcKeys * kRowBytes;  // 32 KB (two 64-dim boxes)
 constexpr int kTcQBytes = kTcRows * kRowBytes;     // 32 KB
-constexpr int kTcSmem = kTcQBytes + kTcStages * 2 * kTcTileBytes + 1024 + 256;
+constexpr int kTcSmem = kTcQBytes + (kTcKStages + kTcVStages) * kTcTileBytes + 1024 + 256;
 constexpr int kTcThreads = 320;  // warps 0-3 / 4-7 softmax of even / odd key tiles, 8 TMA, 9 MMA
 constexpr int kTcMaxSplits = 160;
 
