@@ -14,30 +14,28 @@
 //
 // Tiling: a CTA owns 8 consecutive query positions of one KV group: 8
 // positions x 16 query heads form one M = 128 tile (rows r = 16 * position +
-// head).  Key tiles hold 128 keys and are aligned to c0, so a tile never
+// head).  Key tiles hold 256 keys and are aligned to c0, so a tile never
 // straddles the cache and the block.
 //
-// Shared-memory bandwidth (128 B/cycle) is the tight resource of a
-// single-CTA tcgen05 pipeline: per 128x128 tile the TMA fill (64 KB), the
-// K operand (32 KB) and the V operand (32 KB) already take ~1000 cycles.  So
-// the query tile lives in TMEM and is the A operand of S = Q K^T, as P is of
-// O += P V; only K and V are read from shared memory.
+// The issue cost of one tcgen05.mma barely depends on N (on this B300 an
+// M128 N128 K16 takes ~119 cycles with both operands in shared memory, an
+// M128 N256 K16 ~139), so the scores are computed 256 keys at a time: S =
+// Q K^T is 8 M128 N256 K16 MMAs, O += P V 16 M128 N128 K16 MMAs with P
+// from TMEM.  TMEM holds S (256 fp32 columns), P (256 keys as bf16 pairs,
+// 128 columns) and O (128 columns); because P has its own columns, S of the
+// next tile is computed as soon as the softmax has loaded S into registers,
+// and P.V of a tile overlaps Q.K^T of the next.
 //
 // Warp roles (320 threads):
-//   warps 0-3  softmax of keys 0..63 of every key tile (thread = row = lane)
-//   warps 4-7  softmax of keys 64..127 of the same rows; the two halves
+//   warps 0-3  softmax of keys 0..127 of every key tile (thread = row = lane)
+//   warps 4-7  softmax of keys 128..255 of the same rows; the two halves
 //              exchange their row maxima once per tile
-//   warp 8     TMA producer (Q once; K in a 2-deep ring, V in a 4-deep ring:
-//              V of a tile is consumed a softmax after its K)
+//   warp 8     TMA producer (Q once; K in a 2-deep ring of 256-key tiles,
+//              V in a 2-deep ring of 128-key half tiles)
 //   warp 9     TMEM owner and single-thread MMA issuer
-// TMEM (512 columns): S_0, S_1 (double-buffered scores, fp32 128 cols each;
-// P overwrites the first 64 columns as packed bf16), O (fp32 128 cols), Q
-// (bf16 pairs, 64 cols).  S = Q K^T of tile t + 1 runs while the softmax
-// works on tile t.
-// Per key tile: S = Q K^T (M128 N128 K16 x 8, A from TMEM), softmax in
-// registers with a lazily rescaled running max (rescale only when the max
-// grows by more than 2^8), P back to TMEM, O += P V (A from TMEM, V as an
-// MN-major operand).
+// Per key tile: S = Q K^T, softmax in registers with a lazily rescaled
+// running max (rescale only when the max grows by more than 2^8), P to TMEM,
+// O += P V (V as an MN-major operand).
 // Splits (verify): the cache part is cut across CTAs; each writes (o/l, lse)
 // and the combine kernel merges them.
 #include "mg_internal.h"
@@ -47,7 +45,7 @@ namespace mg {
 
 namespace {
 
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kTcKeys, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -76,21 +74,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase;                        // 32 KB (copied into TMEM)
-  const uint32_t sK = sbase + kTcQBytes;            // K ring: stage s at +32K*s
-  const uint32_t sV = sK + kTcKStages * kTcTileBytes;  // V ring
-  const uint32_t sBar = sV + kTcVStages * kTcTileBytes;
+  const uint32_t sQ = sbase;                              // 32 KB
+  const uint32_t sK = sbase + kTcQBytes;                  // K ring: stage s at +64K*s
+  const uint32_t sV = sK + kTcKStages * kTcKTileBytes;    // V ring of half tiles: +32K*s
+  const uint32_t sBar = sV + kTcVStages * kTcVTileBytes;
   // barrier addresses
-  const uint32_t bar_q = sBar;                             // Q in shared memory
+  const uint32_t bar_q = sBar;                             // Q landed
   const uint32_t bar_kf = sBar + 8;                        // [kTcKStages] K full
   const uint32_t bar_ke = bar_kf + 8 * kTcKStages;         // [kTcKStages] K stage free
-  const uint32_t bar_vf = bar_ke + 8 * kTcKStages;         // [kTcVStages] V full
-  const uint32_t bar_ve = bar_vf + 8 * kTcVStages;         // [kTcVStages] V stage free
-  const uint32_t bar_s = bar_ve + 8 * kTcVStages;          // [2] S buffer ready
-  const uint32_t bar_p = bar_s + 16;                       // [2] P ready (256 arrivals)
-  const uint32_t bar_qt = bar_p + 16;                      // Q in TMEM (256 arrivals)
-  const uint32_t bar_o = bar_qt + 8;                       // O final
-  const uint32_t bar_done = bar_o + 8;                     // all MMAs retired
+  const uint32_t bar_vf = bar_ke + 8 * kTcKStages;         // [kTcVStages] V half full
+  const uint32_t bar_ve = bar_vf + 8 * kTcVStages;         // [kTcVStages] V half free
+  const uint32_t bar_s = bar_ve + 8 * kTcVStages;          // S ready
+  const uint32_t bar_sfree = bar_s + 8;                    // S loaded by the softmax (256)
+  const uint32_t bar_p = bar_sfree + 8;                    // P ready (256 arrivals)
+  const uint32_t bar_pfree = bar_p + 8;                    // P.V retired: P and O free
+  const uint32_t bar_done = bar_pfree + 8;                 // all MMAs retired
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y, b = blockIdx.z;
@@ -135,12 +133,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar_vf + 8 * i, 1);
       mbar_init(bar_ve + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_s + 8 * i, 1);
-      mbar_init(bar_p + 8 * i, 256);
-    }
-    mbar_init(bar_qt, 256);
-    mbar_init(bar_o, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_sfree, 256);
+    mbar_init(bar_p, 256);
+    mbar_init(bar_pfree, 1);
     mbar_init(bar_done, 1);
     fence_mbar_init();
   }
@@ -152,7 +148,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_slot;
-  constexpr uint32_t kColO = 256, kColQ = 384;
+  constexpr uint32_t kColP = kTcKeys, kColO = kTcKeys + kTcKeys / 2;  // S at 0
 
   if (warp == 8) {
     // ------------------------------------------------------- producer ----
@@ -166,99 +162,113 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive_expect_tx(bar_q, kTcQBytes);
       for (int x = 0; x < 2; ++x)
         tma_load_4d(sQ + x * (kTcQBytes / 2), &tq, bar_q, 64 * x, kGroup * g, q_t0, b);
+      // keys kp0.. (rows) of K or V into dst (two 64-dim boxes), completing on fb
+      auto load = [&](bool is_v, int t, int32_t kp0, uint32_t dst, uint32_t bytes, uint32_t fb) {
+        const CUtensorMap *ma = is_v ? &tva : &tka;
+        const CUtensorMap *mb = is_v ? &tvb : &tkb;
+        mbar_arrive_expect_tx(fb, bytes);
+        for (int x = 0; x < 2; ++x) {
+          const uint32_t d = dst + x * (bytes / 2);
+          if (p.staged)
+            tma_load_3d(d, ma, fb, 64 * x, kp0 - ti.c0 + kWindow, b * kHkv + g);
+          else if (t < ti.ncache)
+            tma_load_3d(d, ma, fb, 64 * x, kp0, b * kHkv + g);
+          else
+            tma_load_4d(d, mb, fb, 64 * x, g, kp0 - ti.c0, b);
+        }
+      };
       int issued_k = 0, issued_v = 0;
-      for (int t = 0; t < ntiles; ++t) {
-        const int32_t kp0 = tile_kp0(ti, t);
-        const bool from_cache = t < ti.ncache;
-        // one 128-key tile of K or V into dst, completing on fb
-        auto load_tile = [&](bool is_v, uint32_t dst, uint32_t fb) {
-          const CUtensorMap *ma = is_v ? &tva : &tka;
-          const CUtensorMap *mb = is_v ? &tvb : &tkb;
-          mbar_arrive_expect_tx(fb, kTcTileBytes);
-          for (int x = 0; x < 2; ++x) {
-            const uint32_t d = dst + x * (kTcTileBytes / 2);
-            if (p.staged)
-              tma_load_3d(d, ma, fb, 64 * x, kp0 - ti.c0 + kWindow, b * kHkv + g);
-            else if (from_cache)
-              tma_load_3d(d, ma, fb, 64 * x, kp0, b * kHkv + g);
-            else
-              tma_load_4d(d, mb, fb, 64 * x, g, kp0 - ti.c0, b);
-          }
-        };
-        // K of tile t reuses the stage of tile t - kTcKStages once its
-        // S = Q K^T has run; V reuses the stage of tile t - kTcVStages once
-        // its P.V has run
-        const int ks = t % kTcKStages, vs = t % kTcVStages;
+      bool ok = true;
+      // K of tile t reuses the stage of tile t - 2 once its S = Q K^T has run
+      auto load_k = [&](int t) -> bool {
+        const int ks = t % kTcKStages;
         if (t >= kTcKStages &&
-            !mbar_wait(bar_ke + 8 * ks, ((t / kTcKStages) - 1) & 1, &abort_flag)) {
-          abort_flag = 1;
-          set_err(p.err, MG_DERR_TIMEOUT);
-          break;
-        }
-        load_tile(false, sK + ks * kTcTileBytes, bar_kf + 8 * ks);
+            !mbar_wait(bar_ke + 8 * ks, ((t / kTcKStages) - 1) & 1, &abort_flag))
+          return false;
+        load(false, t, tile_kp0(ti, t), sK + ks * kTcKTileBytes, kTcKTileBytes, bar_kf + 8 * ks);
         ++issued_k;
-        if (t >= kTcVStages &&
-            !mbar_wait(bar_ve + 8 * vs, ((t / kTcVStages) - 1) & 1, &abort_flag)) {
-          abort_flag = 1;
-          set_err(p.err, MG_DERR_TIMEOUT);
+        return true;
+      };
+      // K runs a tile ahead of V (S = Q K^T of tile t + 1 is issued before
+      // P.V of tile t); V half u = 2 t + h reuses the stage of half u - 2
+      // once its P.V has run
+      ok = load_k(0);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        if (t + 1 < ntiles && !load_k(t + 1)) {
+          ok = false;
           break;
         }
-        load_tile(true, sV + vs * kTcTileBytes, bar_vf + 8 * vs);
-        ++issued_v;
+        for (int h = 0; h < 2; ++h) {
+          const int u = 2 * t + h, vs = u % kTcVStages;
+          if (u >= kTcVStages &&
+              !mbar_wait(bar_ve + 8 * vs, ((u / kTcVStages) - 1) & 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          load(true, t, tile_kp0(ti, t) + kTcVRows * h, sV + vs * kTcVTileBytes, kTcVTileBytes,
+               bar_vf + 8 * vs);
+          ++issued_v;
+        }
+      }
+      if (!ok) {
+        abort_flag = 1;
+        set_err(p.err, MG_DERR_TIMEOUT);
       }
       // no copies may be in flight when the CTA retires
       (void)mbar_wait(bar_q, 0, nullptr);
       for (int t = max(0, issued_k - kTcKStages); t < issued_k; ++t)
         (void)mbar_wait(bar_kf + 8 * (t % kTcKStages), (t / kTcKStages) & 1, nullptr);
-      for (int t = max(0, issued_v - kTcVStages); t < issued_v; ++t)
-        (void)mbar_wait(bar_vf + 8 * (t % kTcVStages), (t / kTcVStages) & 1, nullptr);
+      for (int u = max(0, issued_v - kTcVStages); u < issued_v; ++u)
+        (void)mbar_wait(bar_vf + 8 * (u % kTcVStages), (u / kTcVStages) & 1, nullptr);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer ----
     if (lane == 0 && ntiles > 0) {
-      bool ok = mbar_wait(bar_qt, 0, &abort_flag);  // Q copied into TMEM by the softmax warps
-      // S_{t&1} = Q K(t)^T, Q from TMEM
+      bool ok = mbar_wait(bar_q, 0, &abort_flag);
+      // S = Q K(t)^T
       auto qk = [&](int t) -> bool {
         const int st = t % kTcKStages;
         if (!mbar_wait(bar_kf + 8 * st, (t / kTcKStages) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t ks = sK + st * kTcTileBytes;
-        const uint32_t tS = tbase + 128 * (t & 1);
+        const uint32_t ks = sK + st * kTcKTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTcTileBytes / 2) + (kk & 3) * 32;
-          mma_ts(tS, tbase + kColQ + 8 * kk, smem_desc_sw128(ks + off, 16, 1024), kIdescQK,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tbase, smem_desc_sw128(sQ + (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32, 16, 1024),
+                 smem_desc_sw128(ks + (kk >> 2) * (kTcKTileBytes / 2) + (kk & 3) * 32, 16, 1024),
+                 kIdescQK, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_s + 8 * (t & 1));
+        mma_commit(bar_s);
         mma_commit(bar_ke + 8 * st);
         return true;
       };
-      // O += P(t) V(t), P from the first half of S_{t&1}
+      // O += P(t) V(t): two V half tiles of 8 k-steps each
       auto pv = [&](int t) -> bool {
-        const int st = t % kTcVStages, e = t & 1;
-        if (!mbar_wait(bar_p + 8 * e, (t >> 1) & 1, &abort_flag)) return false;
-        if (!mbar_wait(bar_vf + 8 * st, (t / kTcVStages) & 1, &abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t vs = sV + st * kTcTileBytes;
-        const uint32_t tS = tbase + 128 * e;
+        if (!mbar_wait(bar_p, t & 1, &abort_flag)) return false;
+        for (int h = 0; h < 2; ++h) {
+          const int u = 2 * t + h, vs = u % kTcVStages;
+          if (!mbar_wait(bar_vf + 8 * vs, (u / kTcVStages) & 1, &abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t v0 = sV + vs * kTcVTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tbase + kColO, tS + 8 * kk, smem_desc_sw128(vs + kk * 2048, kTcTileBytes / 2, 1024),
-                 kIdescPV, (t == 0 && kk == 0) ? 0u : 1u);
+          for (int kk = 0; kk < 8; ++kk) {
+            mma_ts(tbase + kColO, tbase + kColP + 64 * h + 8 * kk,
+                   smem_desc_sw128(v0 + kk * 2048, kTcVTileBytes / 2, 1024), kIdescPV,
+                   (t == 0 && h == 0 && kk == 0) ? 0u : 1u);
+          }
+          mma_commit(bar_ve + 8 * vs);
         }
-        mma_commit(bar_ve + 8 * st);
-        if (t == ntiles - 1) mma_commit(bar_o);
+        mma_commit(bar_pfree);
         return true;
       };
-      // Issue order: S(0), S(1), then P.V(t) and S(t+2) for t = 0, 1, ...
-      // S(t+2) reuses the TMEM of S(t) = P(t), so it goes after P.V(t); the
-      // MMAs of one thread run in issue order.
+      // Issue order: S(0); then for each t: S(t+1) (once the softmax has
+      // loaded S(t)) and P.V(t) (once P(t) is in TMEM).
       ok = ok && qk(0);
-      if (ntiles > 1) ok = ok && qk(1);
       for (int t = 0; ok && t < ntiles; ++t) {
+        if (t + 1 < ntiles) {
+          ok = mbar_wait(bar_sfree, t & 1, &abort_flag) && qk(t + 1);
+          if (!ok) break;
+        }
         ok = pv(t);
-        if (ok && t + 2 < ntiles) ok = qk(t + 2);
       }
       if (!ok) {
         abort_flag = 1;
@@ -270,7 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------- softmax warps ----
-    const int hh = warp >> 2;                    // half: keys 64 hh .. 64 hh + 63 of each tile
+    const int hh = warp >> 2;                    // half: keys 128 hh .. 128 hh + 127 of each tile
     const int r = (warp & 3) * 32 + lane;        // row = TMEM lane
     const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tL = tbase + lane_bits;       // this lane's column 0
@@ -283,74 +293,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float mrow = -INFINITY, lhalf = 0.f;  // running max (same in both halves), this half's sum
     bool ok = true;
 
-    // Q row r, dims 64 hh .. 64 hh + 63 (swizzled box hh of the Q tile),
-    // into TMEM columns kColQ + 32 hh .. as bf16 pairs
-    if (ntiles > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, &abort_flag));
-      uint32_t qv[32];
-      const uint32_t box = sQ + hh * (kTcQBytes / 2) + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t a0, a1, a2, a3;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                     : "r"(box + ((c ^ (r & 7)) << 4)));
-        qv[4 * c] = a0;
-        qv[4 * c + 1] = a1;
-        qv[4 * c + 2] = a2;
-        qv[4 * c + 3] = a3;
-      }
-      tmem_st32(tL + kColQ + 32 * hh, qv);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_qt);
-    }
-
-    // Every warp runs every tile's two named barriers; after a timeout a warp
+    // Every warp runs every tile's named barriers; after a timeout a warp
     // keeps doing so without touching TMEM (its results are dropped).
     for (int t = 0; t < ntiles; ++t) {
-      const int e = t & 1;
-      const uint32_t tS = tL + 128 * e;
       // tcgen05.ld/st below are warp-collective: the whole warp goes on or stops
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_s + 8 * e, (t >> 1) & 1, &abort_flag));
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_s, t & 1, &abort_flag));
       tc_fence_after();
-      const int32_t kp0 = tile_kp0(ti, t) + 64 * hh;  // first key of this half
-      const bool need_mask = (kp0 < 0) || (kp0 + 63 > ti.qa) ||
+      const int32_t kp0 = tile_kp0(ti, t) + 128 * hh;  // first key of this half
+      const bool need_mask = (kp0 < 0) || (kp0 + 127 > ti.qa) ||
                              (local && kp0 < ti.qz - p.window + 1);
-      uint32_t v[2][32];
+      uint32_t v[4][32];
       if (ok) {
-        tmem_ld32(tS + 64 * hh, v[0]);
-        tmem_ld32(tS + 64 * hh + 32, v[1]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tL + 128 * hh + 32 * c, v[c]);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[0][j] = v[1][j] = 0xff800000u;
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[c][j] = 0xff800000u;
       }
+      // S is in registers: the next tile's S = Q K^T may overwrite it
+      tc_fence_before();
+      mbar_arrive(bar_sfree);
       if (need_mask) {
         // keys kp0 + j are visible for j in [jlo, jhi]; the rest become -inf
         const int32_t jlo = max(max(wlo, 0), kp0) - kp0;
         const int32_t jhi = qp - kp0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int32_t jj = 32 * c + j;
             v[c][j] = (jj < jlo || jj > jhi) ? 0xff800000u : v[c][j];
           }
       }
-      float mx2[2];
+      float mx4[4];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 4; ++c) {
         float a = fmax3(__uint_as_float(v[c][0]), __uint_as_float(v[c][1]),
                         __uint_as_float(v[c][2]));
 #pragma unroll
         for (int j = 3; j < 31; j += 2)
           a = fmax3(a, __uint_as_float(v[c][j]), __uint_as_float(v[c][j + 1]));
-        mx2[c] = fmaxf(a, __uint_as_float(v[c][31]));
+        mx4[c] = fmaxf(a, __uint_as_float(v[c][31]));
       }
-      // the row's max over both halves (every S value is in registers, so P
-      // may overwrite S after this barrier)
-      red_x[hh][r] = fmaxf(mx2[0], mx2[1]);
+      red_x[hh][r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       asm volatile("bar.sync 1, 256;" ::: "memory");
       const float mx = fmaxf(red_x[0][r], red_x[1][r]);
       asm volatile("bar.sync 2, 256;" ::: "memory");  // red_x is reused next tile
@@ -362,12 +350,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       lhalf *= alpha;
       const float muse = (mrow == -INFINITY) ? 0.f : mrow;
-      // P = 2^(s*scale*log2e - m) as bf16 pairs: keys 64 hh + 2c.. -> column 32 hh + c
+      // P = 2^(s*scale*log2e - m) as bf16 pairs
       const uint64_t sc2 = f32x2(sl2, sl2), nm2 = f32x2(-muse, -muse);
       uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pk[4][16];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
+      for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(v[c][j]), __uint_as_float(v[c][j + 1])),
@@ -376,9 +364,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           f32x2_split(x2, x0, x1);
           const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
           ls2[(j >> 1) & 3] = add_f32x2(ls2[(j >> 1) & 3], f32x2(e0, e1));
-          pk[j >> 1] = pack_bf16x2(e0, e1);
+          pk[c][j >> 1] = pack_bf16x2(e0, e1);
         }
-        if (ok) tmem_st16(tS + 32 * hh + 16 * c, pk);
       }
       {
         const uint64_t t2 = add_f32x2(add_f32x2(ls2[0], ls2[1]), add_f32x2(ls2[2], ls2[3]));
@@ -386,32 +373,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         f32x2_split(t2, a0, a1);
         lhalf += a0 + a1;
       }
-      // Rare: the running max grew by more than 2^8 -- rescale O in TMEM
-      // (this half's 64 columns).  S(t) was issued after P.V(t-2), so that
-      // one has retired, but P.V(t-1) may still run: wait for its V stage
-      // release first.  The next P.V waits for this tile's P arrival below.
-      if (ok && t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        const int pst = (t - 1) % kTcVStages;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar_ve + 8 * pst, ((t - 1) / kTcVStages) & 1, &abort_flag)) && ok;
-        tc_fence_after();
+      // P(t) and the O rescale wait until P.V(t-1) has retired (it reads the
+      // P columns and accumulates into O)
+      if (t > 0)
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_pfree, (t - 1) & 1, &abort_flag));
+      tc_fence_after();
+      if (ok) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t o32[32];
-          tmem_ld32(tL + kColO + 64 * hh + 32 * c, o32);
-          tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_st16(tL + kColP + 64 * hh + 16 * c, pk[c]);
+        // Rare: the running max grew by more than 2^8 -- rescale this half's
+        // 64 columns of O.
+        if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o32[j] = __float_as_uint(__uint_as_float(o32[j]) * alpha);
-          tmem_st32(tL + kColO + 64 * hh + 32 * c, o32);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o32[32];
+            tmem_ld32(tL + kColO + 64 * hh + 32 * c, o32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o32[j] = __float_as_uint(__uint_as_float(o32[j]) * alpha);
+            tmem_st32(tL + kColO + 64 * hh + 32 * c, o32);
+          }
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_p + 8 * e);
+      mbar_arrive(bar_p);
     }
 
     // ----------------------------------------------------------- epilogue ----
-    if (ok && ntiles > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_o, 0, &abort_flag))) ok = false;
+    if (ntiles > 0)
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_pfree, (ntiles - 1) & 1, &abort_flag));
     tc_fence_after();
     // the row sum: both halves' partial sums (same running max)
     red_x[hh][r] = lhalf;

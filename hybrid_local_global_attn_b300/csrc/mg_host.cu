@@ -490,18 +490,19 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
     sp.rope = rope_turns(layer->rope_theta);
     if (launch_rope_stage(sp, s) != cudaSuccess) return MG_ERR_CUDA;
     qsrc = sp.qs;
-    if (!map_rows(&tka, sp.ks, w.R, outer, kTcKeys) || !map_rows(&tva, sp.vs, w.R, outer, kTcKeys))
+    if (!map_rows(&tka, sp.ks, w.R, outer, kTcKeys) || !map_rows(&tva, sp.vs, w.R, outer, kTcVRows))
       return MG_ERR_CUDA;
     tkb = tka;
     tvb = tva;
   } else {
     if (!map_rows(&tka, cache->k, cache->slots, outer, kTcKeys) ||
-        !map_rows(&tva, cache->v, cache->slots, outer, kTcKeys))
+        !map_rows(&tva, cache->v, cache->slots, outer, kTcVRows))
       return MG_ERR_CUDA;
     const uint64_t dims[4] = {static_cast<uint64_t>(kD), kHkv, static_cast<uint64_t>(n),
                               static_cast<uint64_t>(B)};
-    const uint32_t box[4] = {64, 1, kTcKeys, 1};
-    if (!make_map(&tkb, k_new, 4, dims, box) || !make_map(&tvb, v_new, 4, dims, box))
+    const uint32_t kbox[4] = {64, 1, kTcKeys, 1};
+    const uint32_t vbox[4] = {64, 1, kTcVRows, 1};
+    if (!make_map(&tkb, k_new, 4, dims, kbox) || !make_map(&tvb, v_new, 4, dims, vbox))
       return MG_ERR_CUDA;
   }
   {

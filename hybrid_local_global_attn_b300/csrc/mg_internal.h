@@ -43,16 +43,20 @@ constexpr int kMaxLocalTokens = 16;
 constexpr int kLocMaxTpc = 6;  // query tokens one CTA takes in turn
 
 // tcgen05 attention (verify + prefill): one query tile of 128 rows
-// (8 positions x 16 heads) per CTA, key tiles of 128.
+// (8 positions x 16 heads) per CTA, key tiles of 256 (S = Q K^T as
+// M128 N256 K16 MMAs: the cost of a tcgen05.mma barely depends on N).
 constexpr int kTcRows = 128;
-constexpr int kTcKeys = 128;
+constexpr int kTcKeys = 256;
+constexpr int kTcVRows = kTcKeys / 2;             // V streams in half tiles
 constexpr int kTcPosPerTile = kTcRows / kGroup;   // 8
 constexpr int kTcPosPerCta = kTcPosPerTile;       // 8
-constexpr int kTcKStages = 2;  // K ring (freed by Q.K^T)
-constexpr int kTcVStages = 4;  // V ring (freed by P.V, which comes a softmax later)
-constexpr int kTcTileBytes = kTcKeys * kRowBytes;  // 32 KB (two 64-dim boxes)
-constexpr int kTcQBytes = kTcRows * kRowBytes;     // 32 KB
-constexpr int kTcSmem = kTcQBytes + (kTcKStages + kTcVStages) * kTcTileBytes + 1024 + 256;
+constexpr int kTcKStages = 2;                     // K tiles (64 KB)
+constexpr int kTcVStages = 2;                     // V half tiles (32 KB)
+constexpr int kTcKTileBytes = kTcKeys * kRowBytes;   // 64 KB (two 64-dim boxes)
+constexpr int kTcVTileBytes = kTcVRows * kRowBytes;  // 32 KB
+constexpr int kTcQBytes = kTcRows * kRowBytes;       // 32 KB
+constexpr int kTcSmem =
+    kTcQBytes + kTcKStages * kTcKTileBytes + kTcVStages * kTcVTileBytes + 1024 + 256;
 constexpr int kTcThreads = 320;  // warps 0-3 / 4-7 softmax of even / odd key tiles, 8 TMA, 9 MMA
 constexpr int kTcMaxSplits = 160;
 
