@@ -55,7 +55,10 @@ def run_verify(mg, kind, cache, p0s, q, kn, vn, max_len):
 
 @pytest.mark.parametrize("kind", [0, 1])
 @pytest.mark.parametrize("p0s,n", [([0, 100], 16), ([2100, 1], 16), ([5000, 130], 5),
-                                   ([2032, 2048], 16), ([700, 300], 1)])
+                                   ([2032, 2048], 16), ([700, 300], 1),
+                                   # blocks that wrap the ring inside themselves, a second
+                                   # group of 3 tokens, three sequences
+                                   ([2040, 4090, 9], 11), ([6139, 31], 13), ([4095, 2047], 2)])
 def test_verify_against_oracle(mg, kind, p0s, n):
     B = len(p0s)
     T = max(p0s) + n
