@@ -104,8 +104,10 @@ size_t mg_cache_bytes(int32_t kind, int32_t batch, int32_t capacity);
 /* Host-only.  Workspace bytes that mg_attn_decode (op MG_OP_DECODE, n = 1),
  * mg_attn_verify (MG_OP_VERIFY, n = draft tokens) or mg_attn_prefill
  * (MG_OP_PREFILL, n = chunk tokens) need for this layer, batch and
- * max_len.  The workspace holds split-KV partials and, for local layers,
- * RoPE-rotated copies of the queries and of the keys in the window.
+ * max_len.  The workspace holds split-KV partials (global decode, global
+ * verify) and, for local prefill, RoPE-rotated copies of the queries and
+ * of the keys in the window; local decode and local verify merge inside a
+ * thread-block cluster and need none.
  * Returns 0 if no workspace is needed, (size_t)-1 for bad arguments. */
 size_t mg_workspace_bytes(int32_t op, const mg_layer *layer, int32_t batch,
                           int32_t n, int32_t max_len);
