@@ -5,6 +5,10 @@
 // 解释了 Meta 如何在 24 GB 的容量内容纳 Muse Glimmer", section
 // "窄缓存为长上下文留出空间" (evict or cyclically reuse stale entries).
 // Pure data movement: one thread moves one 16-byte chunk of K and of V.
+// The same kernel commits a verified draft block: only the accepted prefix
+// of each sequence is written ("第三招：D-Flash投机解码实现3倍提速",
+// kongchang.com: the main model checks the drafted block in one pass and
+// keeps what it accepts).
 #include "mg_internal.h"
 #include "mg_ptx.cuh"
 
@@ -21,14 +25,29 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   const int g = static_cast<int>(idx >> 4) & 1;      // KV head
   const int c = static_cast<int>(idx & 15);          // 16-byte chunk of the row
   const int32_t pos0 = p.pos0[b];
-  if (pos0 < 0) {
-    if (idx == 0) set_err(p.err, MG_DERR_POSITION);
+  // Tokens of this sequence to write: all n, or the committed prefix.
+  int32_t nb = p.n;
+  bool skip = pos0 < 0;
+  uint32_t why = MG_DERR_POSITION;
+  if (p.count != nullptr) {
+    nb = p.count[b];
+    if (nb < 0 || nb > p.n) {
+      skip = true;
+      why = MG_DERR_COUNT;
+    } else if (static_cast<int64_t>(pos0) + nb > 0x7fffffff) {
+      skip = true;  // the next position would not fit an int32
+    }
+    if (idx == 0 && p.pos_next != nullptr) p.pos_next[b] = skip ? pos0 : pos0 + nb;
+  }
+  if (skip) {
+    if (idx == 0) set_err(p.err, why);
     return;
   }
+  if (t >= nb) return;  // rejected draft: never written
   // A ring keeps only the last `slots` tokens of this call; skipping the
   // earlier ones gives the same final state as appending one at a time and
   // avoids two writers racing for one slot.
-  if (p.kind == 0 && t < p.n - p.slots) return;
+  if (p.kind == 0 && t < nb - p.slots) return;
   const int64_t pos = static_cast<int64_t>(pos0) + t;
   int64_t slot;
   if (p.kind == 0) {

@@ -353,6 +353,36 @@ int mg_kv_append(const mg_layer *layer, const mg_cache *cache, const int32_t *d_
   p.k_cache = static_cast<__nv_bfloat16 *>(cache->k);
   p.v_cache = static_cast<__nv_bfloat16 *>(cache->v);
   p.pos0 = d_pos0;
+  p.count = nullptr;
+  p.pos_next = nullptr;
+  p.err = d_err;
+  p.batch = cache->batch;
+  p.n = n;
+  p.slots = cache->slots;
+  p.kind = layer->kind;
+  return launch_status(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
+}
+
+int mg_kv_commit(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos0, int32_t n,
+                 const int32_t *d_count, const void *k_new, const void *v_new,
+                 int32_t *d_pos_next, uint32_t *d_err, void *stream) {
+  int st = check_layer(layer);
+  if (st != MG_OK) return st;
+  if ((st = check_cache(layer, cache)) != MG_OK) return st;
+  if (n < 0 || d_pos0 == nullptr || d_count == nullptr || d_err == nullptr) return MG_ERR_INVALID;
+  if (d_pos_next != nullptr && static_cast<const void *>(d_pos_next) == static_cast<const void *>(d_pos0))
+    return MG_ERR_INVALID;
+  if (n == 0) return MG_OK;
+  if (k_new == nullptr || v_new == nullptr || !aligned16(k_new) || !aligned16(v_new))
+    return MG_ERR_INVALID;
+  AppendParams p;
+  p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  p.k_cache = static_cast<__nv_bfloat16 *>(cache->k);
+  p.v_cache = static_cast<__nv_bfloat16 *>(cache->v);
+  p.pos0 = d_pos0;
+  p.count = d_count;
+  p.pos_next = d_pos_next;
   p.err = d_err;
   p.batch = cache->batch;
   p.n = n;

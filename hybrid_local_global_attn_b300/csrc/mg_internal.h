@@ -70,6 +70,10 @@ struct AppendParams {
   const __nv_bfloat16 *k_new, *v_new;  // [B][n][2][128]
   __nv_bfloat16 *k_cache, *v_cache;    // [B][2][slots][128]
   const int32_t *pos0;
+  // speculative commit: keep the first count[b] of the n tokens (nullptr:
+  // all n) and optionally write pos0[b] + count[b] to pos_next
+  const int32_t *count;
+  int32_t *pos_next;
   uint32_t *err;
   int32_t batch, n, slots, kind;
 };

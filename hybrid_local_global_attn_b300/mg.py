@@ -54,11 +54,12 @@ lib.mg_status_str.restype = ctypes.c_char_p
 lib.mg_layer_kind.argtypes = [_i32]
 lib.mg_layer_kind.restype = ctypes.c_int
 lib.mg_kv_append.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P]
+lib.mg_kv_commit.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, _P]
 lib.mg_attn_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_append_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_verify.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_prefill.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
-for _f in (lib.mg_kv_append, lib.mg_attn_decode, lib.mg_append_decode, lib.mg_attn_verify,
+for _f in (lib.mg_kv_append, lib.mg_kv_commit, lib.mg_attn_decode, lib.mg_append_decode, lib.mg_attn_verify,
            lib.mg_attn_prefill):
     _f.restype = ctypes.c_int
 
@@ -133,6 +134,16 @@ def mg_kv_append(layer, cache: KVCache, pos0, k_new, v_new, err, stream=None):
     _call(lib.mg_kv_append, ctypes.byref(layer), ctypes.byref(cache.struct), _ptr(pos0, torch.int32),
           int(k_new.shape[1]), _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
           _ptr(err, torch.int32), _stream(stream))
+
+
+def mg_kv_commit(layer, cache: KVCache, pos0, count, k_new, v_new, err, pos_next=None,
+                 stream=None):
+    """Write the first count[b] tokens of a verified block (k_new/v_new
+    [B][n][2][128]) at pos0[b]; optionally pos_next[b] = pos0[b] + count[b]."""
+    _call(lib.mg_kv_commit, ctypes.byref(layer), ctypes.byref(cache.struct), _ptr(pos0, torch.int32),
+          int(k_new.shape[1]), _ptr(count, torch.int32), _ptr(k_new, torch.bfloat16),
+          _ptr(v_new, torch.bfloat16), _ptr(pos_next, torch.int32), _ptr(err, torch.int32),
+          _stream(stream))
 
 
 def mg_attn_decode(layer, cache: KVCache, pos, max_len, q, o, ws, err, stream=None):

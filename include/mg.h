@@ -71,6 +71,7 @@ typedef enum {
 /* Bits OR-ed into *d_err by the kernels. */
 #define MG_DERR_POSITION 1u /* a device position was negative or beyond max_len / capacity */
 #define MG_DERR_TIMEOUT 2u  /* a pipeline wait ran out its time limit; the CTA gave up */
+#define MG_DERR_COUNT 4u    /* a commit count was outside [0, n]; that sequence was left as it was */
 
 /* One attention layer.  kind = MG_LOCAL requires window == 2048 and a
  * positive rope_theta (10000 is the value used throughout; the pages do not
@@ -134,6 +135,32 @@ int mg_layer_kind(int32_t l);
 int mg_kv_append(const mg_layer *layer, const mg_cache *cache,
                  const int32_t *d_pos0, int32_t n, const void *k_new,
                  const void *v_new, uint32_t *d_err, void *stream);
+
+/*
+ * Speculative commit [P1 §04; P4 "第三招：D-Flash投机解码实现3倍提速"]: the
+ * main model checks a block of drafted tokens in one mg_attn_verify pass and
+ * keeps the longest accepted prefix.  This call writes the first count[b]
+ * tokens of the block that verify scored (positions p0[b] .. p0[b]+count[b]-1:
+ * the anchor token and the accepted drafts) into the cache and never writes
+ * the rejected ones, so rolling a rejected draft back costs nothing and the
+ * ring slots it would have reused keep their old keys.  The cache afterwards
+ * equals mg_kv_append of those count[b] tokens; count[b] == 0 leaves
+ * sequence b as it was.  Acceptance depends on verify's output (through the
+ * caller's sampling), so this is a separate call after verify, not part of it.
+ *   k_new, v_new : bf16 [batch][n][2][128] (device), the block given to verify
+ *   d_pos0       : int32 [batch] (device), the block's first position
+ *   d_count      : int32 [batch] (device), tokens to keep; a count outside
+ *                  [0, n] skips sequence b and flags MG_DERR_COUNT
+ *   d_pos_next   : int32 [batch] (device) or NULL; receives p0[b] + count[b]
+ *                  (p0[b] itself when sequence b was skipped).  Must not alias
+ *                  d_pos0 (MG_ERR_INVALID): every CTA of a sequence reads p0.
+ *   n            : block size, 0 <= n; n == 0 is a no-op
+ * Positions are checked as in mg_kv_append (MG_DERR_POSITION).
+ */
+int mg_kv_commit(const mg_layer *layer, const mg_cache *cache,
+                 const int32_t *d_pos0, int32_t n, const int32_t *d_count,
+                 const void *k_new, const void *v_new, int32_t *d_pos_next,
+                 uint32_t *d_err, void *stream);
 
 /*
  * Decode attention for one query token per sequence [P1 §04: decode is

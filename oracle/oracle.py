@@ -109,6 +109,18 @@ def cache_append(kind, k_cache, v_cache, pos0, k_new, v_new):
         raise ValueError(f"mg_oracle_cache_append failed: {rc}")
 
 
+def cache_commit(kind, k_cache, v_cache, pos0, count, k_block, v_block):
+    """Speculative commit ("Meta开源30B模型Muse Glimmer：一张显卡跑本地Agent的实战解析",
+    section "第三招：D-Flash投机解码实现3倍提速": the main model checks a drafted
+    block in one pass and keeps what it accepts).  The kept tokens are the first
+    `count` of the block; the cache must then hold the linear history of kept
+    tokens only, which is the append of that prefix and nothing else."""
+    if not 0 <= count <= len(k_block):
+        raise ValueError(f"commit count {count} outside [0, {len(k_block)}]")
+    if count:
+        cache_append(kind, k_cache, v_cache, pos0, k_block[:count], v_block[:count])
+
+
 def decode_from_cache(lay, k_cache, v_cache, p, q):
     kc = bits(k_cache); vc = bits(v_cache); qq = bits(q)
     slots = kc.shape[1]

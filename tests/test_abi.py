@@ -108,6 +108,14 @@ def test_host_side_rejections_launch_nothing(mg):
     assert lib.mg_kv_append(by(L), by(cache), fake, -1, fake, fake, fake, None) == 1
     # n == 0 is a no-op
     assert lib.mg_kv_append(by(L), by(cache), fake, 0, fake, fake, fake, None) == 0
+    # commit: counts are required; the next-position output must not alias pos0
+    other = ctypes.c_void_p(0x3000)
+    assert lib.mg_kv_commit(by(L), by(cache), fake, 4, None, fake, fake, None, fake, None) == 1
+    assert lib.mg_kv_commit(by(L), by(cache), fake, 4, other, fake, fake, fake, fake, None) == 1
+    assert lib.mg_kv_commit(by(L), by(cache), fake, -1, other, fake, fake, None, fake, None) == 1
+    assert lib.mg_kv_commit(by(L), by(cache), fake, 4, other, ctypes.c_void_p(0x1008), fake,
+                            None, fake, None) == 1
+    assert lib.mg_kv_commit(by(L), by(cache), fake, 0, other, fake, fake, None, fake, None) == 0
     # local layer with a cache that is not a 2048-slot ring
     c2 = mg.mg_cache(0x10000, 0x20000, 1, 4096)
     assert lib.mg_kv_append(by(L), by(c2), fake, 1, fake, fake, fake, None) == 2

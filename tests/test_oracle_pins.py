@@ -145,6 +145,47 @@ def test_cache_append_slots_bitwise():
         orc.cache_append(orc.GLOBAL, gc, gv, T, k[:1], v[:1])
 
 
+@pytest.mark.parametrize("kind", [orc.LOCAL, orc.GLOBAL])
+def test_commit_rolls_back_rejected_drafts(kind):
+    # A speculative round [P4 第三招]: a 16-token block at p0 = 2040 (it
+    # crosses the ring wrap) of which only the first 5 tokens are kept; the
+    # other 11 are junk.  Afterwards the ring must still hold positions
+    # p0 + i - 2048 for the rejected i (the slots the junk would have
+    # reused), and decoding from the cache must equal attention over the
+    # linear history of kept tokens, at the last kept position and after the
+    # true continuation is appended.
+    p0, n, keep, T = 2040, 16, 5, 2070
+    k, v = rand_hist(T, 21)
+    jk, jv = rand_hist(n, 22)  # junk drafts
+    blk_k = torch.cat([k[p0:p0 + keep], jk[keep:]])
+    blk_v = torch.cat([v[p0:p0 + keep], jv[keep:]])
+    slots = 2048 if kind == orc.LOCAL else T
+    kc = np.zeros((2, slots, 128), np.uint16)
+    vc = np.zeros((2, slots, 128), np.uint16)
+    orc.cache_append(kind, kc, vc, 0, k[:p0], v[:p0])
+    orc.cache_commit(kind, kc, vc, p0, keep, blk_k, blk_v)
+    kb = orc.bits(k)
+    for i in range(keep, n):
+        s = (p0 + i) % slots
+        old = p0 + i - 2048  # the position a local slot held before the block
+        want = kb[old] if kind == orc.LOCAL and old >= 0 else np.zeros_like(kb[0])
+        assert np.array_equal(kc[:, s, :], want), f"rejected draft {i} reached slot {s}"
+    lay = orc.layer(kind)
+    for p in (p0 + keep - 1, T - 1):
+        if p == T - 1:
+            orc.cache_append(kind, kc, vc, p0 + keep, k[p0 + keep:], v[p0 + keep:])
+        q = synth.randn_bf16((32, 128), 2000 + p)
+        got = orc.decode_from_cache(lay, kc, vc, p, q)
+        ref = orc.attention(lay, k[:p + 1], v[:p + 1], [p], q.unsqueeze(0))[0]
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    # keeping nothing changes nothing; a count beyond the block is refused
+    before = kc.copy()
+    orc.cache_commit(kind, kc, vc, T, 0, blk_k, blk_v)
+    assert np.array_equal(kc, before)
+    with pytest.raises(ValueError):
+        orc.cache_commit(kind, kc, vc, T, n + 1, blk_k, blk_v)
+
+
 @pytest.mark.parametrize("kind,p", [(orc.LOCAL, 0), (orc.LOCAL, 100), (orc.LOCAL, 2046),
                                     (orc.LOCAL, 2047), (orc.LOCAL, 3000), (orc.GLOBAL, 3000)])
 def test_zero_keys_give_window_mean(kind, p):
