@@ -23,6 +23,9 @@
 //    lse), written to the workspace; a combine kernel merges the splits.
 //  * Optionally the token's own K/V is appended by the CTA whose split holds
 //    its slot, before that tile is loaded (mg_append_decode).
+//  * The cache is linear or paged (a page table maps each 256-multiple run
+//    of positions of a sequence to a page of a shared pool); a 64-key tile
+//    always lies inside one page.
 #include "mg_internal.h"
 #include "mg_ptx.cuh"
 #include "mma_frag.cuh"
@@ -73,11 +76,16 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     c = (c + kDecTile - 1) / kDecTile * kDecTile;
     const int32_t first = split * c;
     const int32_t upto = min(first + min(c, kDecPrefetchTiles * kDecTile), min(p.max_len, p.slots));
-    for (int32_t row = first; row < upto; row += kDecTile)
+    // (a paged cache's table may still be changing: a stale entry only
+    // warms the wrong page)
+    for (int32_t row = first; row < upto; row += kDecTile) {
+      int32_t r, o;
+      cache_coord(p.map, b, g, row, &r, &o, nullptr);
       for (int x = 0; x < 2; ++x) {
-        tma_prefetch_l2_3d(&tk, 64 * x, row, b * kHkv + g);
-        tma_prefetch_l2_3d(&tv, 64 * x, row, b * kHkv + g);
+        tma_prefetch_l2_3d(&tk, 64 * x, r, o);
+        tma_prefetch_l2_3d(&tv, 64 * x, r, o);
       }
+    }
   }
   __syncthreads();
   pdl_wait();
@@ -110,7 +118,9 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       // proxy, hence the proxy fence after the stores).
       if (fused_here) {
         const size_t src = (static_cast<size_t>(b) * kHkv + g) * kD;
-        const size_t dst = ((static_cast<size_t>(b) * kHkv + g) * p.slots + pq) * kD;
+        int32_t r, o;
+        cache_coord(p.map, b, g, pq, &r, &o, lane == 0 ? p.err : nullptr);
+        const size_t dst = (static_cast<size_t>(o) * p.map.rows + r) * kD;
         const int c = lane & 15;
         if (lane < 16)
           reinterpret_cast<uint4 *>(p.k_cache + dst)[c] =
@@ -122,8 +132,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         __syncwarp();
       }
       if (lane == 0) {
-        const int32_t c2 = b * kHkv + g;
         int issued = 0;
+        // a tile never straddles two pages (64 | split start, 256 | page size);
+        // the page entry is reloaded only when the tile enters a new page
+        int32_t cur_lp = -1, cur_row0 = 0, cur_outer = b * kHkv + g;
         for (int t = 0; t < ntiles; ++t) {
           const int st = t % NS;
           if (t >= NS && !mbar_wait(bar_empty + 8 * st, ((t / NS) - 1) & 1, &abort_flag)) {
@@ -133,12 +145,19 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           }
           const uint32_t dst = smem_base + st * kDecStageBytes;
           const uint32_t fb = bar_full + 8 * st;
-          const int32_t row = s0 + t * kDecTile;
+          const int32_t pos = s0 + t * kDecTile;
+          if (p.map.table != nullptr && pos / p.map.rows != cur_lp) {
+            cur_lp = pos / p.map.rows;
+            int32_t r;
+            cache_coord(p.map, b, g, pos, &r, &cur_outer, p.err);
+            cur_row0 = cur_lp * p.map.rows;
+          }
+          const int32_t row = pos - cur_row0;
           mbar_arrive_expect_tx(fb, kDecStageBytes);
-          tma_load_3d(dst, &tk, fb, 0, row, c2);
-          tma_load_3d(dst + 8192, &tk, fb, 64, row, c2);
-          tma_load_3d(dst + 16384, &tv, fb, 0, row, c2);
-          tma_load_3d(dst + 24576, &tv, fb, 64, row, c2);
+          tma_load_3d(dst, &tk, fb, 0, row, cur_outer);
+          tma_load_3d(dst + 8192, &tk, fb, 64, row, cur_outer);
+          tma_load_3d(dst + 16384, &tv, fb, 0, row, cur_outer);
+          tma_load_3d(dst + 24576, &tv, fb, 64, row, cur_outer);
           ++issued;
         }
         // Never leave the CTA with copies in flight: wait (bounded) for the

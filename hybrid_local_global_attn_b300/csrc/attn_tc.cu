@@ -51,12 +51,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct TileInfo {
   int32_t c0, qa, qz;     // block start, first and last valid query position
+  int32_t cbase;          // cache tiles end here: c0, or c0 rounded up to 256 (paged)
   int32_t ncache, nnew;   // tiles from the cache part / the block part
-  int32_t u_begin, v_lo;  // first cache tile index (from c0 down), first block tile
+  int32_t u_begin, v_lo;  // first cache tile index (from cbase down), first block tile
 };
 
 __device__ __forceinline__ int32_t tile_kp0(const TileInfo &ti, int t) {
-  if (t < ti.ncache) return ti.c0 - kTcKeys * (ti.u_begin + t + 1);
+  if (t < ti.ncache) return ti.cbase - kTcKeys * (ti.u_begin + t + 1);
   return ti.c0 + kTcKeys * (ti.v_lo + (t - ti.ncache));
 }
 
@@ -104,6 +105,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   ti.c0 = p.pos0[b];
   const bool bad = ti.c0 < 0 || static_cast<int64_t>(ti.c0) + p.n > p.max_len ||
                    (!p.staged && ti.c0 > p.slots);
+  // A paged cache's tiles are aligned to 256 so that each lies in one page;
+  // the top one then reaches past c0 and its keys >= c0 are masked.
+  ti.cbase = (p.map.table != nullptr && !local) ? (ti.c0 + kTcKeys - 1) / kTcKeys * kTcKeys : ti.c0;
   ti.qa = ti.c0 + kTcPosPerCta * qb;
   ti.qz = min(ti.qa + kTcPosPerCta - 1, ti.c0 + p.n - 1);
   ti.ncache = ti.nnew = ti.u_begin = ti.v_lo = 0;
@@ -162,6 +166,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive_expect_tx(bar_q, kTcQBytes);
       for (int x = 0; x < 2; ++x)
         tma_load_4d(sQ + x * (kTcQBytes / 2), &tq, bar_q, 64 * x, kGroup * g, q_t0, b);
+      // Cache tile t lies in rows [crow0, crow0 + 256) of outer index couter
+      // (linear: rows from 0 of the sequence's head; paged: its page).  K of
+      // tile t + 1 is issued before V of tile t, so two tiles' entries live.
+      int32_t crow0[2] = {0, 0}, couter[2] = {b * kHkv + g, b * kHkv + g};
+      auto locate = [&](int t) {
+        if (p.map.table == nullptr || t >= ti.ncache) return;
+        const int32_t kp0 = tile_kp0(ti, t);
+        int32_t r, o;
+        cache_coord(p.map, b, g, kp0, &r, &o, p.err);
+        crow0[t & 1] = kp0 - r;
+        couter[t & 1] = o;
+      };
       // keys kp0.. (rows) of K or V into dst (two 64-dim boxes), completing on fb
       auto load = [&](bool is_v, int t, int32_t kp0, uint32_t dst, uint32_t bytes, uint32_t fb) {
         const CUtensorMap *ma = is_v ? &tva : &tka;
@@ -172,7 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (p.staged)
             tma_load_3d(d, ma, fb, 64 * x, kp0 - ti.c0 + kWindow, b * kHkv + g);
           else if (t < ti.ncache)
-            tma_load_3d(d, ma, fb, 64 * x, kp0, b * kHkv + g);
+            tma_load_3d(d, ma, fb, 64 * x, kp0 - crow0[t & 1], couter[t & 1]);
           else
             tma_load_4d(d, mb, fb, 64 * x, g, kp0 - ti.c0, b);
         }
@@ -185,6 +201,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (t >= kTcKStages &&
             !mbar_wait(bar_ke + 8 * ks, ((t / kTcKStages) - 1) & 1, &abort_flag))
           return false;
+        locate(t);
         load(false, t, tile_kp0(ti, t), sK + ks * kTcKTileBytes, kTcKTileBytes, bar_kf + 8 * ks);
         ++issued_k;
         return true;
@@ -300,8 +317,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_s, t & 1, &abort_flag));
       tc_fence_after();
       const int32_t kp0 = tile_kp0(ti, t) + 128 * hh;  // first key of this half
+      const bool cache_tile = t < ti.ncache;
       const bool need_mask = (kp0 < 0) || (kp0 + 127 > ti.qa) ||
-                             (local && kp0 < ti.qz - p.window + 1);
+                             (local && kp0 < ti.qz - p.window + 1) ||
+                             (cache_tile && kp0 + 127 >= ti.c0);
       uint32_t v[4][32];
       if (ok) {
 #pragma unroll
@@ -319,7 +338,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (need_mask) {
         // keys kp0 + j are visible for j in [jlo, jhi]; the rest become -inf
         const int32_t jlo = max(max(wlo, 0), kp0) - kp0;
-        const int32_t jhi = qp - kp0;
+        const int32_t jhi = (cache_tile ? min(qp, ti.c0 - 1) : qp) - kp0;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll

@@ -14,11 +14,8 @@
 
 namespace mg {
 
-__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
-  pdl_wait();  // positions and rows may come from the previous kernel
-  pdl_launch_dependents();
-  const int b = blockIdx.y;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+// Thread idx of sequence b moves one 16-byte chunk of one K row and one V row.
+__device__ __forceinline__ void append_chunk(const AppendParams &p, int b, int64_t idx) {
   const int64_t total = static_cast<int64_t>(p.n) * (kHkv * 16);
   if (idx >= total) return;
   const int32_t t = static_cast<int32_t>(idx >> 5);  // token within the call
@@ -60,11 +57,44 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
     slot = pos;
   }
   const size_t src = ((static_cast<size_t>(b) * p.n + t) * kHkv + g) * kD + c * 8;
-  const size_t dst = ((static_cast<size_t>(b) * kHkv + g) * p.slots + slot) * kD + c * 8;
+  size_t dst;
+  if (p.kind == 0) {
+    dst = ((static_cast<size_t>(b) * kHkv + g) * p.slots + slot) * kD + c * 8;
+  } else {
+    int32_t row, outer;
+    cache_coord(p.map, b, g, static_cast<int32_t>(slot), &row, &outer, c == 0 ? p.err : nullptr);
+    dst = (static_cast<size_t>(outer) * p.map.rows + row) * kD + c * 8;
+  }
   const uint4 kv = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src));
   const uint4 vv = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src));
   *reinterpret_cast<uint4 *>(p.k_cache + dst) = kv;
   *reinterpret_cast<uint4 *>(p.v_cache + dst) = vv;
+}
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  pdl_wait();  // positions and rows may come from the previous kernel
+  pdl_launch_dependents();
+  append_chunk(p, blockIdx.y, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
+}
+
+// One commit into many layers' caches: blockIdx.z is the layer.  Only the
+// first layer writes the next positions; every layer checks the counts.
+__global__ void __launch_bounds__(256)
+    kv_commit_layers_kernel(const __grid_constant__ CommitLayersParams cp) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int l = blockIdx.z;
+  AppendParams p = cp.common;
+  const size_t off = static_cast<size_t>(l) * cp.layer_stride;
+  p.k_new += off;
+  p.v_new += off;
+  p.k_cache = cp.k_cache[l];
+  p.v_cache = cp.v_cache[l];
+  p.slots = cp.slots[l];
+  p.kind = cp.kind[l];
+  p.map = cp.map[l];
+  if (l != 0) p.pos_next = nullptr;
+  append_chunk(p, blockIdx.y, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
 }
 
 cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s) {
@@ -73,6 +103,15 @@ cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s) {
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(p.batch));
   return launch_pdl(kv_append_kernel, grid, dim3(256), 0, s, p);
+}
+
+cudaError_t launch_kv_commit_layers(const CommitLayersParams &p, cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(p.common.n) * (kHkv * 16);
+  const int64_t blocks = (total + 255) / 256;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(p.common.batch),
+            static_cast<unsigned>(p.layers));
+  return launch_pdl(kv_commit_layers_kernel, grid, dim3(256), 0, s, p);
 }
 
 }  // namespace mg

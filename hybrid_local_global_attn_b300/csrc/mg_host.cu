@@ -185,7 +185,32 @@ int check_cache(const mg_layer *L, const mg_cache *C) {
   if (C->batch < 1 || C->slots < 1) return MG_ERR_INVALID;
   if (L->kind == MG_LOCAL && C->slots != kWindow) return MG_ERR_UNSUPPORTED;
   if (!aligned16(C->k) || !aligned16(C->v)) return MG_ERR_INVALID;
+  if (C->page_table != nullptr) {
+    if (L->kind != MG_GLOBAL) return MG_ERR_UNSUPPORTED;  // the ring is never paged
+    if (C->page_size < kTcKeys || C->page_size % kTcKeys != 0) return MG_ERR_UNSUPPORTED;
+    if (C->slots % C->page_size != 0 || C->num_pages < 1) return MG_ERR_INVALID;
+    if (static_cast<int64_t>(C->num_pages) * kHkv > 0x7fffffff) return MG_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(C->page_table) % 4 != 0) return MG_ERR_INVALID;
+  }
   return MG_OK;
+}
+
+// Rows of a checked cache as the kernels address them.
+CacheMap cache_map(const mg_cache *C) {
+  CacheMap m;
+  const bool paged = C->page_table != nullptr;
+  m.table = C->page_table;
+  m.rows = paged ? C->page_size : C->slots;
+  m.pages_per_seq = paged ? C->slots / C->page_size : 0;
+  m.num_pages = paged ? C->num_pages : 0;
+  return m;
+}
+
+// 3D tensor map (128 dims, rows, outer) over a checked cache's K or V.
+bool map_cache(CUtensorMap *m, const mg_cache *C, const void *base, uint32_t box_rows) {
+  if (C->page_table != nullptr)
+    return map_rows(m, base, C->page_size, static_cast<uint64_t>(C->num_pages) * kHkv, box_rows);
+  return map_rows(m, base, C->slots, static_cast<uint64_t>(C->batch) * kHkv, box_rows);
 }
 
 int splits_decode(int32_t kind, int32_t batch, int32_t max_len) {
@@ -313,6 +338,11 @@ size_t mg_cache_bytes(int32_t kind, int32_t batch, int32_t capacity) {
   return static_cast<size_t>(2) * batch * kHkv * slots * kD * 2;
 }
 
+size_t mg_page_pool_bytes(int32_t num_pages, int32_t page_size) {
+  if (num_pages < 0 || page_size < kTcKeys || page_size % kTcKeys != 0) return 0;
+  return static_cast<size_t>(2) * num_pages * kHkv * page_size * kD * 2;
+}
+
 size_t mg_workspace_bytes(int32_t op, const mg_layer *layer, int32_t batch, int32_t n,
                           int32_t max_len) {
   if (check_layer(layer) != MG_OK) return static_cast<size_t>(-1);
@@ -360,6 +390,7 @@ int mg_kv_append(const mg_layer *layer, const mg_cache *cache, const int32_t *d_
   p.n = n;
   p.slots = cache->slots;
   p.kind = layer->kind;
+  p.map = cache_map(cache);
   return launch_status(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -388,7 +419,48 @@ int mg_kv_commit(const mg_layer *layer, const mg_cache *cache, const int32_t *d_
   p.n = n;
   p.slots = cache->slots;
   p.kind = layer->kind;
+  p.map = cache_map(cache);
   return launch_status(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
+}
+
+int mg_kv_commit_layers(int32_t n_layers, const mg_layer *layers, const mg_cache *caches,
+                        const int32_t *d_pos0, int32_t n, const int32_t *d_count,
+                        const void *k_new, const void *v_new, int32_t *d_pos_next,
+                        uint32_t *d_err, void *stream) {
+  if (n_layers < 1 || n_layers > MG_COMMIT_MAX_LAYERS || layers == nullptr || caches == nullptr)
+    return MG_ERR_INVALID;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    int st = check_layer(&layers[l]);
+    if (st != MG_OK) return st;
+    if ((st = check_cache(&layers[l], &caches[l])) != MG_OK) return st;
+    if (caches[l].batch != caches[0].batch) return MG_ERR_INVALID;
+  }
+  if (n < 0 || d_pos0 == nullptr || d_count == nullptr || d_err == nullptr) return MG_ERR_INVALID;
+  if (d_pos_next != nullptr && static_cast<const void *>(d_pos_next) == static_cast<const void *>(d_pos0))
+    return MG_ERR_INVALID;
+  if (n == 0) return MG_OK;
+  if (k_new == nullptr || v_new == nullptr || !aligned16(k_new) || !aligned16(v_new))
+    return MG_ERR_INVALID;
+  CommitLayersParams p;
+  std::memset(&p, 0, sizeof p);
+  p.common.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  p.common.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  p.common.pos0 = d_pos0;
+  p.common.count = d_count;
+  p.common.pos_next = d_pos_next;
+  p.common.err = d_err;
+  p.common.batch = caches[0].batch;
+  p.common.n = n;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    p.k_cache[l] = static_cast<__nv_bfloat16 *>(caches[l].k);
+    p.v_cache[l] = static_cast<__nv_bfloat16 *>(caches[l].v);
+    p.slots[l] = caches[l].slots;
+    p.kind[l] = layers[l].kind;
+    p.map[l] = cache_map(&caches[l]);
+  }
+  p.layer_stride = static_cast<size_t>(caches[0].batch) * n * kHkv * kD;
+  p.layers = n_layers;
+  return launch_status(launch_kv_commit_layers(p, static_cast<cudaStream_t>(stream)));
 }
 
 static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
@@ -408,9 +480,7 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   if (ws_bytes < w.total || (w.total > 0 && ws == nullptr)) return MG_ERR_WORKSPACE;
   if (w.total > 0 && !aligned16(ws)) return MG_ERR_INVALID;
   CUtensorMap tk, tv;
-  const uint64_t outer = static_cast<uint64_t>(cache->batch) * kHkv;
-  if (!map_rows(&tk, cache->k, cache->slots, outer, kDecTile) ||
-      !map_rows(&tv, cache->v, cache->slots, outer, kDecTile))
+  if (!map_cache(&tk, cache, cache->k, kDecTile) || !map_cache(&tv, cache, cache->v, kDecTile))
     return MG_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (layer->kind == MG_LOCAL)
@@ -431,6 +501,7 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   p.splits = w.splits;
   p.max_len = max_len;
   p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
+  p.map = cache_map(cache);
   cudaError_t e = launch_decode(p, tk, tv, s);
   if (e != cudaSuccess) return MG_ERR_CUDA;
   CombineParams c;
@@ -525,8 +596,7 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
     tkb = tka;
     tvb = tva;
   } else {
-    if (!map_rows(&tka, cache->k, cache->slots, outer, kTcKeys) ||
-        !map_rows(&tva, cache->v, cache->slots, outer, kTcVRows))
+    if (!map_cache(&tka, cache, cache->k, kTcKeys) || !map_cache(&tva, cache, cache->v, kTcVRows))
       return MG_ERR_CUDA;
     const uint64_t dims[4] = {static_cast<uint64_t>(kD), kHkv, static_cast<uint64_t>(n),
                               static_cast<uint64_t>(B)};
@@ -557,6 +627,7 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
   p.max_len = max_len;
   p.slots = cache->slots;
   p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
+  p.map = cache_map(cache);
   if (launch_attn_tc(p, tq, tka, tva, tkb, tvb, s) != cudaSuccess) return MG_ERR_CUDA;
   if (w.splits > 1) {
     CombineParams c;

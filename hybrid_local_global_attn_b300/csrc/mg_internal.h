@@ -66,6 +66,38 @@ struct RopeTurns {
 // Slot steps between the keys one thread of the local kernel rotates.
 constexpr int kRopeSteps[3] = {8, 64, 72};
 
+// Where a global layer keeps token position pos of (sequence b, KV head g).
+// Linear: row pos of [batch][2][slots][128] (outer index b * 2 + g); paged:
+// row pos % page_size of page table[b][pos / page_size] in the pool
+// [num_pages][2][page_size][128] (outer index page * 2 + g).  In both
+// cases the element offset of the row is (outer * rows + row) * 128, and a
+// 3D tensor map (128, rows, outer) reads it at (x, row, outer).
+struct CacheMap {
+  const int32_t *table;  // nullptr: linear
+  int32_t rows;          // slots (linear) or page_size (paged)
+  int32_t pages_per_seq, num_pages;
+};
+
+#ifdef __CUDACC__
+// (row, outer) of position pos; an out-of-range page entry flags
+// MG_DERR_PAGE (when err != nullptr) and becomes page 0.
+__device__ __forceinline__ void cache_coord(const CacheMap &m, int b, int g, int32_t pos,
+                                            int32_t *row, int32_t *outer, uint32_t *err) {
+  if (m.table == nullptr) {
+    *row = pos;
+    *outer = b * 2 + g;
+    return;
+  }
+  int32_t page = m.table[static_cast<size_t>(b) * m.pages_per_seq + pos / m.rows];
+  if (page < 0 || page >= m.num_pages) {
+    if (err != nullptr) atomicOr(err, MG_DERR_PAGE);
+    page = 0;
+  }
+  *row = pos % m.rows;
+  *outer = page * 2 + g;
+}
+#endif
+
 struct AppendParams {
   const __nv_bfloat16 *k_new, *v_new;  // [B][n][2][128]
   __nv_bfloat16 *k_cache, *v_cache;    // [B][2][slots][128]
@@ -76,6 +108,18 @@ struct AppendParams {
   int32_t *pos_next;
   uint32_t *err;
   int32_t batch, n, slots, kind;
+  CacheMap map;  // global layers: where each position's row lives
+};
+
+// A commit into up to MG_COMMIT_MAX_LAYERS caches in one launch; the block
+// rows of layer l start l * layer_stride elements after common.k_new/v_new.
+struct CommitLayersParams {
+  AppendParams common;  // positions, counts, rows of layer 0, batch, n, error word
+  __nv_bfloat16 *k_cache[MG_COMMIT_MAX_LAYERS], *v_cache[MG_COMMIT_MAX_LAYERS];
+  int32_t slots[MG_COMMIT_MAX_LAYERS], kind[MG_COMMIT_MAX_LAYERS];
+  CacheMap map[MG_COMMIT_MAX_LAYERS];
+  size_t layer_stride;
+  int32_t layers;
 };
 
 struct DecodeParams {  // global layers
@@ -91,6 +135,7 @@ struct DecodeParams {  // global layers
   uint32_t *err;
   int32_t batch, slots, splits, max_len;
   float scale_log2;        // softmax scale * log2(e)
+  CacheMap map;            // linear or paged rows of the cache
 };
 
 struct LocalParams {  // local layers, n <= kMaxLocalTokens query tokens
@@ -138,6 +183,10 @@ struct TcParams {
   uint32_t *err;
   int32_t batch, n, kind, window, staged, splits, qblocks, max_len, slots;
   float scale_log2;
+  // Global layers: rows of the cache.  A paged cache aligns the cache's key
+  // tiles to multiples of 256 (so a tile never straddles two pages) and
+  // masks the keys of the top tile at or past the block start.
+  CacheMap map;
 };
 
 // Launch with programmatic stream serialization, so the kernel may be
@@ -166,6 +215,7 @@ cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id);
 
 // Kernel launchers (defined next to each kernel).
 cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s);
+cudaError_t launch_kv_commit_layers(const CommitLayersParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                           cudaStream_t s);
 // single-token ring kernel (picks p.tpc itself) and the tcgen05 ring kernel

@@ -26,7 +26,7 @@ VERIFY_MAX = 16
 N_LAYERS = 52
 LOCAL, GLOBAL = 0, 1
 OP_DECODE, OP_VERIFY, OP_PREFILL = 0, 1, 2
-DERR_POSITION, DERR_TIMEOUT = 1, 2
+DERR_POSITION, DERR_TIMEOUT, DERR_COUNT, DERR_PAGE = 1, 2, 4, 8
 ROPE_THETA = 10000.0
 SCALE = 1.0 / math.sqrt(D)
 
@@ -38,7 +38,9 @@ class mg_layer(ctypes.Structure):
 
 class mg_cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
-                ("batch", ctypes.c_int32), ("slots", ctypes.c_int32)]
+                ("batch", ctypes.c_int32), ("slots", ctypes.c_int32),
+                ("page_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -47,6 +49,8 @@ _LP = ctypes.POINTER(mg_layer)
 _CP = ctypes.POINTER(mg_cache)
 lib.mg_cache_bytes.argtypes = [_i32, _i32, _i32]
 lib.mg_cache_bytes.restype = ctypes.c_size_t
+lib.mg_page_pool_bytes.argtypes = [_i32, _i32]
+lib.mg_page_pool_bytes.restype = ctypes.c_size_t
 lib.mg_workspace_bytes.argtypes = [_i32, _LP, _i32, _i32, _i32]
 lib.mg_workspace_bytes.restype = ctypes.c_size_t
 lib.mg_status_str.argtypes = [ctypes.c_int]
@@ -55,11 +59,12 @@ lib.mg_layer_kind.argtypes = [_i32]
 lib.mg_layer_kind.restype = ctypes.c_int
 lib.mg_kv_append.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P]
 lib.mg_kv_commit.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, _P]
+lib.mg_kv_commit_layers.argtypes = [_i32, _LP, _CP, _P, _i32, _P, _P, _P, _P, _P, _P]
 lib.mg_attn_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_append_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_verify.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_prefill.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
-for _f in (lib.mg_kv_append, lib.mg_kv_commit, lib.mg_attn_decode, lib.mg_append_decode, lib.mg_attn_verify,
+for _f in (lib.mg_kv_append, lib.mg_kv_commit, lib.mg_kv_commit_layers, lib.mg_attn_decode, lib.mg_append_decode, lib.mg_attn_verify,
            lib.mg_attn_prefill):
     _f.restype = ctypes.c_int
 
@@ -76,6 +81,10 @@ def mg_status_str(status: int) -> str:
 
 def mg_cache_bytes(kind: int, batch: int, capacity: int) -> int:
     return int(lib.mg_cache_bytes(kind, batch, capacity))
+
+
+def mg_page_pool_bytes(num_pages: int, page_size: int) -> int:
+    return int(lib.mg_page_pool_bytes(num_pages, page_size))
 
 
 def mg_layer_kind(l: int) -> int:
@@ -107,6 +116,38 @@ class KVCache:
 
     def nbytes(self) -> int:
         return self.k.numel() * 2 + self.v.numel() * 2
+
+
+class PagedKVCache:
+    """A global layer's paged cache: k and v pools bf16 [num_pages][2][page_size][128]
+    shared by the batch, and a page table int32 [batch][capacity // page_size]
+    (all on the GPU; the table is the caller's to fill, -1 = unassigned)."""
+
+    def __init__(self, batch: int, capacity: int, num_pages: int, page_size: int = 256,
+                 device="cuda"):
+        if capacity % page_size:
+            raise ValueError("capacity must be a multiple of page_size")
+        self.kind = GLOBAL
+        self.batch = batch
+        self.slots = int(capacity)
+        self.page_size = int(page_size)
+        self.num_pages = int(num_pages)
+        self.k = torch.zeros((num_pages, HKV, page_size, D), dtype=torch.bfloat16, device=device)
+        self.v = torch.zeros_like(self.k)
+        self.table = torch.full((batch, capacity // page_size), -1, dtype=torch.int32, device=device)
+        self.struct = mg_cache(self.k.data_ptr(), self.v.data_ptr(), batch, self.slots,
+                               self.table.data_ptr(), self.page_size, self.num_pages)
+
+    def nbytes(self) -> int:
+        return self.k.numel() * 2 + self.v.numel() * 2
+
+    def linear(self, b: int, upto: int):
+        """Sequence b's rows [0, upto) gathered through the table: (k, v) [2][upto][128]."""
+        ps = self.page_size
+        pages = self.table[b, :(upto + ps - 1) // ps].long()
+        k = self.k[pages].permute(1, 0, 2, 3).reshape(HKV, -1, D)[:, :upto]
+        v = self.v[pages].permute(1, 0, 2, 3).reshape(HKV, -1, D)[:, :upto]
+        return k, v
 
 
 def _ptr(t, dtype=None):
@@ -144,6 +185,20 @@ def mg_kv_commit(layer, cache: KVCache, pos0, count, k_new, v_new, err, pos_next
           int(k_new.shape[1]), _ptr(count, torch.int32), _ptr(k_new, torch.bfloat16),
           _ptr(v_new, torch.bfloat16), _ptr(pos_next, torch.int32), _ptr(err, torch.int32),
           _stream(stream))
+
+
+def mg_kv_commit_layers(layers, caches, pos0, count, k_new, v_new, err, pos_next=None,
+                        stream=None):
+    """mg_kv_commit into every cache of `caches` in one launch; k_new/v_new
+    are [n_layers][B][n][2][128]."""
+    L = len(layers)
+    if len(caches) != L or k_new.shape[0] != L or v_new.shape != k_new.shape:
+        raise ValueError("one layer, one cache and one block per layer")
+    lay_arr = (mg_layer * L)(*layers)
+    cache_arr = (mg_cache * L)(*[c.struct for c in caches])
+    _call(lib.mg_kv_commit_layers, L, lay_arr, cache_arr, _ptr(pos0, torch.int32), int(k_new.shape[2]),
+          _ptr(count, torch.int32), _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16),
+          _ptr(pos_next, torch.int32), _ptr(err, torch.int32), _stream(stream))
 
 
 def mg_attn_decode(layer, cache: KVCache, pos, max_len, q, o, ws, err, stream=None):

@@ -50,6 +50,7 @@ extern "C" {
 #define MG_D 128      /* head dim [P1 §01] */
 #define MG_WINDOW 2048 /* local window = ring slots [P1 §01] */
 #define MG_VERIFY_MAX 16 /* draft block [P1 §04; P4 "第三招"] */
+#define MG_COMMIT_MAX_LAYERS 64 /* layers one mg_kv_commit_layers call can take */
 
 typedef enum { MG_LOCAL = 0, MG_GLOBAL = 1 } mg_kind;
 
@@ -72,6 +73,7 @@ typedef enum {
 #define MG_DERR_POSITION 1u /* a device position was negative or beyond max_len / capacity */
 #define MG_DERR_TIMEOUT 2u  /* a pipeline wait ran out its time limit; the CTA gave up */
 #define MG_DERR_COUNT 4u    /* a commit count was outside [0, n]; that sequence was left as it was */
+#define MG_DERR_PAGE 8u     /* a page-table entry was outside [0, num_pages); page 0 was used */
 
 /* One attention layer.  kind = MG_LOCAL requires window == 2048 and a
  * positive rope_theta (10000 is the value used throughout; the pages do not
@@ -84,16 +86,33 @@ typedef struct {
   float scale;       /* softmax scale, > 0 */
 } mg_layer;
 
-/* One layer's KV cache.  k and v each hold bf16 [batch][2][slots][128]:
- * a local layer has slots == 2048 and keeps position pos in slot
- * pos % 2048, reusing the oldest entry [P2 "窄缓存为长上下文留出空间"];
- * a global layer keeps position pos in slot pos, so slots is its capacity.
- * K is stored verbatim (un-rotated). */
+/* One layer's KV cache.  K is stored verbatim (un-rotated).
+ *
+ * Linear (page_table == NULL): k and v each hold bf16 [batch][2][slots][128].
+ * A local layer has slots == 2048 and keeps position pos in slot pos % 2048,
+ * reusing the oldest entry [P2 "窄缓存为长上下文留出空间"]; a global layer
+ * keeps position pos in slot pos, so slots is its capacity.
+ *
+ * Paged (global layers only): k and v each hold a pool of num_pages pages,
+ * bf16 [num_pages][2][page_size][128], shared by all sequences of the batch.
+ * Sequence b keeps position pos in row pos % page_size of physical page
+ * page_table[b * (slots / page_size) + pos / page_size], so sequences of
+ * different lengths take only the pages they use (the pages weigh page size
+ * and fragmentation against usage [P2 "窄缓存为长上下文留出空间"]).  slots
+ * is the per-sequence capacity and a multiple of page_size; page_size is a
+ * multiple of 256; page_table is int32 [batch][slots / page_size] in device
+ * memory, owned and filled by the caller (entries of positions a call does
+ * not touch are never read).  A kernel that meets an entry outside
+ * [0, num_pages) flags MG_DERR_PAGE and uses page 0 instead (the result is
+ * then wrong, but no memory outside the pool is touched). */
 typedef struct {
   void *k;
   void *v;
   int32_t batch;
   int32_t slots;
+  const int32_t *page_table; /* NULL: linear layout */
+  int32_t page_size;         /* paged: tokens per page, a multiple of 256 */
+  int32_t num_pages;         /* paged: pages in each of the k and v pools */
 } mg_cache;
 
 /* Host-only.  Bytes of one layer's K+V cache: 2 (K,V) x batch x 2 heads x
@@ -101,6 +120,11 @@ typedef struct {
  * and capacity for MG_GLOBAL.  Per token per layer this is 1024 bytes
  * [P1 §01].  Returns 0 for a bad kind or a negative size. */
 size_t mg_cache_bytes(int32_t kind, int32_t batch, int32_t capacity);
+
+/* Host-only.  Bytes of one layer's paged K+V pools: 2 (K,V) x num_pages x
+ * 2 heads x page_size x 128 x 2 bytes.  Returns 0 for a negative size or a
+ * page_size that is not a positive multiple of 256. */
+size_t mg_page_pool_bytes(int32_t num_pages, int32_t page_size);
 
 /* Host-only.  Workspace bytes that mg_attn_decode (op MG_OP_DECODE, n = 1),
  * mg_attn_verify (MG_OP_VERIFY, n = draft tokens) or mg_attn_prefill
@@ -161,6 +185,24 @@ int mg_kv_commit(const mg_layer *layer, const mg_cache *cache,
                  const int32_t *d_pos0, int32_t n, const int32_t *d_count,
                  const void *k_new, const void *v_new, int32_t *d_pos_next,
                  uint32_t *d_err, void *stream);
+
+/*
+ * mg_kv_commit of one verified block into the caches of n_layers layers in a
+ * single launch (the block's K/V rows of every layer are kept until the
+ * caller knows how many tokens were accepted; one launch instead of one per
+ * layer).  The same result as calling mg_kv_commit(&layers[l], &caches[l],
+ * d_pos0, n, d_count, k_new + l * batch * n * 256, v_new + ..., d_pos_next,
+ * ...) for l = 0 .. n_layers - 1.
+ *   layers, caches : host arrays of n_layers entries (1 <= n_layers <=
+ *                    MG_COMMIT_MAX_LAYERS); every cache has the same batch
+ *   k_new, v_new   : bf16 [n_layers][batch][n][2][128] (device)
+ * Other arguments as in mg_kv_commit.
+ */
+int mg_kv_commit_layers(int32_t n_layers, const mg_layer *layers,
+                        const mg_cache *caches, const int32_t *d_pos0,
+                        int32_t n, const int32_t *d_count, const void *k_new,
+                        const void *v_new, int32_t *d_pos_next,
+                        uint32_t *d_err, void *stream);
 
 /*
  * Decode attention for one query token per sequence [P1 §04: decode is

@@ -121,6 +121,35 @@ def cache_commit(kind, k_cache, v_cache, pos0, count, k_block, v_block):
         cache_append(kind, k_cache, v_cache, pos0, k_block[:count], v_block[:count])
 
 
+def paged_append(k_pool, v_pool, table_row, page_size, pos0, k_new, v_new):
+    """Paged global cache ("Tomas Koutsky 解释了 Meta 如何在 24 GB 的容量内容纳
+    Muse Glimmer", "窄缓存为长上下文留出空间": page size and fragmentation set
+    the memory actually used).  Position p of the sequence is row p % page_size
+    of page table_row[p // page_size] of the pool ([num_pages][2][page_size][128]
+    uint16 bit patterns, in place)."""
+    kn = bits(k_new)
+    vn = bits(v_new)
+    for t in range(kn.shape[0]):
+        p = pos0 + t
+        page = int(table_row[p // page_size])
+        if not 0 <= page < k_pool.shape[0]:
+            raise ValueError(f"position {p}: page {page} outside the pool")
+        k_pool[page, :, p % page_size, :] = kn[t]
+        v_pool[page, :, p % page_size, :] = vn[t]
+
+
+def paged_history(k_pool, v_pool, table_row, page_size, upto):
+    """Rows 0 .. upto-1 of a sequence read back through its page table, as a
+    linear history ([upto][2][128] uint16, the layout attention() takes)."""
+    k = np.empty((upto, 2, D), np.uint16)
+    v = np.empty((upto, 2, D), np.uint16)
+    for p in range(upto):
+        page = int(table_row[p // page_size])
+        k[p] = k_pool[page, :, p % page_size, :]
+        v[p] = v_pool[page, :, p % page_size, :]
+    return k, v
+
+
 def decode_from_cache(lay, k_cache, v_cache, p, q):
     kc = bits(k_cache); vc = bits(v_cache); qq = bits(q)
     slots = kc.shape[1]

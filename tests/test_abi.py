@@ -116,6 +116,19 @@ def test_host_side_rejections_launch_nothing(mg):
     assert lib.mg_kv_commit(by(L), by(cache), fake, 4, other, ctypes.c_void_p(0x1008), fake,
                             None, fake, None) == 1
     assert lib.mg_kv_commit(by(L), by(cache), fake, 0, other, fake, fake, None, fake, None) == 0
+    # multi-layer commit: layer count in [1, 64], one batch for all caches
+    lays = (mg.mg_layer * 2)(L, G)
+    gcache = mg.mg_cache(0x10000, 0x20000, 1, 4096)
+    caches = (mg.mg_cache * 2)(cache, gcache)
+    for nl in (0, 65):
+        assert lib.mg_kv_commit_layers(nl, lays, caches, fake, 4, other, fake, fake, None, fake,
+                                       None) == 1
+    caches2 = (mg.mg_cache * 2)(cache, mg.mg_cache(0x10000, 0x20000, 2, 4096))
+    assert lib.mg_kv_commit_layers(2, lays, caches2, fake, 4, other, fake, fake, None, fake,
+                                   None) == 1
+    caches3 = (mg.mg_cache * 2)(gcache, gcache)  # local layer on a 4096-slot cache
+    assert lib.mg_kv_commit_layers(2, lays, caches3, fake, 4, other, fake, fake, None, fake,
+                                   None) == 2
     # local layer with a cache that is not a 2048-slot ring
     c2 = mg.mg_cache(0x10000, 0x20000, 1, 4096)
     assert lib.mg_kv_append(by(L), by(c2), fake, 1, fake, fake, fake, None) == 2

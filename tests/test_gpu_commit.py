@@ -169,3 +169,42 @@ def test_speculative_rounds_against_linear_history(mg, kind):
     for b, p in enumerate(p_host):
         ref = orc.attention(olay, k[b, :p + 1], v[b, :p + 1], [p], qd[b:b + 1])[0]
         compare(od[b], ref, f"kind {kind} decode after rounds b {b} p {p}")
+
+
+def test_commit_layers_equals_per_layer_commits(mg):
+    """One launch into four layers (local, local, local, global) gives the
+    caches the oracle expects for each layer, the same as four commits."""
+    kinds = [0, 0, 0, 1]
+    p0s, counts, n = [2041, 5000], [9, 3], 16
+    B, T = len(p0s), max(p0s) + n
+    ks, vs, blocks_k, blocks_v, caches = [], [], [], [], []
+    for l, kind in enumerate(kinds):
+        k, v = synth.history(B, T, 70 + l, l)
+        jk, jv = synth.history(B, n, 80 + l, l)
+        bk = torch.stack([torch.cat([k[b, p:p + c], jk[b, c:]])
+                          for b, (p, c) in enumerate(zip(p0s, counts))])
+        bv = torch.stack([torch.cat([v[b, p:p + c], jv[b, c:]])
+                          for b, (p, c) in enumerate(zip(p0s, counts))])
+        ks.append(k)
+        vs.append(v)
+        blocks_k.append(bk)
+        blocks_v.append(bv)
+        caches.append(gpu_cache(mg, kind, B, 2048 if kind == 0 else T, k, v, p0s))
+    err = mg.error_word()
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    mg.mg_kv_commit_layers([mg.make_layer(kd) for kd in kinds], caches,
+                           torch.tensor(p0s, dtype=torch.int32, device="cuda"),
+                           torch.tensor(counts, dtype=torch.int32, device="cuda"),
+                           torch.stack(blocks_k).cuda().contiguous(),
+                           torch.stack(blocks_v).cuda().contiguous(), err, pos_next=nxt)
+    torch.cuda.synchronize()
+    check_err(err)
+    assert nxt.tolist() == [p + c for p, c in zip(p0s, counts)]
+    for l, kind in enumerate(kinds):
+        slots = 2048 if kind == 0 else T
+        for b in range(B):
+            kc, vc = oracle_cache(kind, slots, ks[l][b], vs[l][b], p0s[b])
+            orc.cache_commit(oracle_kind(kind), kc, vc, p0s[b], counts[b], blocks_k[l][b],
+                             blocks_v[l][b])
+            assert np.array_equal(bits_of(caches[l].k[b]), kc), f"layer {l} K of sequence {b}"
+            assert np.array_equal(bits_of(caches[l].v[b]), vc), f"layer {l} V of sequence {b}"

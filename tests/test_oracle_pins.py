@@ -186,6 +186,43 @@ def test_commit_rolls_back_rejected_drafts(kind):
         orc.cache_commit(kind, kc, vc, T, n + 1, blk_k, blk_v)
 
 
+def test_paged_storage_map_worked_example_and_round_trip():
+    # Page size 256, sequence 0 owns pages [5, 2, 7] and sequence 1 pages
+    # [0, 3]: position 300 of sequence 0 is row 44 of page 2, position 700
+    # row 188 of page 7; position 10 of sequence 1 row 10 of page 0.
+    ps, pool = 256, 8
+    kp = np.zeros((pool, 2, ps, 128), np.uint16)
+    vp = np.zeros_like(kp)
+    k0, v0 = rand_hist(701, 31)
+    k1, v1 = rand_hist(300, 32)
+    t0, t1 = [5, 2, 7], [0, 3]
+    orc.paged_append(kp, vp, t0, ps, 0, k0[:301], v0[:301])  # two calls, the second
+    orc.paged_append(kp, vp, t0, ps, 301, k0[301:], v0[301:])  # crossing a page
+    orc.paged_append(kp, vp, t1, ps, 0, k1, v1)
+    b0, b1 = orc.bits(k0), orc.bits(k1)
+    assert np.array_equal(kp[2, :, 44], b0[300])
+    assert np.array_equal(kp[7, :, 188], b0[700])
+    assert np.array_equal(kp[0, :, 10], b1[10])
+    assert np.array_equal(vp[3, :, 299 - 256], orc.bits(v1)[299])
+    # pages nobody owns stay untouched
+    for page in (1, 4, 6):
+        assert not kp[page].any() and not vp[page].any()
+    # reading back through the tables gives each linear history
+    hk, hv = orc.paged_history(kp, vp, t0, ps, 701)
+    assert np.array_equal(hk, b0) and np.array_equal(hv, orc.bits(v0))
+    hk, hv = orc.paged_history(kp, vp, t1, ps, 300)
+    assert np.array_equal(hk, b1)
+    # attention over the paged history is attention over the linear one
+    q = synth.randn_bf16((32, 128), 33)
+    lay = orc.layer(orc.GLOBAL)
+    hk, hv = orc.paged_history(kp, vp, t0, ps, 701)
+    a = orc.attention(lay, hk, hv, [700], q.unsqueeze(0))
+    b = orc.attention(lay, k0, v0, [700], q.unsqueeze(0))
+    assert np.array_equal(a, b)
+    with pytest.raises(ValueError):
+        orc.paged_append(kp, vp, [9], ps, 0, k1[:1], v1[:1])  # page outside the pool
+
+
 @pytest.mark.parametrize("kind,p", [(orc.LOCAL, 0), (orc.LOCAL, 100), (orc.LOCAL, 2046),
                                     (orc.LOCAL, 2047), (orc.LOCAL, 3000), (orc.GLOBAL, 3000)])
 def test_zero_keys_give_window_mean(kind, p):
