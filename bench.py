@@ -392,6 +392,103 @@ def leg_verify(wl):
             "commit_us_52_layers": c1_ms * 1e3, "commit_us_52_layers_per_layer_calls": c_ms * 1e3}
 
 
+def _graph_us(fn, reps=8, calls=1):
+    """Mean device time (us) of one of `calls` calls captured by fn into a graph."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+
+
+def leg_paged(wl, page_size=256):
+    """Global layers through a paged cache.  (a, b) The full-context cache of
+    one global layer copied into a pool of page_size-token pages in shuffled
+    order; 13 decode and 13 verify calls from one graph, beside the same calls
+    on that layer's linear cache.  (c) Four sequences of different lengths in
+    one pool (pages handed out in shuffled order), decoded together, beside
+    the same batch in a linear cache sized for the longest."""
+    import torch
+    mg, dev, err = wl.mg, wl.dev, wl.err
+    ps = page_size
+    rng = torch.Generator().manual_seed(5)
+    l0 = next(l for l in range(N_LAYERS) if wl.kinds[l] == mg.GLOBAL)
+    lin, lay = wl.caches[l0], wl.layers[l0]
+    slots = (wl.cap + ps - 1) // ps * ps
+    npg = slots // ps
+    paged = mg.PagedKVCache(1, slots, npg, ps, device=dev)
+    perm = torch.randperm(npg, generator=rng)
+    paged.table[0] = perm.to(device=dev, dtype=torch.int32)
+    for src, dst in ((lin.k, paged.k), (lin.v, paged.v)):
+        full = torch.zeros((2, slots, 128), dtype=torch.bfloat16, device=dev)
+        full[:, :wl.cap] = src[0]
+        dst[perm.to(dev)] = full.view(2, npg, ps, 128).permute(1, 0, 2, 3)
+        del full
+    n_glob = sum(1 for k in wl.kinds if k == mg.GLOBAL)
+    p = PROMPT - 1
+    pos = torch.tensor([p], dtype=torch.int32, device=dev)
+    q = wl.ver_q[l0][:, 0].contiguous()
+    o = torch.empty((1, 32, 128), dtype=torch.bfloat16, device=dev)
+    ws = mg.workspace(mg.OP_DECODE, lay, 1, 1, PROMPT, device=dev)
+    res = {"page_size": ps}
+    for name, cache in (("linear", lin), ("paged", paged)):
+        us = _graph_us(lambda: [mg.mg_attn_decode(lay, cache, pos, PROMPT, q, o, ws, err)
+                                for _ in range(n_glob)], calls=n_glob)
+        res[f"decode_us_{name}"] = us
+        res[f"decode_gbs_{name}"] = decode_layer_bytes(1, p) / us / 1e3
+    p0 = torch.tensor([PROMPT], dtype=torch.int32, device=dev)
+    wsv = mg.workspace(mg.OP_VERIFY, lay, 1, 16, PROMPT + 16, device=dev)
+    ov = torch.empty((1, 16, 32, 128), dtype=torch.bfloat16, device=dev)
+    for name, cache in (("linear", lin), ("paged", paged)):
+        us = _graph_us(lambda: [mg.mg_attn_verify(lay, cache, p0, PROMPT + 16, wl.ver_q[l0],
+                                                  wl.ver_k[l0], wl.ver_v[l0], ov, wsv, err)
+                                for _ in range(n_glob)], calls=n_glob)
+        res[f"verify_us_{name}"] = us
+        res[f"verify_gbs_{name}"] = verify_layer_bytes(1, PROMPT, 16) / us / 1e3
+    del paged
+    # (c) a batch of different lengths sharing one pool
+    lens = [PROMPT, PROMPT // 2, PROMPT // 4, PROMPT // 16]
+    B = len(lens)
+    need = [(n + ps - 1) // ps for n in lens]
+    pool = mg.PagedKVCache(B, slots, sum(need), ps, device=dev)
+    order = torch.randperm(sum(need), generator=rng).tolist()
+    for b, m in enumerate(need):
+        pool.table[b, :m] = torch.tensor(order[:m], dtype=torch.int32)
+        del order[:m]
+    pool.k.normal_()
+    pool.v.normal_()
+    linb = mg.KVCache(mg.GLOBAL, B, slots, device=dev)
+    for b, n in enumerate(lens):
+        kb, vb = pool.linear(b, n)
+        linb.k[b, :, :n] = kb
+        linb.v[b, :, :n] = vb
+    posb = torch.tensor([n - 1 for n in lens], dtype=torch.int32, device=dev)
+    qb = torch.randn((B, 32, 128), device=dev).to(torch.bfloat16)
+    ob = torch.empty_like(qb)
+    wsb = mg.workspace(mg.OP_DECODE, lay, B, 1, PROMPT, device=dev)
+    nbytes = sum(decode_layer_bytes(1, n - 1) for n in lens)
+    batch = {"lengths": lens, "pool_mib": pool.nbytes() / 2 ** 20,
+             "linear_mib": linb.nbytes() / 2 ** 20}
+    for name, cache in (("linear", linb), ("paged", pool)):
+        us = _graph_us(lambda: [mg.mg_attn_decode(lay, cache, posb, PROMPT, qb, ob, wsb, err)
+                                for _ in range(n_glob)], calls=n_glob)
+        batch[f"decode_us_{name}"] = us
+        batch[f"decode_gbs_{name}"] = nbytes / us / 1e3
+    res["batch4_variable_length"] = batch
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after the paged leg"
+    return res
+
+
 def run_gpu(args, rank, world):
     import torch
     from hybrid_local_global_attn_b300 import mg
@@ -418,6 +515,9 @@ def run_gpu(args, rank, world):
     if "verify" in legs:
         line_extra["verify"] = leg_verify(wl)
         log("verify: " + json.dumps(line_extra["verify"]))
+    if "paged" in legs:
+        line_extra["paged"] = leg_paged(wl)
+        log("paged: " + json.dumps(line_extra["paged"]))
 
     # ------------------------------------------------------------- decode ----
     ws_dec = [mg.workspace(mg.OP_DECODE, layers[l], 1, 1, cap, device=dev) for l in range(N_LAYERS)]
@@ -444,7 +544,10 @@ def run_gpu(args, rank, world):
     g_dec = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_dec):
         decode_step()
-    launches_per_step = 2 * N_LAYERS  # fused append+decode, then combine, per layer
+    # local layer: one ring kernel (append fused, splits merged in the
+    # cluster); global layer: the split pass with the fused append, then the
+    # combine kernel
+    launches_per_step = sum(mg.mg_decode_kernel_count(layers[l], 1, cap) for l in range(N_LAYERS))
     for i in range(W):
         stage(i)
         g_dec.replay()
@@ -715,7 +818,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="mg", choices=["mg", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--legs", default="prefill,verify,decode",
+    ap.add_argument("--legs", default="prefill,verify,paged,decode",
                     help="comma list of legs to run besides decode")
     ap.add_argument("--fill", default="prefill", choices=["prefill", "random"],
                     help="random: fill caches without attention (profiling runs only)")

@@ -21,6 +21,8 @@
 //    base 2 with quad shuffles; row sums stay per thread until the end.
 //  * The four warps merge in shared memory into the CTA's partial (o / l,
 //    lse), written to the workspace; a combine kernel merges the splits.
+//    With a single split per (sequence, KV head) -- large batches -- the
+//    CTA writes the output itself and no combine runs.
 //  * Optionally the token's own K/V is appended by the CTA whose split holds
 //    its slot, before that tile is loaded (mg_append_decode).
 //  * The cache is linear or paged (a page table maps each 256-multiple run
@@ -342,16 +344,24 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       float acc = 0.f;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) acc += mo[(w * kGroup + r) * kRowPad + d];
-      part_o(r, d) = acc;
+      if (p.splits == 1)
+        p.o[(row0 + r) * kD + d] = __float2bfloat16_rn(acc);  // the only split: final
+      else
+        part_o(r, d) = acc;
     }
-    if (warp == 0 && tq == 0) {
+    if (warp == 0 && tq == 0 && p.splits > 1) {
       part_lse(gr) = Lr[0] > 0.f ? Mr[0] + __log2f(Lr[0]) : -INFINITY;
       part_lse(gr + 8) = Lr[1] > 0.f ? Mr[1] + __log2f(Lr[1]) : -INFINITY;
     }
   } else {
     // no keys for this split: lse = -inf, o = 0
-    for (int i = threadIdx.x; i < kGroup * kD; i += kDecWarps * 32) part_o(i / kD, i % kD) = 0.f;
-    if (threadIdx.x < kGroup) part_lse(threadIdx.x) = -INFINITY;
+    for (int i = threadIdx.x; i < kGroup * kD; i += kDecWarps * 32) {
+      if (p.splits == 1)
+        p.o[(row0 + i / kD) * kD + i % kD] = __float2bfloat16_rn(0.f);
+      else
+        part_o(i / kD, i % kD) = 0.f;
+    }
+    if (threadIdx.x < kGroup && p.splits > 1) part_lse(threadIdx.x) = -INFINITY;
   }
 }
 

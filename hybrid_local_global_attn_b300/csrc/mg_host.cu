@@ -250,12 +250,15 @@ bool ws_layout(int32_t op, const mg_layer *L, int32_t batch, int32_t n, int32_t 
       // one cluster per (sequence, KV head) merges in shared memory: no workspace
       w->splits = kLocCluster;
     } else {
+      // one split: the kernel writes o directly and needs no workspace
       w->splits = splits_decode(L->kind, batch, max_len);
-      const size_t rows = static_cast<size_t>(batch) * kHq;
-      w->part_o = off;
-      off = align256(off + rows * w->splits * kD * sizeof(float));
-      w->part_lse = off;
-      off = align256(off + rows * w->splits * sizeof(float));
+      if (w->splits > 1) {
+        const size_t rows = static_cast<size_t>(batch) * kHq;
+        w->part_o = off;
+        off = align256(off + rows * w->splits * kD * sizeof(float));
+        w->part_lse = off;
+        off = align256(off + rows * w->splits * sizeof(float));
+      }
     }
   } else if (op == MG_OP_VERIFY && local) {
     // the ring kernel: one cluster per (sequence, KV head, token), no workspace
@@ -288,6 +291,7 @@ bool ws_layout(int32_t op, const mg_layer *L, int32_t batch, int32_t n, int32_t 
 }
 
 int launch_status(cudaError_t e) { return e == cudaSuccess ? MG_OK : MG_ERR_CUDA; }
+
 
 template <typename T>
 T *at(void *base, size_t off) {
@@ -349,6 +353,13 @@ size_t mg_workspace_bytes(int32_t op, const mg_layer *layer, int32_t batch, int3
   WsLayout w;
   if (!ws_layout(op, layer, batch, n, max_len, &w)) return static_cast<size_t>(-1);
   return w.total;
+}
+
+int mg_decode_kernel_count(const mg_layer *layer, int32_t batch, int32_t max_len) {
+  if (check_layer(layer) != MG_OK) return -1;
+  WsLayout w;
+  if (!ws_layout(MG_OP_DECODE, layer, batch, 1, max_len, &w)) return -1;
+  return (layer->kind == MG_LOCAL || w.splits == 1) ? 1 : 2;
 }
 
 const char *mg_status_str(int status) {
@@ -493,8 +504,10 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
   p.k_cache = static_cast<__nv_bfloat16 *>(cache->k);
   p.v_cache = static_cast<__nv_bfloat16 *>(cache->v);
-  p.part_o = at<float>(ws, w.part_o);
-  p.part_lse = at<float>(ws, w.part_lse);
+  const bool split = w.splits > 1;
+  p.part_o = split ? at<float>(ws, w.part_o) : nullptr;
+  p.part_lse = split ? at<float>(ws, w.part_lse) : nullptr;
+  p.o = static_cast<__nv_bfloat16 *>(o);
   p.err = d_err;
   p.batch = cache->batch;
   p.slots = cache->slots;
@@ -504,6 +517,7 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   p.map = cache_map(cache);
   cudaError_t e = launch_decode(p, tk, tv, s);
   if (e != cudaSuccess) return MG_ERR_CUDA;
+  if (!split) return MG_OK;
   CombineParams c;
   c.part_o = p.part_o;
   c.part_lse = p.part_lse;

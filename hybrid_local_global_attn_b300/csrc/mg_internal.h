@@ -132,11 +132,15 @@ struct DecodeParams {  // global layers
   __nv_bfloat16 *k_cache, *v_cache;
   float *part_o;           // [B][32][splits][128]
   float *part_lse;         // [B][32][splits]   (log2 domain)
+  // splits == 1: each CTA writes its rows of o directly (no partials, no
+  // combine kernel)
+  __nv_bfloat16 *o;        // [B][32][128]
   uint32_t *err;
   int32_t batch, slots, splits, max_len;
   float scale_log2;        // softmax scale * log2(e)
   CacheMap map;            // linear or paged rows of the cache
 };
+
 
 struct LocalParams {  // local layers, n <= kMaxLocalTokens query tokens
   const int32_t *pos;  // [B]: position of query token 0

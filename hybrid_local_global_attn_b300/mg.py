@@ -56,6 +56,8 @@ lib.mg_workspace_bytes.restype = ctypes.c_size_t
 lib.mg_status_str.argtypes = [ctypes.c_int]
 lib.mg_status_str.restype = ctypes.c_char_p
 lib.mg_layer_kind.argtypes = [_i32]
+lib.mg_decode_kernel_count.argtypes = [_LP, _i32, _i32]
+lib.mg_decode_kernel_count.restype = ctypes.c_int
 lib.mg_layer_kind.restype = ctypes.c_int
 lib.mg_kv_append.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P]
 lib.mg_kv_commit.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, _P]
@@ -85,6 +87,10 @@ def mg_cache_bytes(kind: int, batch: int, capacity: int) -> int:
 
 def mg_page_pool_bytes(num_pages: int, page_size: int) -> int:
     return int(lib.mg_page_pool_bytes(num_pages, page_size))
+
+
+def mg_decode_kernel_count(layer, batch: int, max_len: int) -> int:
+    return int(lib.mg_decode_kernel_count(ctypes.byref(layer), batch, max_len))
 
 
 def mg_layer_kind(l: int) -> int:
@@ -233,7 +239,8 @@ def mg_attn_prefill(layer, cache: KVCache, pos0, max_len, q, k_new, v_new, o, ws
 
 
 def workspace(op, layer, batch, n, max_len, device="cuda"):
-    """Caller-side workspace allocation (torch) of the size libmg asks for."""
+    """Caller-side workspace allocation (torch) of the size libmg asks for
+    (left uninitialised: nothing in it needs to start at any value)."""
     nbytes = mg_workspace_bytes(op, layer, batch, n, max_len)
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 

@@ -132,10 +132,18 @@ size_t mg_page_pool_bytes(int32_t num_pages, int32_t page_size);
  * max_len.  The workspace holds split-KV partials (global decode, global
  * verify) and, for local prefill, RoPE-rotated copies of the queries and
  * of the keys in the window; local decode and local verify merge inside a
- * thread-block cluster and need none.
+ * thread-block cluster and need none.  Nothing in a workspace needs
+ * initialising.  A global-layer decode with one split per (sequence, KV
+ * head) -- large batches -- writes its output directly and needs none.
  * Returns 0 if no workspace is needed, (size_t)-1 for bad arguments. */
 size_t mg_workspace_bytes(int32_t op, const mg_layer *layer, int32_t batch,
                           int32_t n, int32_t max_len);
+
+/* Host-only.  Number of kernels one mg_attn_decode / mg_append_decode call
+ * launches for this layer, batch and max_len: 1 (a local layer, or a global
+ * layer with a single split) or 2 (a global layer: the split pass, then the
+ * combine kernel).  Returns -1 for bad arguments. */
+int mg_decode_kernel_count(const mg_layer *layer, int32_t batch, int32_t max_len);
 
 /* Static description of a status code. */
 const char *mg_status_str(int status);
@@ -211,7 +219,8 @@ int mg_kv_commit_layers(int32_t n_layers, const mg_layer *layers,
  * (mg_kv_append first).  Key set: [max(0, p-2047), p] for a local layer,
  * with RoPE applied to q at p and to each key at its own position;
  * [0, p] for a global layer, no RoPE.  Split-KV: the key set is cut into
- * splits handled by separate CTAs, merged by a log-sum-exp combine.
+ * splits handled by separate CTAs, merged by a log-sum-exp combine kernel
+ * (a single split writes the output directly).
  *   q, o     : bf16 [batch][32][128] (device)
  *   max_len  : 1 + the largest pos[b] the caller may pass (sizes the grid
  *              and the workspace); pos[b] >= max_len is skipped + flagged
@@ -250,12 +259,13 @@ int mg_append_decode(const mg_layer *layer, const mg_cache *cache,
  * inside libmg.so (held by every GPU that loads the library until the process
  * exits).  A call whose mg_workspace_bytes(MG_OP_DECODE, layer, batch, 1,
  * max_len) exceeds it returns MG_ERR_WORKSPACE and launches nothing (at the
- * default split counts this is batch above ~250).  The array is shared by
- * all calls on a device and keeps the last call's contents; nothing in it
- * has to start at zero.  Calls that overlap on the GPU (e.g. on two streams)
- * race on it.  The first call on each device looks up the array's device
- * address (cudaGetSymbolAddress, that device current); make that first call
- * before any stream capture.
+ * default split counts no batch needs more than about 2.5 MB: a batch large
+ * enough for one split per KV head needs none).  The array is shared by all
+ * calls on a device and keeps the last call's contents; nothing in it has to
+ * start at zero.  Calls that overlap on the GPU (e.g. on two streams) race on
+ * it.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, that device current); make that first call before
+ * any stream capture.
  */
 #define MG_NOALLOC_SCRATCH_BYTES (4u << 20)
 int mg_attn_decode_noalloc(const mg_layer *layer, const mg_cache *cache,

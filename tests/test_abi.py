@@ -155,3 +155,14 @@ def test_host_side_rejections_launch_nothing(mg):
                                fake, None) == 3
     assert lib.mg_attn_prefill(by(G), by(gc), fake, 0, 10, fake, fake, fake, fake, fake, 1 << 30,
                                fake, None) == 1
+
+
+def test_noalloc_scratch_covers_every_decode_batch(mg):
+    """The fixed array behind mg_attn_decode_noalloc (4 MiB) holds the decode
+    workspace of any batch at the longest context: one split per KV head
+    needs none, and the split count keeps splits x batch near 148."""
+    lay = mg.make_layer(mg.GLOBAL)
+    for B in list(range(1, 160)) + [256, 512, 4096]:
+        for max_len in (1, 4096, 131072, 1 << 20):
+            need = mg.mg_workspace_bytes(mg.OP_DECODE, lay, B, 1, max_len)
+            assert need <= 4 << 20, (B, max_len, need)

@@ -169,3 +169,41 @@ def test_append_decode_mixed_batch(mg, kind):
         # slots never written stay zero on both sides
         assert np.array_equal(bits_of(cache.k[b]), kc), f"K cache b {b}"
         assert np.array_equal(bits_of(cache.v[b]), vc), f"V cache b {b}"
+
+
+@pytest.mark.parametrize("B,T", [(1, 131072 + 64), (3, 5000), (40, 700), (160, 900)])
+def test_global_decode_repeats_exactly(mg, B, T):
+    """Global decode at batch 1, 3, 40 and 160 (148, 49, 3 and 1 splits per
+    KV head; a single split writes the output without partials or combine):
+    eager calls and graph replays give the same bits, sampled rows match the
+    oracle, and the kernel count the library reports fits the split count."""
+    lay = mg.make_layer(1)
+    positions = [T - 1 - (37 * b) % (T // 2) for b in range(B)]
+    k, v = synth.history(B, T, 9, 3)
+    q = synth.queries(B, 1, 9, 3)[:, 0]
+    cache = fill_for_decode(mg, 1, k, v, positions, capacity=T)
+    ws = mg.workspace(mg.OP_DECODE, lay, B, 1, T)
+    o = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    err = mg.error_word()
+    pos = torch.tensor(positions, dtype=torch.int32, device="cuda")
+    qd = q.cuda().contiguous()
+    outs = []
+    for _ in range(2):
+        mg.mg_attn_decode(lay, cache, pos, T, qd, o, ws, err)
+        torch.cuda.synchronize()
+        outs.append(o.clone())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mg.mg_attn_decode(lay, cache, pos, T, qd, o, ws, err)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    check_err(err)
+    outs.append(o.clone())
+    assert all(torch.equal(outs[0], x) for x in outs[1:])
+    assert mg.mg_decode_kernel_count(lay, B, T) == (1 if B == 160 else 2)
+    olay = orc.layer(orc.GLOBAL)
+    for b in sorted({0, B // 2, B - 1}):
+        p = positions[b]
+        ref = orc.attention(olay, k[b, :p + 1], v[b, :p + 1], [p], q[b:b + 1])[0]
+        compare(o[b], ref, f"B {B} b {b} p {p}")
