@@ -150,6 +150,101 @@ def paged_history(k_pool, v_pool, table_row, page_size, upto):
     return k, v
 
 
+# ----------------------------------------------------------- FP8 cache ----
+# An FP8 KV cache for global layers: e4m3 codes with one power-of-two scale
+# per KV head for K and one for V (the pages list cache quantisation as a way
+# to shrink the cache, "Tomas Koutsky 解释了 Meta 如何在 24 GB 的容量内容纳
+# Muse Glimmer", "窄缓存为长上下文留出空间").  e4m3 here is the OCP FP8 E4M3
+# format: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0
+# holds the subnormals m * 2^-9; no infinities; S.1111.111 is NaN, so the
+# largest finite magnitude is 1.75 * 2^8 = 448.
+
+E4M3_MAX = 448.0
+
+# Column of a position inside its 16-position group of a transposed V tile:
+# positions 2t, 2t+1 go to columns 4t, 4t+1 and positions 8+2t, 9+2t to
+# columns 4t+2, 4t+3 (t = 0..3).
+E4M3_V_COLUMN = [4 * ((j % 8) // 2) + 2 * (j // 8) + (j % 2) for j in range(16)]
+
+
+def e4m3_encode(x):
+    """float64 array -> uint8 e4m3 codes: round to nearest, ties to even,
+    magnitudes above 448 saturate to 448, the sign of zero is kept."""
+    x = np.asarray(x, dtype=np.float64)
+    neg = np.signbit(x)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    _, ex = np.frexp(a)                           # a = f * 2^ex, f in [0.5, 1)
+    binade = np.maximum(ex - 1, -6)               # below 2^-6 the spacing stays 2^-9
+    quantum = np.ldexp(1.0, binade - 3)           # 3 mantissa bits
+    r = a / quantum                               # exact: power-of-two divisor
+    n = np.floor(r)
+    frac = r - n
+    up = (frac > 0.5) | ((frac == 0.5) & (np.mod(n, 2.0) == 1.0))
+    v = np.minimum((n + up) * quantum, E4M3_MAX)  # a carry may move up one binade
+    _, ev = np.frexp(v)
+    e_field = np.where(v >= 2.0 ** -6, ev - 1 + 7, 0)
+    mant = np.where(e_field == 0, v / 2.0 ** -9, (np.ldexp(v, -(e_field - 7)) - 1.0) * 8.0)
+    code = (e_field * 8 + mant).astype(np.int64) | (neg.astype(np.int64) << 7)
+    return code.astype(np.uint8)
+
+
+def e4m3_decode(code):
+    """uint8 e4m3 codes -> float64 values (NaN for the NaN codes)."""
+    c = np.asarray(code).astype(np.int64)
+    e = (c >> 3) & 15
+    m = c & 7
+    v = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return np.where((c >> 7) & 1 == 1, -v, v)
+
+
+def _check_pow2(scales):
+    for s in scales:
+        m, _ = np.frexp(float(s))
+        if not (s > 0 and m == 0.5):
+            raise ValueError(f"scale {s} is not a positive power of two")
+
+
+def e4m3_cache_append(k_codes, vt_codes, k_scale, v_scale, pos0, k_new, v_new):
+    """Store positions pos0 .. pos0+n-1 of one sequence in an FP8 cache (in
+    place).  K: k_codes[g][p][d] = e4m3(k / k_scale[g]).  V, transposed per
+    64-position tile: vt_codes[g][p // 64][d][16 * ((p % 64) // 16) +
+    E4M3_V_COLUMN[p % 16]] = e4m3(v / v_scale[g]).  Scales are powers of two,
+    so the division is exact and the code is the value's correct rounding."""
+    _check_pow2(list(k_scale) + list(v_scale))
+    kn = bits(k_new).astype(np.uint32) << 16
+    vn = bits(v_new).astype(np.uint32) << 16
+    kf = kn.view(np.float32).astype(np.float64)
+    vf = vn.view(np.float32).astype(np.float64)
+    for t in range(kf.shape[0]):
+        p = pos0 + t
+        col = 16 * ((p % 64) // 16) + E4M3_V_COLUMN[p % 16]
+        for g in range(HKV):
+            k_codes[g, p, :] = e4m3_encode(kf[t, g] / k_scale[g])
+            vt_codes[g, p // 64, :, col] = e4m3_encode(vf[t, g] / v_scale[g])
+
+
+def e4m3_history(k_codes, vt_codes, k_scale, v_scale, upto):
+    """Positions 0 .. upto-1 of an FP8 cache dequantised (code value x scale,
+    exactly representable in bf16), as bf16 bit patterns [upto][2][128] for
+    attention()."""
+    k = np.empty((upto, HKV, D), np.float64)
+    v = np.empty((upto, HKV, D), np.float64)
+    for p in range(upto):
+        col = 16 * ((p % 64) // 16) + E4M3_V_COLUMN[p % 16]
+        for g in range(HKV):
+            k[p, g] = e4m3_decode(k_codes[g, p, :]) * k_scale[g]
+            v[p, g] = e4m3_decode(vt_codes[g, p // 64, :, col]) * v_scale[g]
+
+    def to_bf16_bits(a):
+        f = a.astype(np.float32)
+        assert np.array_equal(f.astype(np.float64), a), "value not exact in fp32"
+        b = f.view(np.uint32)
+        assert not np.any(b & 0xFFFF), "value not exact in bf16"
+        return (b >> 16).astype(np.uint16)
+    return to_bf16_bits(k), to_bf16_bits(v)
+
+
 def decode_from_cache(lay, k_cache, v_cache, p, q):
     kc = bits(k_cache); vc = bits(v_cache); qq = bits(q)
     slots = kc.shape[1]

@@ -223,6 +223,73 @@ def test_paged_storage_map_worked_example_and_round_trip():
         orc.paged_append(kp, vp, [9], ps, 0, k1[:1], v1[:1])  # page outside the pool
 
 
+def test_e4m3_codec_against_library_cast():
+    # Every finite bf16 value, scaled by powers of two into and past the
+    # e4m3 range: the oracle's round-to-nearest-even code equals torch's
+    # float8_e4m3fn cast of the value clamped to +-448 (the saturation the
+    # cache uses); decoding all 256 codes equals torch's widening.
+    allbits = np.arange(65536, dtype=np.uint32)
+    f32 = (allbits << 16).view(np.float32)
+    f = f32[np.isfinite(f32)].astype(np.float64)
+    for sc in (2.0 ** -8, 1.0, 2.0 ** 5):
+        x = f * sc
+        got = orc.e4m3_encode(x)
+        want = torch.tensor(np.clip(x, -448.0, 448.0)).to(torch.float8_e4m3fn).view(torch.uint8)
+        assert np.array_equal(got, want.numpy()), sc
+    codes = np.arange(256, dtype=np.uint8)
+    lib = torch.tensor(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(orc.e4m3_decode(codes), lib)
+
+
+def test_e4m3_hand_values():
+    # ties go to the even code, magnitudes past 448 saturate, the sign of
+    # zero stays, subnormals step by 2^-9
+    cases = {1.0: 0x38, 1.0625: 0x38, 1.1875: 0x3A, 1.9375: 0x40, 448.0: 0x7E, 500.0: 0x7E,
+             -500.0: 0xFE, 2.0 ** -9: 0x01, 2.0 ** -10: 0x00, 3 * 2.0 ** -10: 0x02,
+             2.0 ** -6: 0x08, -1e-10: 0x80, 0.0: 0x00, -2.5: 0xC2}
+    got = orc.e4m3_encode(np.array(list(cases)))
+    assert got.tolist() == list(cases.values())
+    assert orc.e4m3_decode(np.array([0x7F, 0xFF])).tolist().count(0) == 0  # NaN codes
+    assert np.isnan(orc.e4m3_decode(np.array([0x7F]))[0])
+
+
+def test_e4m3_cache_layout_and_round_trip():
+    # V column order inside a 16-position group is a permutation; position 70
+    # of head 1 sits in tile 1, column sigma(6) = 12; position 93 in column
+    # 16 + sigma(13) = 27.  Values that are exact e4m3 multiples of the scale
+    # come back bit for bit; others come back as the correctly rounded code.
+    assert sorted(orc.E4M3_V_COLUMN) == list(range(16))
+    assert orc.E4M3_V_COLUMN[6] == 12 and orc.E4M3_V_COLUMN[13] == 11
+    T = 128
+    kc = np.zeros((2, T, 128), np.uint8)
+    vt = np.zeros((2, T // 64, 128, 64), np.uint8)
+    ks, vs = [2.0 ** -2, 2.0], [1.0, 2.0 ** -3]
+    vals = orc.e4m3_decode(np.arange(0, 0x7E, dtype=np.uint8))  # finite, non-negative
+    rng = np.random.default_rng(3)
+    k = rng.choice(vals, size=(T, 2, 128)) * np.array(ks)[None, :, None]
+    v = rng.choice(vals, size=(T, 2, 128)) * np.array(vs)[None, :, None]
+    kb = torch.tensor(k, dtype=torch.float32).to(torch.bfloat16)
+    vb = torch.tensor(v, dtype=torch.float32).to(torch.bfloat16)
+    orc.e4m3_cache_append(kc, vt, ks, vs, 0, kb[:70], vb[:70])
+    orc.e4m3_cache_append(kc, vt, ks, vs, 70, kb[70:], vb[70:])
+    assert np.array_equal(kc[1, 70], orc.e4m3_encode(k[70, 1] / ks[1]))
+    assert np.array_equal(vt[1, 1, :, 12], orc.e4m3_encode(v[70, 1] / vs[1]))
+    assert np.array_equal(vt[0, 1, :, 27], orc.e4m3_encode(v[93, 0] / vs[0]))
+    hk, hv = orc.e4m3_history(kc, vt, ks, vs, T)
+    assert np.array_equal(hk, orc.bits(kb)) and np.array_equal(hv, orc.bits(vb))
+    # arbitrary bf16 inputs: the stored value is the nearest e4m3 multiple
+    kr, vr = rand_hist(T, 41)
+    orc.e4m3_cache_append(kc, vt, ks, vs, 0, kr, vr)
+    hk, _ = orc.e4m3_history(kc, vt, ks, vs, T)
+    x = f64(kr) / np.array(ks)[None, :, None]
+    got = (hk.astype(np.uint32) << 16).view(np.float32).astype(np.float64) / np.array(ks)[None, :, None]
+    err = np.abs(got - x)
+    bound = np.maximum(np.ldexp(1.0, np.frexp(np.abs(x))[1] - 1 - 4), 2.0 ** -10)  # half a step
+    assert np.all(err <= bound * (1 + 1e-12))
+    with pytest.raises(ValueError):
+        orc.e4m3_cache_append(kc, vt, [0.3, 1.0], vs, 0, kr[:1], vr[:1])
+
+
 @pytest.mark.parametrize("kind,p", [(orc.LOCAL, 0), (orc.LOCAL, 100), (orc.LOCAL, 2046),
                                     (orc.LOCAL, 2047), (orc.LOCAL, 3000), (orc.GLOBAL, 3000)])
 def test_zero_keys_give_window_mean(kind, p):
