@@ -489,6 +489,53 @@ def leg_paged(wl, page_size=256):
     return res
 
 
+def leg_e4m3(wl, steps=16):
+    """Global layers from FP8 (e4m3) caches: each of the 13 global caches is
+    quantised into its own FP8 cache (per-head scales 1.0: N(0,1) data sits
+    well inside the e4m3 range), then (a) the 13 global decodes from one
+    graph and (b) the whole 52-layer decode step with the global layers on
+    FP8, beside the same graphs on the bf16 caches."""
+    import torch
+    mg, dev, err = wl.mg, wl.dev, wl.err
+    glob = [l for l in range(N_LAYERS) if wl.kinds[l] == mg.GLOBAL]
+    p_q = PROMPT - 1
+    e4 = {}
+    for l in glob:
+        c = mg.E4M3KVCache(1, wl.cap, device=dev)
+        src = wl.caches[l]
+        for a in range(0, PROMPT, 16384):  # quantise through the library's append
+            z = min(PROMPT, a + 16384)
+            kn = src.k[0, :, a:z].permute(1, 0, 2).unsqueeze(0).contiguous()
+            vn = src.v[0, :, a:z].permute(1, 0, 2).unsqueeze(0).contiguous()
+            mg.mg_kv_append(wl.layers[l], c, torch.tensor([a], dtype=torch.int32, device=dev), kn, vn,
+                            err)
+        e4[l] = c
+    torch.cuda.synchronize()
+    pos = torch.tensor([p_q], dtype=torch.int32, device=dev)
+    q = torch.randn((N_LAYERS, 1, 32, 128), device=dev).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    ws = [mg.workspace(mg.OP_DECODE, wl.layers[l], 1, 1, PROMPT, device=dev) for l in range(N_LAYERS)]
+    res = {"scales": "1.0 per KV head", "caches_mib": sum(c.nbytes() for c in e4.values()) / 2 ** 20}
+    for name, caches in (("bf16", {l: wl.caches[l] for l in glob}), ("e4m3", e4)):
+        us = _graph_us(lambda: [mg.mg_attn_decode(wl.layers[l], caches[l], pos, PROMPT, q[l], o[l],
+                                                  ws[l], err) for l in glob], calls=len(glob))
+        nbytes = (p_q + 1) * (KV_BYTES_PER_KEY if name == "bf16" else KV_BYTES_PER_KEY // 2) \
+            + QO_BYTES_PER_TOKEN
+        res[f"global_decode_us_{name}"] = us
+        res[f"global_decode_gbs_{name}"] = nbytes / us / 1e3
+    # the whole step: 39 local layers (bf16 ring) + 13 global layers
+    for name in ("bf16", "e4m3"):
+        caches = [e4[l] if (name == "e4m3" and l in e4) else wl.caches[l] for l in range(N_LAYERS)]
+        us = _graph_us(lambda: [mg.mg_attn_decode(wl.layers[l], caches[l], pos, PROMPT, q[l], o[l],
+                                                  ws[l], err) for l in range(N_LAYERS)])
+        res[f"step_us_{name}"] = us
+        res[f"tokens_per_s_{name}"] = 1e6 / us
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after the e4m3 leg"
+    del e4
+    return res
+
+
 def run_gpu(args, rank, world):
     import torch
     from hybrid_local_global_attn_b300 import mg
@@ -518,6 +565,9 @@ def run_gpu(args, rank, world):
     if "paged" in legs:
         line_extra["paged"] = leg_paged(wl)
         log("paged: " + json.dumps(line_extra["paged"]))
+    if "e4m3" in legs:
+        line_extra["e4m3"] = leg_e4m3(wl)
+        log("e4m3: " + json.dumps(line_extra["e4m3"]))
 
     # ------------------------------------------------------------- decode ----
     ws_dec = [mg.workspace(mg.OP_DECODE, layers[l], 1, 1, cap, device=dev) for l in range(N_LAYERS)]
@@ -746,7 +796,19 @@ def run_ncu_case(name):
     dev = torch.device("cuda", 0)
     err = mg.error_word()
     bf = torch.bfloat16
-    if name in ("decode_global", "verify_global"):
+    if name == "decode_global_e4m3":
+        T = 262144  # 128 MB of FP8 K/V codes: larger than L2
+        cache = mg.E4M3KVCache(1, T)
+        cache.k.random_(0, 0x7E)  # finite codes
+        cache.v.random_(0, 0x7E)
+        lay = mg.make_layer(mg.GLOBAL)
+        ws = mg.workspace(mg.OP_DECODE, lay, 1, 1, T)
+        q = torch.randn((1, 32, 128), device=dev).to(bf)
+        o = torch.empty_like(q)
+        pos = torch.tensor([T - 1], dtype=torch.int32, device=dev)
+        for _ in range(4):
+            mg.mg_attn_decode(lay, cache, pos, T, q, o, ws, err)
+    elif name in ("decode_global", "verify_global"):
         T = 262144  # 256 MB of K/V per layer
         cache = mg.KVCache(mg.GLOBAL, 1, T)
         cache.k.normal_()
@@ -818,12 +880,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="mg", choices=["mg", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--legs", default="prefill,verify,paged,decode",
+    ap.add_argument("--legs", default="prefill,verify,paged,e4m3,decode",
                     help="comma list of legs to run besides decode")
     ap.add_argument("--fill", default="prefill", choices=["prefill", "random"],
                     help="random: fill caches without attention (profiling runs only)")
     ap.add_argument("--ncu-case", default=None,
-                    help="decode_global | verify_global | decode_local | verify_local | "
+                    help="decode_global | decode_global_e4m3 | verify_global | decode_local | verify_local | "
                          "prefill_global | prefill_local")
     ap.add_argument("--micro", action="store_true",
                     help="per-call cost of each entry point in graphs of back-to-back calls")

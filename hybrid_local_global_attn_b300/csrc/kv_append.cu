@@ -9,10 +9,27 @@
 // of each sequence is written ("第三招：D-Flash投机解码实现3倍提速",
 // kongchang.com: the main model checks the drafted block in one pass and
 // keeps what it accepts).
+#include <cuda_fp8.h>
+
 #include "mg_internal.h"
 #include "mg_ptx.cuh"
 
 namespace mg {
+
+// e4m3 codes (round to nearest even, saturated) of 8 bf16 values times mul,
+// in memory order.
+__device__ __forceinline__ uint2 e4m3_pack8(uint4 raw, float mul) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t out[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16) * mul;
+    const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * mul;
+    const uint32_t two = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+    out[i >> 1] |= (two & 0xFFFFu) << (16 * (i & 1));
+  }
+  return make_uint2(out[0], out[1]);
+}
 
 // Thread idx of sequence b moves one 16-byte chunk of one K row and one V row.
 __device__ __forceinline__ void append_chunk(const AppendParams &p, int b, int64_t idx) {
@@ -57,6 +74,25 @@ __device__ __forceinline__ void append_chunk(const AppendParams &p, int b, int64
     slot = pos;
   }
   const size_t src = ((static_cast<size_t>(b) * p.n + t) * kHkv + g) * kD + c * 8;
+  if (p.dtype == MG_E4M3) {
+    // FP8 global cache (linear): 8 dims of K -> 8 code bytes of the K row;
+    // 8 dims of V -> one code byte in each of 8 rows of the transposed tile
+    const uint4 kraw = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src));
+    const uint4 vraw = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src));
+    const uint2 kc = e4m3_pack8(kraw, p.k_mul[g]);
+    const uint2 vc = e4m3_pack8(vraw, p.v_mul[g]);
+    const size_t head = static_cast<size_t>(b) * kHkv + g;
+    uint8_t *kdst = reinterpret_cast<uint8_t *>(p.k_cache) + (head * p.slots + slot) * kD + c * 8;
+    *reinterpret_cast<uint2 *>(kdst) = kc;
+    const int j = static_cast<int>(slot % 16);
+    const int col = 16 * static_cast<int>((slot % 64) / 16) + 4 * ((j % 8) / 2) + 2 * (j / 8) + j % 2;
+    uint8_t *vdst = reinterpret_cast<uint8_t *>(p.v_cache) +
+                    (head * (p.slots / 64) + slot / 64) * (kD * 64) + static_cast<size_t>(c * 8) * 64 + col;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      vdst[i * 64] = static_cast<uint8_t>((i < 4 ? vc.x : vc.y) >> (8 * (i & 3)));
+    return;
+  }
   size_t dst;
   if (p.kind == 0) {
     dst = ((static_cast<size_t>(b) * kHkv + g) * p.slots + slot) * kD + c * 8;
@@ -93,6 +129,11 @@ __global__ void __launch_bounds__(256)
   p.slots = cp.slots[l];
   p.kind = cp.kind[l];
   p.map = cp.map[l];
+  p.dtype = cp.dtype[l];
+  p.k_mul[0] = cp.k_mul[l][0];
+  p.k_mul[1] = cp.k_mul[l][1];
+  p.v_mul[0] = cp.v_mul[l][0];
+  p.v_mul[1] = cp.v_mul[l][1];
   if (l != 0) p.pos_next = nullptr;
   append_chunk(p, blockIdx.y, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
 }

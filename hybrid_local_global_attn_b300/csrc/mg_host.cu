@@ -39,10 +39,13 @@ EncodeTiledFn encode_fn() {
 struct MapKey {
   const void *base;
   uint32_t rank;
+  uint32_t bytes_per_elem;  // 2: bf16, 1: e4m3 codes
+  uint32_t swizzle;         // bytes: 128 or 64
   uint64_t dims[4];
   uint32_t box[4];
   bool operator==(const MapKey &o) const {
-    return base == o.base && rank == o.rank && std::memcmp(dims, o.dims, sizeof dims) == 0 &&
+    return base == o.base && rank == o.rank && bytes_per_elem == o.bytes_per_elem &&
+           swizzle == o.swizzle && std::memcmp(dims, o.dims, sizeof dims) == 0 &&
            std::memcmp(box, o.box, sizeof box) == 0;
   }
 };
@@ -55,18 +58,22 @@ constexpr int kMapCache = 512;
 MapEntry g_maps[kMapCache];
 std::mutex g_map_mu;
 
-// bf16 tensor, contiguous rows of 128 elements; strides derive from dims.
+// Dense tensor (bf16 or bytes) whose strides derive from dims; boxes land in
+// shared memory with the given swizzle (128 or 64 bytes).
 bool make_map(CUtensorMap *out, const void *base, uint32_t rank, const uint64_t *dims,
-              const uint32_t *box) {
+              const uint32_t *box, uint32_t bytes_per_elem = 2, uint32_t swizzle = 128) {
   MapKey key{};
   key.base = base;
   key.rank = rank;
+  key.bytes_per_elem = bytes_per_elem;
+  key.swizzle = swizzle;
   for (uint32_t i = 0; i < rank; ++i) {
     key.dims[i] = dims[i];
     key.box[i] = box[i];
   }
   size_t h = reinterpret_cast<uintptr_t>(base) >> 8;
   for (uint32_t i = 0; i < rank; ++i) h = h * 1000003u ^ (dims[i] * 31u + box[i]);
+  h = h * 31u + bytes_per_elem * 7u + swizzle;
   MapEntry &e = g_maps[h % kMapCache];
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
@@ -79,7 +86,7 @@ bool make_map(CUtensorMap *out, const void *base, uint32_t rank, const uint64_t 
   if (fn == nullptr) return false;
   cuuint64_t gdim[4], gstride[3];
   cuuint32_t gbox[4], estr[4] = {1, 1, 1, 1};
-  uint64_t stride = 2;
+  uint64_t stride = bytes_per_elem;
   for (uint32_t i = 0; i < rank; ++i) {
     gdim[i] = dims[i];
     gbox[i] = box[i];
@@ -87,8 +94,10 @@ bool make_map(CUtensorMap *out, const void *base, uint32_t rank, const uint64_t 
     stride *= dims[i];
   }
   CUtensorMap m;
-  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), gdim,
-                  gstride, gbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(&m, bytes_per_elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                  rank, const_cast<void *>(base), gdim, gstride, gbox, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   {
@@ -112,15 +121,15 @@ bool map_rows(CUtensorMap *m, const void *base, uint64_t rows, uint64_t outer, u
 
 cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id) {
   static std::mutex mu;
-  static uint64_t done[4] = {0, 0, 0, 0};  // bit d: set on device d
+  static uint64_t done[8] = {};  // bit d: set on device d
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || kernel_id < 0 || kernel_id >= 4) return cudaErrorInvalidValue;
+  if (dev < 0 || dev >= 64 || kernel_id < 0 || kernel_id >= 8) return cudaErrorInvalidValue;
   std::lock_guard<std::mutex> lk(mu);
   if (done[kernel_id] & (1ull << dev)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && kernel_id >= 2)  // the local-layer kernels run 16-CTA clusters
+  if (e == cudaSuccess && (kernel_id == 2 || kernel_id == 3))  // local layers: 16-CTA clusters
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[kernel_id] |= 1ull << dev;
   return e;
@@ -180,11 +189,27 @@ int check_layer(const mg_layer *L) {
   return MG_OK;
 }
 
+// A positive power of two whose reciprocal is also a normal float.
+bool pow2_scale(float s) {
+  if (!(s > 0.f) || !std::isfinite(s)) return false;
+  int e = 0;
+  const float m = std::frexp(s, &e);
+  return m == 0.5f && e - 1 >= -126 && e - 1 <= 126;
+}
+
 int check_cache(const mg_layer *L, const mg_cache *C) {
   if (C == nullptr || C->k == nullptr || C->v == nullptr) return MG_ERR_INVALID;
   if (C->batch < 1 || C->slots < 1) return MG_ERR_INVALID;
   if (L->kind == MG_LOCAL && C->slots != kWindow) return MG_ERR_UNSUPPORTED;
   if (!aligned16(C->k) || !aligned16(C->v)) return MG_ERR_INVALID;
+  if (C->dtype != MG_BF16) {
+    // FP8: global layers, linear layout, whole 64-position tiles, power-of-two scales
+    if (C->dtype != MG_E4M3 || L->kind != MG_GLOBAL || C->page_table != nullptr)
+      return MG_ERR_UNSUPPORTED;
+    if (C->slots % 64 != 0) return MG_ERR_INVALID;
+    for (int g = 0; g < kHkv; ++g)
+      if (!pow2_scale(C->k_scale[g]) || !pow2_scale(C->v_scale[g])) return MG_ERR_INVALID;
+  }
   if (C->page_table != nullptr) {
     if (L->kind != MG_GLOBAL) return MG_ERR_UNSUPPORTED;  // the ring is never paged
     if (C->page_size < kTcKeys || C->page_size % kTcKeys != 0) return MG_ERR_UNSUPPORTED;
@@ -193,6 +218,16 @@ int check_cache(const mg_layer *L, const mg_cache *C) {
     if (reinterpret_cast<uintptr_t>(C->page_table) % 4 != 0) return MG_ERR_INVALID;
   }
   return MG_OK;
+}
+
+// Element type of a checked cache and, for FP8, the exact reciprocals of its
+// power-of-two scales.
+void set_dtype(const mg_cache *C, int32_t *dtype, float *k_mul, float *v_mul) {
+  *dtype = C->dtype;
+  for (int g = 0; g < kHkv; ++g) {
+    k_mul[g] = C->dtype == MG_E4M3 ? 1.0f / C->k_scale[g] : 1.0f;
+    v_mul[g] = C->dtype == MG_E4M3 ? 1.0f / C->v_scale[g] : 1.0f;
+  }
 }
 
 // Rows of a checked cache as the kernels address them.
@@ -342,6 +377,11 @@ size_t mg_cache_bytes(int32_t kind, int32_t batch, int32_t capacity) {
   return static_cast<size_t>(2) * batch * kHkv * slots * kD * 2;
 }
 
+size_t mg_e4m3_cache_bytes(int32_t batch, int32_t capacity) {
+  if (batch < 0 || capacity < 0 || capacity % 64 != 0) return 0;
+  return static_cast<size_t>(2) * batch * kHkv * capacity * kD;
+}
+
 size_t mg_page_pool_bytes(int32_t num_pages, int32_t page_size) {
   if (num_pages < 0 || page_size < kTcKeys || page_size % kTcKeys != 0) return 0;
   return static_cast<size_t>(2) * num_pages * kHkv * page_size * kD * 2;
@@ -402,6 +442,7 @@ int mg_kv_append(const mg_layer *layer, const mg_cache *cache, const int32_t *d_
   p.slots = cache->slots;
   p.kind = layer->kind;
   p.map = cache_map(cache);
+  set_dtype(cache, &p.dtype, p.k_mul, p.v_mul);
   return launch_status(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -431,6 +472,7 @@ int mg_kv_commit(const mg_layer *layer, const mg_cache *cache, const int32_t *d_
   p.slots = cache->slots;
   p.kind = layer->kind;
   p.map = cache_map(cache);
+  set_dtype(cache, &p.dtype, p.k_mul, p.v_mul);
   return launch_status(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -468,6 +510,7 @@ int mg_kv_commit_layers(int32_t n_layers, const mg_layer *layers, const mg_cache
     p.slots[l] = caches[l].slots;
     p.kind[l] = layers[l].kind;
     p.map[l] = cache_map(&caches[l]);
+    set_dtype(&caches[l], &p.dtype[l], p.k_mul[l], p.v_mul[l]);
   }
   p.layer_stride = static_cast<size_t>(caches[0].batch) * n * kHkv * kD;
   p.layers = n_layers;
@@ -491,8 +534,22 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   if (ws_bytes < w.total || (w.total > 0 && ws == nullptr)) return MG_ERR_WORKSPACE;
   if (w.total > 0 && !aligned16(ws)) return MG_ERR_INVALID;
   CUtensorMap tk, tv;
-  if (!map_cache(&tk, cache, cache->k, kDecTile) || !map_cache(&tv, cache, cache->v, kDecTile))
+  const bool e4m3 = cache->dtype == MG_E4M3;
+  if (e4m3) {
+    // K codes: (128 bytes, slots, batch x heads); V codes: transposed tiles
+    // (64 positions, 128 dims, slots / 64, batch x heads)
+    const uint64_t outer = static_cast<uint64_t>(cache->batch) * kHkv;
+    const uint64_t kd[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(cache->slots), outer};
+    const uint32_t kb[3] = {static_cast<uint32_t>(kD), kE4m3Tile, 1};
+    const uint64_t vd[4] = {64, static_cast<uint64_t>(kD), static_cast<uint64_t>(cache->slots / 64),
+                            outer};
+    const uint32_t vb[4] = {64, static_cast<uint32_t>(kD), kE4m3Tile / 64, 1};
+    if (!make_map(&tk, cache->k, 3, kd, kb, 1, 128) || !make_map(&tv, cache->v, 4, vd, vb, 1, 64))
+      return MG_ERR_CUDA;
+  } else if (!map_cache(&tk, cache, cache->k, kDecTile) ||
+             !map_cache(&tv, cache, cache->v, kDecTile)) {
     return MG_ERR_CUDA;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (layer->kind == MG_LOCAL)
     return launch_status(launch_local(layer, cache, d_pos, 1, max_len, q, k_new, v_new,
@@ -515,7 +572,11 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   p.max_len = max_len;
   p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
   p.map = cache_map(cache);
-  cudaError_t e = launch_decode(p, tk, tv, s);
+  for (int g = 0; g < kHkv; ++g) {
+    p.k_scale[g] = e4m3 ? cache->k_scale[g] : 1.0f;
+    p.v_scale[g] = e4m3 ? cache->v_scale[g] : 1.0f;
+  }
+  cudaError_t e = e4m3 ? launch_decode_e4m3(p, tk, tv, s) : launch_decode(p, tk, tv, s);
   if (e != cudaSuccess) return MG_ERR_CUDA;
   if (!split) return MG_OK;
   CombineParams c;
@@ -558,6 +619,7 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
   if (d_pos0 == nullptr || d_err == nullptr || q == nullptr || o == nullptr ||
       k_new == nullptr || v_new == nullptr)
     return MG_ERR_INVALID;
+  if (cache->dtype != MG_BF16) return MG_ERR_UNSUPPORTED;  // FP8 caches: decode only
   if (!aligned16(q) || !aligned16(o) || !aligned16(k_new) || !aligned16(v_new))
     return MG_ERR_INVALID;
   if (n < 1) return MG_ERR_INVALID;

@@ -35,6 +35,11 @@ constexpr int kDecSmem = kDecStages * kDecStageBytes + 1024 /*align*/ + 256 /*ba
                          64 * 8 /*rope turns*/;
 constexpr int kDecMaxSplits = 296;
 constexpr int kDecPrefetchTiles = 8;  // L2-prefetched tiles per global-layer CTA
+// FP8 (e4m3) global decode: 128-key stages of 32 KB (K codes + transposed V
+// codes), 3 deep
+constexpr int kE4m3Tile = 128;
+constexpr int kE4m3Stages = 3;
+constexpr int kE4m3PrefetchTiles = 8;
 
 // Local layers (ring attention for up to 16 query tokens): one 16-CTA cluster
 // per (sequence, KV head, group of query tokens), 128 ring slots per CTA.
@@ -109,6 +114,11 @@ struct AppendParams {
   uint32_t *err;
   int32_t batch, n, slots, kind;
   CacheMap map;  // global layers: where each position's row lives
+  // MG_E4M3 caches (global, linear): codes of k * k_mul[g], v * v_mul[g]
+  // (the reciprocals of power-of-two scales, so exact); V transposed per
+  // 64-position tile
+  int32_t dtype;
+  float k_mul[2], v_mul[2];
 };
 
 // A commit into up to MG_COMMIT_MAX_LAYERS caches in one launch; the block
@@ -118,6 +128,8 @@ struct CommitLayersParams {
   __nv_bfloat16 *k_cache[MG_COMMIT_MAX_LAYERS], *v_cache[MG_COMMIT_MAX_LAYERS];
   int32_t slots[MG_COMMIT_MAX_LAYERS], kind[MG_COMMIT_MAX_LAYERS];
   CacheMap map[MG_COMMIT_MAX_LAYERS];
+  int32_t dtype[MG_COMMIT_MAX_LAYERS];
+  float k_mul[MG_COMMIT_MAX_LAYERS][2], v_mul[MG_COMMIT_MAX_LAYERS][2];
   size_t layer_stride;
   int32_t layers;
 };
@@ -139,6 +151,7 @@ struct DecodeParams {  // global layers
   int32_t batch, slots, splits, max_len;
   float scale_log2;        // softmax scale * log2(e)
   CacheMap map;            // linear or paged rows of the cache
+  float k_scale[2], v_scale[2];  // MG_E4M3 caches: per KV head (powers of two)
 };
 
 
@@ -222,6 +235,9 @@ cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t s);
 cudaError_t launch_kv_commit_layers(const CommitLayersParams &p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                           cudaStream_t s);
+// FP8 cache: tk over K codes (128-byte rows), tv over transposed V tiles
+cudaError_t launch_decode_e4m3(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                               cudaStream_t s);
 // single-token ring kernel (picks p.tpc itself) and the tcgen05 ring kernel
 // for draft blocks (8 tokens per CTA)
 cudaError_t launch_local_tc(const LocalParams &p, const CUtensorMap &tk, const CUtensorMap &tv,

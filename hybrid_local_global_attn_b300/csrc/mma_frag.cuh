@@ -39,6 +39,23 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D (16x8 fp32) += A (16x16 f16, row) * B (16x8 f16, col).
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of 16-byte chunk `c` (0..3) of row `r` in a 64-byte-swizzled
+// box whose rows are 64 bytes (the chunk index is XOR-ed with bits 7..8 of
+// the row's byte offset).
+__device__ __forceinline__ uint32_t sw64(uint32_t r, uint32_t c) {
+  return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4);
+}
+
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled
 // box whose rows are 128 bytes.
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) {

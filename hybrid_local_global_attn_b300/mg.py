@@ -25,6 +25,7 @@ WINDOW = 2048
 VERIFY_MAX = 16
 N_LAYERS = 52
 LOCAL, GLOBAL = 0, 1
+BF16, E4M3 = 0, 1
 OP_DECODE, OP_VERIFY, OP_PREFILL = 0, 1, 2
 DERR_POSITION, DERR_TIMEOUT, DERR_COUNT, DERR_PAGE = 1, 2, 4, 8
 ROPE_THETA = 10000.0
@@ -40,7 +41,8 @@ class mg_cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("batch", ctypes.c_int32), ("slots", ctypes.c_int32),
                 ("page_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
-                ("num_pages", ctypes.c_int32)]
+                ("num_pages", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("k_scale", ctypes.c_float * 2), ("v_scale", ctypes.c_float * 2)]
 
 
 _P = ctypes.c_void_p
@@ -49,6 +51,8 @@ _LP = ctypes.POINTER(mg_layer)
 _CP = ctypes.POINTER(mg_cache)
 lib.mg_cache_bytes.argtypes = [_i32, _i32, _i32]
 lib.mg_cache_bytes.restype = ctypes.c_size_t
+lib.mg_e4m3_cache_bytes.argtypes = [_i32, _i32]
+lib.mg_e4m3_cache_bytes.restype = ctypes.c_size_t
 lib.mg_page_pool_bytes.argtypes = [_i32, _i32]
 lib.mg_page_pool_bytes.restype = ctypes.c_size_t
 lib.mg_workspace_bytes.argtypes = [_i32, _LP, _i32, _i32, _i32]
@@ -83,6 +87,10 @@ def mg_status_str(status: int) -> str:
 
 def mg_cache_bytes(kind: int, batch: int, capacity: int) -> int:
     return int(lib.mg_cache_bytes(kind, batch, capacity))
+
+
+def mg_e4m3_cache_bytes(batch: int, capacity: int) -> int:
+    return int(lib.mg_e4m3_cache_bytes(batch, capacity))
 
 
 def mg_page_pool_bytes(num_pages: int, page_size: int) -> int:
@@ -154,6 +162,28 @@ class PagedKVCache:
         k = self.k[pages].permute(1, 0, 2, 3).reshape(HKV, -1, D)[:, :upto]
         v = self.v[pages].permute(1, 0, 2, 3).reshape(HKV, -1, D)[:, :upto]
         return k, v
+
+
+class E4M3KVCache:
+    """A global layer's FP8 cache: K codes uint8 [batch][2][slots][128], V codes
+    transposed per 64-position tile uint8 [batch][2][slots // 64][128][64], and
+    one power-of-two scale per KV head for K and for V."""
+
+    def __init__(self, batch: int, capacity: int, k_scale=(1.0, 1.0), v_scale=(1.0, 1.0),
+                 device="cuda"):
+        slots = (int(capacity) + 63) // 64 * 64
+        self.kind = GLOBAL
+        self.batch = batch
+        self.slots = slots
+        self.k = torch.zeros((batch, HKV, slots, D), dtype=torch.uint8, device=device)
+        self.v = torch.zeros((batch, HKV, slots // 64, D, 64), dtype=torch.uint8, device=device)
+        self.k_scale = tuple(float(x) for x in k_scale)
+        self.v_scale = tuple(float(x) for x in v_scale)
+        self.struct = mg_cache(self.k.data_ptr(), self.v.data_ptr(), batch, slots, None, 0, 0, E4M3,
+                               (ctypes.c_float * 2)(*self.k_scale), (ctypes.c_float * 2)(*self.v_scale))
+
+    def nbytes(self) -> int:
+        return self.k.numel() + self.v.numel()
 
 
 def _ptr(t, dtype=None):

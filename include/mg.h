@@ -54,6 +54,9 @@ extern "C" {
 
 typedef enum { MG_LOCAL = 0, MG_GLOBAL = 1 } mg_kind;
 
+/* Element type of a KV cache. */
+typedef enum { MG_BF16 = 0, MG_E4M3 = 1 } mg_dtype;
+
 typedef enum {
   MG_OP_DECODE = 0,
   MG_OP_VERIFY = 1,
@@ -104,7 +107,21 @@ typedef struct {
  * memory, owned and filled by the caller (entries of positions a call does
  * not touch are never read).  A kernel that meets an entry outside
  * [0, num_pages) flags MG_DERR_PAGE and uses page 0 instead (the result is
- * then wrong, but no memory outside the pool is touched). */
+ * then wrong, but no memory outside the pool is touched).
+ *
+ * FP8 (dtype == MG_E4M3; global layers, linear layout, slots a multiple of
+ * 64): the cache holds OCP E4M3 codes (round to nearest even, saturated at
+ * +-448) of k / k_scale[g] and v / v_scale[g], one scale per KV head, each a
+ * positive power of two so that the division is exact; attention reads the
+ * codes back as code value x scale (cache quantisation shrinks the cache
+ * [P2 "窄缓存为长上下文留出空间"]; half the bytes of bf16).
+ *   k : uint8 [batch][2][slots][128]
+ *   v : uint8 [batch][2][slots / 64][128][64], i.e. each 64-position tile
+ *       transposed (dims x positions); inside a tile, position p sits in
+ *       column 16 * ((p % 64) / 16) + c(p % 16), c(j) = 4 * ((j % 8) / 2) +
+ *       2 * (j / 8) + j % 2.
+ * Only append, commit and decode take an FP8 cache (verify and prefill
+ * return MG_ERR_UNSUPPORTED). */
 typedef struct {
   void *k;
   void *v;
@@ -113,6 +130,9 @@ typedef struct {
   const int32_t *page_table; /* NULL: linear layout */
   int32_t page_size;         /* paged: tokens per page, a multiple of 256 */
   int32_t num_pages;         /* paged: pages in each of the k and v pools */
+  int32_t dtype;             /* mg_dtype; MG_BF16 unless stated */
+  float k_scale[2];          /* MG_E4M3: per KV head, positive powers of two */
+  float v_scale[2];
 } mg_cache;
 
 /* Host-only.  Bytes of one layer's K+V cache: 2 (K,V) x batch x 2 heads x
@@ -120,6 +140,11 @@ typedef struct {
  * and capacity for MG_GLOBAL.  Per token per layer this is 1024 bytes
  * [P1 §01].  Returns 0 for a bad kind or a negative size. */
 size_t mg_cache_bytes(int32_t kind, int32_t batch, int32_t capacity);
+
+/* Host-only.  Bytes of one global layer's FP8 (MG_E4M3) K+V cache: 2 x
+ * batch x 2 heads x capacity x 128 bytes (512 per token).  Returns 0 for a
+ * negative size or a capacity that is not a multiple of 64. */
+size_t mg_e4m3_cache_bytes(int32_t batch, int32_t capacity);
 
 /* Host-only.  Bytes of one layer's paged K+V pools: 2 (K,V) x num_pages x
  * 2 heads x page_size x 128 x 2 bytes.  Returns 0 for a negative size or a

@@ -205,6 +205,12 @@ def _check_pow2(scales):
             raise ValueError(f"scale {s} is not a positive power of two")
 
 
+def _e4m3_v_columns(pos):
+    """Column of each position inside its transposed 64-position V tile."""
+    pos = np.asarray(pos)
+    return 16 * ((pos % 64) // 16) + np.asarray(E4M3_V_COLUMN)[pos % 16]
+
+
 def e4m3_cache_append(k_codes, vt_codes, k_scale, v_scale, pos0, k_new, v_new):
     """Store positions pos0 .. pos0+n-1 of one sequence in an FP8 cache (in
     place).  K: k_codes[g][p][d] = e4m3(k / k_scale[g]).  V, transposed per
@@ -212,29 +218,29 @@ def e4m3_cache_append(k_codes, vt_codes, k_scale, v_scale, pos0, k_new, v_new):
     E4M3_V_COLUMN[p % 16]] = e4m3(v / v_scale[g]).  Scales are powers of two,
     so the division is exact and the code is the value's correct rounding."""
     _check_pow2(list(k_scale) + list(v_scale))
-    kn = bits(k_new).astype(np.uint32) << 16
-    vn = bits(v_new).astype(np.uint32) << 16
-    kf = kn.view(np.float32).astype(np.float64)
-    vf = vn.view(np.float32).astype(np.float64)
-    for t in range(kf.shape[0]):
-        p = pos0 + t
-        col = 16 * ((p % 64) // 16) + E4M3_V_COLUMN[p % 16]
-        for g in range(HKV):
-            k_codes[g, p, :] = e4m3_encode(kf[t, g] / k_scale[g])
-            vt_codes[g, p // 64, :, col] = e4m3_encode(vf[t, g] / v_scale[g])
+    kf = (bits(k_new).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    vf = (bits(v_new).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    n = kf.shape[0]
+    pos = np.arange(pos0, pos0 + n)
+    tiles, cols = pos // 64, _e4m3_v_columns(pos)
+    dims = np.arange(D)
+    for g in range(HKV):
+        k_codes[g, pos0:pos0 + n, :] = e4m3_encode(kf[:, g, :] / k_scale[g])
+        vt_codes[g, tiles[:, None], dims[None, :], cols[:, None]] = e4m3_encode(vf[:, g, :] / v_scale[g])
 
 
 def e4m3_history(k_codes, vt_codes, k_scale, v_scale, upto):
     """Positions 0 .. upto-1 of an FP8 cache dequantised (code value x scale,
     exactly representable in bf16), as bf16 bit patterns [upto][2][128] for
     attention()."""
+    pos = np.arange(upto)
+    tiles, cols = pos // 64, _e4m3_v_columns(pos)
+    dims = np.arange(D)
     k = np.empty((upto, HKV, D), np.float64)
     v = np.empty((upto, HKV, D), np.float64)
-    for p in range(upto):
-        col = 16 * ((p % 64) // 16) + E4M3_V_COLUMN[p % 16]
-        for g in range(HKV):
-            k[p, g] = e4m3_decode(k_codes[g, p, :]) * k_scale[g]
-            v[p, g] = e4m3_decode(vt_codes[g, p // 64, :, col]) * v_scale[g]
+    for g in range(HKV):
+        k[:, g, :] = e4m3_decode(k_codes[g, :upto, :]) * k_scale[g]
+        v[:, g, :] = e4m3_decode(vt_codes[g, tiles[:, None], dims[None, :], cols[:, None]]) * v_scale[g]
 
     def to_bf16_bits(a):
         f = a.astype(np.float32)

@@ -116,6 +116,23 @@ def test_host_side_rejections_launch_nothing(mg):
     assert lib.mg_kv_commit(by(L), by(cache), fake, 4, other, ctypes.c_void_p(0x1008), fake,
                             None, fake, None) == 1
     assert lib.mg_kv_commit(by(L), by(cache), fake, 0, other, fake, fake, None, fake, None) == 0
+    # FP8 caches: global, linear, 64-multiple slots, power-of-two scales;
+    # verify and prefill take none
+    def e4(slots, ks=(1.0, 0.5), vs=(2.0, 1.0), table=None):
+        return mg.mg_cache(0x10000, 0x20000, 1, slots, table, 256 if table else 0, 4 if table else 0,
+                           mg.E4M3, (ctypes.c_float * 2)(*ks), (ctypes.c_float * 2)(*vs))
+    assert lib.mg_kv_append(by(L), by(e4(2048)), fake, 0, fake, fake, fake, None) == 2
+    assert lib.mg_kv_append(by(G), by(e4(4096, ks=(0.3, 1.0))), fake, 0, fake, fake, fake, None) == 1
+    assert lib.mg_kv_append(by(G), by(e4(4096, vs=(0.0, 1.0))), fake, 0, fake, fake, fake, None) == 1
+    assert lib.mg_kv_append(by(G), by(e4(4000)), fake, 0, fake, fake, fake, None) == 1
+    assert lib.mg_kv_append(by(G), by(e4(4096, table=0x3000)), fake, 0, fake, fake, fake, None) == 2
+    assert lib.mg_kv_append(by(G), by(e4(4096)), fake, 0, fake, fake, fake, None) == 0
+    assert lib.mg_attn_verify(by(G), by(e4(4096)), fake, 16, 1000, fake, fake, fake, fake, fake,
+                              1 << 30, fake, None) == 2
+    assert lib.mg_attn_prefill(by(G), by(e4(4096)), fake, 16, 1000, fake, fake, fake, fake, fake,
+                               1 << 30, fake, None) == 2
+    assert mg.mg_e4m3_cache_bytes(2, 4096) == 2 * 2 * 2 * 4096 * 128
+    assert mg.mg_e4m3_cache_bytes(2, 4000) == 0
     # multi-layer commit: layer count in [1, 64], one batch for all caches
     lays = (mg.mg_layer * 2)(L, G)
     gcache = mg.mg_cache(0x10000, 0x20000, 1, 4096)
