@@ -244,9 +244,11 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
 
+  // The position is loaded first, but nothing below waits for it until the
+  // loads that do not depend on it are in flight: the piece's tiles, the
+  // block's rows and the raw query (for an invalid position they are read
+  // and then dropped).
   const int32_t p0 = p.pos[b];  // position of query token 0 of the sequence
-  const bool bad = p0 < 0 || static_cast<int64_t>(p0) + p.n > p.max_len;
-  if (bad && my_rank == 0 && g == 0 && i0 == 0 && threadIdx.x == 0) set_err(p.err, MG_DERR_POSITION);
 
   if (threadIdx.x == 0) {  // the piece's two tiles
     for (int t = 0; t < kLocTiles; ++t) {
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(kLocThreads, 1)
     // after the first barrier below.
     const int k = threadIdx.x >> 4, c = threadIdx.x & 15;
     uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = kr;
-    if (k < p.n && !bad) {
+    if (k < p.n) {
       const size_t src = ((static_cast<size_t>(b) * p.n + k) * kHkv + g) * kD;
       kr = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src) + c);
       vr = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src) + c);
@@ -279,6 +281,7 @@ __global__ void __launch_bounds__(kLocThreads, 1)
                  "r"(vr.x), "r"(vr.y), "r"(vr.z), "r"(vr.w)
                  : "memory");
   }
+  const bool bad = p0 < 0 || static_cast<int64_t>(p0) + p.n > p.max_len;
   {
     // ---------------------------------------------------- consumer warps ----
     const int tid = threadIdx.x;
@@ -297,16 +300,6 @@ __global__ void __launch_bounds__(kLocThreads, 1)
     const int qr = (tid & 127) >> 3, qc = tid & 7;
     bool waited = false, ok = true, rotated = false;
 
-    // fused append of a single new token: the warp whose keys hold its slot
-    const int32_t slot_new = p0 & (kWindow - 1);
-    const bool patch_here = patch_mode && !bad && slot_new >= key0 && slot_new < key0 + 16;
-    uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
-    if (patch_here) {
-      const size_t src = (static_cast<size_t>(b) * kHkv + g) * kD;
-      new_row = lane < 16 ? __ldg(reinterpret_cast<const uint4 *>(p.k_new + src) + (lane & 15))
-                          : __ldg(reinterpret_cast<const uint4 *>(p.v_new + src) + (lane & 15));
-    }
-
     uint4 qx = make_uint4(0u, 0u, 0u, 0u), qy = qx;  // raw dims 8 qc.. and 64 + 8 qc..
     auto load_q = [&](int i) {
       const uint4 *src = reinterpret_cast<const uint4 *>(
@@ -314,7 +307,18 @@ __global__ void __launch_bounds__(kLocThreads, 1)
       qx = __ldg(src);
       qy = __ldg(src + 8);
     };
-    if (!bad) load_q(i0);
+    load_q(i0);  // needs no position: issued before anything waits for it
+    if (bad && my_rank == 0 && g == 0 && i0 == 0 && tid == 0) set_err(p.err, MG_DERR_POSITION);
+
+    // fused append of a single new token: the warp whose keys hold its slot
+    const int32_t slot_new = p0 & (kWindow - 1);
+    const bool patch_here = patch_mode && !bad && slot_new >= key0 && slot_new < key0 + 16;
+    uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
+    if (patch_mode) {  // the row's address needs no position; only patch_here uses it
+      const size_t src = (static_cast<size_t>(b) * kHkv + g) * kD;
+      new_row = lane < 16 ? __ldg(reinterpret_cast<const uint4 *>(p.k_new + src) + (lane & 15))
+                          : __ldg(reinterpret_cast<const uint4 *>(p.v_new + src) + (lane & 15));
+    }
 
     for (int t = 0; t < cnt; ++t) {
       const int i = i0 + t;

@@ -224,9 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
 
+  // The position is loaded first, but nothing waits for it until the loads
+  // that do not depend on it are in flight: the piece's tiles, the raw
+  // queries and the block's rows (for an invalid position they are read and
+  // then dropped).
   const int32_t p0 = p.pos[b];
-  const bool bad = p0 < 0 || static_cast<int64_t>(p0) + p.n > p.max_len;
-  if (bad && my_rank == 0 && g == 0 && i0 == 0 && tid == 0) set_err(p.err, MG_DERR_POSITION);
   if (tid == 0) {  // the piece's 128 K and V rows
     mbar_arrive_expect_tx(bar_k, kPiece * kRowBytes);
     mbar_arrive_expect_tx(bar_v, kPiece * kRowBytes);
@@ -236,6 +238,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // raw query of row qr (token qr / 16, head qr % 16), dims 32 kh.. and 64 + 32 kh..
+  const int qr = tid >> 1, qt = qr >> 4;
+  uint4 qx[4], qy[4];
+  {
+    const bool live = qt < cnt;
+    const __nv_bfloat16 *src =
+        p.q + ((static_cast<size_t>(b) * p.n + i0 + (live ? qt : 0)) * kHq + g * kGroup + (qr & 15)) * kD +
+        32 * kh;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      qx[c] = live ? __ldg(reinterpret_cast<const uint4 *>(src) + c) : make_uint4(0u, 0u, 0u, 0u);
+      qy[c] = live ? __ldg(reinterpret_cast<const uint4 *>(src + 64) + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  // block rows 128..143 of K and V (first CTA): thread tid < 128 takes row
+  // tid / 8, 8-dim chunk tid % 8 (and its partner 64 dims on); K rotated by
+  // its slot's angle
+  const int bk = tid >> 3, bc = tid & 7;
+  uint4 kx = make_uint4(0u, 0u, 0u, 0u), ky = kx, vx = kx, vy = kx;
+  if (blk_here && tid < 128 && bk < p.n) {
+    const size_t src = ((static_cast<size_t>(b) * p.n + bk) * kHkv + g) * kD + 8 * bc;
+    kx = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src));
+    ky = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src + 64));
+    vx = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src));
+    vy = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src + 64));
+  }
+
+  // now the position
+  const bool bad = p0 < 0 || static_cast<int64_t>(p0) + p.n > p.max_len;
+  if (bad && my_rank == 0 && g == 0 && i0 == 0 && tid == 0) set_err(p.err, MG_DERR_POSITION);
   // query-version angles: entry (t, v, f) = R((b_t + 2048 v) w_f), b_t the slot of token t
   for (int e = tid; e < kTpc * 2 * 64; e += kThreads) {
     const int t = e >> 7, v = (e >> 6) & 1, f = e & 63;
@@ -255,32 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (blk_here) need_lo = need_hi = true;  // block slots may fall on either side
   }
 
-  // raw query of row qr (token qr / 16, head qr % 16), dims 32 kh.. and 64 + 32 kh..
-  const int qr = tid >> 1, qt = qr >> 4;
-  uint4 qx[4], qy[4];
-  {
-    const bool live = qt < cnt && !bad;
-    const __nv_bfloat16 *src =
-        p.q + ((static_cast<size_t>(b) * p.n + i0 + (live ? qt : 0)) * kHq + g * kGroup + (qr & 15)) * kD +
-        32 * kh;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      qx[c] = live ? __ldg(reinterpret_cast<const uint4 *>(src) + c) : make_uint4(0u, 0u, 0u, 0u);
-      qy[c] = live ? __ldg(reinterpret_cast<const uint4 *>(src + 64) + c) : make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  // block rows 128..143 of K and V (first CTA): thread tid < 128 takes row
-  // tid / 8, 8-dim chunk tid % 8 (and its partner 64 dims on); K rotated by
-  // its slot's angle
   if (blk_here && tid < 128) {
-    const int k = tid >> 3, c = tid & 7;
-    uint4 kx = make_uint4(0u, 0u, 0u, 0u), ky = kx, vx = kx, vy = kx;
+    const int k = bk, c = bc;
+    if (bad) kx = ky = vx = vy = make_uint4(0u, 0u, 0u, 0u);
     if (k < p.n && !bad) {
-      const size_t src = ((static_cast<size_t>(b) * p.n + k) * kHkv + g) * kD + 8 * c;
-      kx = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src));
-      ky = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src + 64));
-      vx = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src));
-      vy = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src + 64));
       float2 a[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e)
