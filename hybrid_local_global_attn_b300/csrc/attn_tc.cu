@@ -125,7 +125,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const int ntiles = ti.ncache + ti.nnew;
 
-  if (threadIdx.x == 0) {
+  // The producer lane sets up the barriers and at once issues every copy the
+  // first key tile needs (Q, K and both V halves of tile 0: no stage waits),
+  // so they overlap the TMEM allocation and the CTA barrier below.
+  // Cache tile t lies in rows [crow0, crow0 + 256) of outer index couter
+  // (linear: rows from 0 of the sequence's head; paged: its page).  K of
+  // tile t + 1 is issued before V of tile t, so two tiles' entries live.
+  int32_t crow0[2] = {0, 0}, couter[2] = {b * kHkv + g, b * kHkv + g};
+  auto locate = [&](int t) {
+    if (p.map.table == nullptr || t >= ti.ncache) return;
+    const int32_t kp0 = tile_kp0(ti, t);
+    int32_t r, o;
+    cache_coord(p.map, b, g, kp0, &r, &o, p.err);
+    crow0[t & 1] = kp0 - r;
+    couter[t & 1] = o;
+  };
+  // keys kp0.. (rows) of K or V into dst (two 64-dim boxes), completing on fb
+  auto load = [&](bool is_v, int t, int32_t kp0, uint32_t dst, uint32_t bytes, uint32_t fb) {
+    const CUtensorMap *ma = is_v ? &tva : &tka;
+    const CUtensorMap *mb = is_v ? &tvb : &tkb;
+    mbar_arrive_expect_tx(fb, bytes);
+    for (int x = 0; x < 2; ++x) {
+      const uint32_t d = dst + x * (bytes / 2);
+      if (p.staged)
+        tma_load_3d(d, ma, fb, 64 * x, kp0 - ti.c0 + kWindow, b * kHkv + g);
+      else if (t < ti.ncache)
+        tma_load_3d(d, ma, fb, 64 * x, kp0 - crow0[t & 1], couter[t & 1]);
+      else
+        tma_load_4d(d, mb, fb, 64 * x, g, kp0 - ti.c0, b);
+    }
+  };
+  int issued_k = 0, issued_v = 0;
+  bool ok = true;
+  // K of tile t reuses the stage of tile t - 2 once its S = Q K^T has run
+  auto load_k = [&](int t) -> bool {
+    const int ks = t % kTcKStages;
+    if (t >= kTcKStages &&
+        !mbar_wait(bar_ke + 8 * ks, ((t / kTcKStages) - 1) & 1, &abort_flag))
+      return false;
+    locate(t);
+    load(false, t, tile_kp0(ti, t), sK + ks * kTcKTileBytes, kTcKTileBytes, bar_kf + 8 * ks);
+    ++issued_k;
+    return true;
+  };
+  // K runs a tile ahead of V (S = Q K^T of tile t + 1 is issued before
+  // P.V of tile t); V half u = 2 t + h reuses the stage of half u - 2
+  // once its P.V has run
+  if (warp == 8 && lane == 0) {
     abort_flag = 0;
     if (bad && split == 0 && qb == 0) set_err(p.err, MG_DERR_POSITION);
     mbar_init(bar_q, 1);
@@ -143,6 +189,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(bar_pfree, 1);
     mbar_init(bar_done, 1);
     fence_mbar_init();
+    if (ntiles > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tka);
+      tma_prefetch_desc(&tva);
+      tma_prefetch_desc(&tkb);
+      tma_prefetch_desc(&tvb);
+      const int32_t q_t0 = kTcPosPerCta * qb;  // position index within the block
+      mbar_arrive_expect_tx(bar_q, kTcQBytes);
+      for (int x = 0; x < 2; ++x)
+        tma_load_4d(sQ + x * (kTcQBytes / 2), &tq, bar_q, 64 * x, kGroup * g, q_t0, b);
+      (void)load_k(0);  // stage 0: no wait
+      for (int h = 0; h < 2; ++h) {  // V halves 0 and 1: stages 0 and 1, no wait
+        load(true, 0, tile_kp0(ti, 0) + kTcVRows * h, sV + h * kTcVTileBytes, kTcVTileBytes,
+             bar_vf + 8 * h);
+        ++issued_v;
+      }
+    }
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(&tmem_base_slot), 512);
@@ -157,65 +220,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------- producer ----
     if (lane == 0 && ntiles > 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tka);
-      tma_prefetch_desc(&tva);
-      tma_prefetch_desc(&tkb);
-      tma_prefetch_desc(&tvb);
-      const int32_t q_t0 = kTcPosPerCta * qb;  // position index within the block
-      mbar_arrive_expect_tx(bar_q, kTcQBytes);
-      for (int x = 0; x < 2; ++x)
-        tma_load_4d(sQ + x * (kTcQBytes / 2), &tq, bar_q, 64 * x, kGroup * g, q_t0, b);
-      // Cache tile t lies in rows [crow0, crow0 + 256) of outer index couter
-      // (linear: rows from 0 of the sequence's head; paged: its page).  K of
-      // tile t + 1 is issued before V of tile t, so two tiles' entries live.
-      int32_t crow0[2] = {0, 0}, couter[2] = {b * kHkv + g, b * kHkv + g};
-      auto locate = [&](int t) {
-        if (p.map.table == nullptr || t >= ti.ncache) return;
-        const int32_t kp0 = tile_kp0(ti, t);
-        int32_t r, o;
-        cache_coord(p.map, b, g, kp0, &r, &o, p.err);
-        crow0[t & 1] = kp0 - r;
-        couter[t & 1] = o;
-      };
-      // keys kp0.. (rows) of K or V into dst (two 64-dim boxes), completing on fb
-      auto load = [&](bool is_v, int t, int32_t kp0, uint32_t dst, uint32_t bytes, uint32_t fb) {
-        const CUtensorMap *ma = is_v ? &tva : &tka;
-        const CUtensorMap *mb = is_v ? &tvb : &tkb;
-        mbar_arrive_expect_tx(fb, bytes);
-        for (int x = 0; x < 2; ++x) {
-          const uint32_t d = dst + x * (bytes / 2);
-          if (p.staged)
-            tma_load_3d(d, ma, fb, 64 * x, kp0 - ti.c0 + kWindow, b * kHkv + g);
-          else if (t < ti.ncache)
-            tma_load_3d(d, ma, fb, 64 * x, kp0 - crow0[t & 1], couter[t & 1]);
-          else
-            tma_load_4d(d, mb, fb, 64 * x, g, kp0 - ti.c0, b);
-        }
-      };
-      int issued_k = 0, issued_v = 0;
-      bool ok = true;
-      // K of tile t reuses the stage of tile t - 2 once its S = Q K^T has run
-      auto load_k = [&](int t) -> bool {
-        const int ks = t % kTcKStages;
-        if (t >= kTcKStages &&
-            !mbar_wait(bar_ke + 8 * ks, ((t / kTcKStages) - 1) & 1, &abort_flag))
-          return false;
-        locate(t);
-        load(false, t, tile_kp0(ti, t), sK + ks * kTcKTileBytes, kTcKTileBytes, bar_kf + 8 * ks);
-        ++issued_k;
-        return true;
-      };
-      // K runs a tile ahead of V (S = Q K^T of tile t + 1 is issued before
-      // P.V of tile t); V half u = 2 t + h reuses the stage of half u - 2
-      // once its P.V has run
-      ok = load_k(0);
+      // K(0), V(0) went out before the CTA barrier
       for (int t = 0; ok && t < ntiles; ++t) {
         if (t + 1 < ntiles && !load_k(t + 1)) {
           ok = false;
           break;
         }
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2 && t > 0; ++h) {
           const int u = 2 * t + h, vs = u % kTcVStages;
           if (u >= kTcVStages &&
               !mbar_wait(bar_ve + 8 * vs, ((u / kTcVStages) - 1) & 1, &abort_flag)) {
@@ -432,14 +443,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool have = ok && ntiles > 0 && lrow > 0.f;
     const float inv = have ? 1.f / lrow : 0.f;
     const size_t orow = (static_cast<size_t>(b) * p.n + tloc) * kHq + h;
+    uint32_t oa[2][32];  // this thread's 64 output dims, both loads in flight at once
+    if (ok && ntiles > 0) {
+      tmem_ld32(tL + kColO + 64 * hh, oa[0]);
+      tmem_ld32(tL + kColO + 64 * hh + 32, oa[1]);
+      tmem_wait_ld();
+    }
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int d0 = 64 * hh + 32 * c;  // first dim of this 32-column chunk
-      uint32_t a[32];
-      if (ok && ntiles > 0) {
-        tmem_ld32(tL + kColO + d0, a);
-        tmem_wait_ld();
-      }
+      const uint32_t *a = oa[c];
       if (!row_valid) continue;
       if (p.splits == 1) {
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD + d0);
