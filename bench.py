@@ -536,6 +536,60 @@ def leg_e4m3(wl, steps=16):
     return res
 
 
+def leg_sweep(wl, hbm_peak, ctx=32768, batches=(1, 4, 16), steps=16):
+    """The decode sweep: one fused append + decode step through all 52 layers
+    at context `ctx` for each batch size, from a CUDA graph (caches filled
+    with N(0,1) values; every sequence at the same position).  GB/s of
+    algorithmic bytes (K/V of each key set + q/o)."""
+    import torch
+    mg, dev, err = wl.mg, wl.dev, wl.err
+    bf = torch.bfloat16
+    res = {"context": ctx}
+    for B in batches:
+        cap = ctx + steps + 8
+        layers = [mg.make_layer(mg.mg_layer_kind(l)) for l in range(N_LAYERS)]
+        caches = []
+        for l in range(N_LAYERS):
+            c = mg.KVCache(mg.mg_layer_kind(l), B, cap, device=dev)
+            c.k.normal_()
+            c.v.normal_()
+            caches.append(c)
+        ws = [mg.workspace(mg.OP_DECODE, layers[l], B, 1, cap, device=dev) for l in range(N_LAYERS)]
+        q = torch.randn((N_LAYERS, B, 32, 128), device=dev).to(bf)
+        kn = torch.randn((N_LAYERS, B, 1, 2, 128), device=dev).to(bf)
+        vn = torch.randn_like(kn)
+        o = torch.empty_like(q)
+        pos = torch.full((B,), ctx, dtype=torch.int32, device=dev)
+
+        def step():
+            for l in range(N_LAYERS):
+                mg.mg_append_decode(layers[l], caches[l], pos, cap, q[l], kn[l], vn[l], o[l], ws[l], err)
+
+        step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            g.replay()
+        e0.record()
+        for i in range(steps):
+            g.replay()  # the same position each step: the same bytes
+        e1.record()
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        nbytes = B * sum(decode_layer_bytes(mg.mg_layer_kind(l), ctx) for l in range(N_LAYERS))
+        res[f"b{B}"] = {"us_per_step": us, "gbs": nbytes / us / 1e3,
+                        "frac_of_measured_hbm": nbytes / us / 1e3 / hbm_peak,
+                        "tokens_per_s": B * 1e6 / us}
+        del caches, ws, q, kn, vn, o
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after the sweep"
+    return res
+
+
 def run_gpu(args, rank, world):
     import torch
     from hybrid_local_global_attn_b300 import mg
@@ -568,6 +622,9 @@ def run_gpu(args, rank, world):
     if "e4m3" in legs:
         line_extra["e4m3"] = leg_e4m3(wl)
         log("e4m3: " + json.dumps(line_extra["e4m3"]))
+    if "sweep" in legs:
+        line_extra["decode_sweep"] = leg_sweep(wl, hbm_peak)
+        log("sweep: " + json.dumps(line_extra["decode_sweep"]))
 
     # ------------------------------------------------------------- decode ----
     ws_dec = [mg.workspace(mg.OP_DECODE, layers[l], 1, 1, cap, device=dev) for l in range(N_LAYERS)]
@@ -890,7 +947,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="mg", choices=["mg", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--legs", default="prefill,verify,paged,e4m3,decode",
+    ap.add_argument("--legs", default="prefill,verify,paged,e4m3,sweep,decode",
                     help="comma list of legs to run besides decode")
     ap.add_argument("--fill", default="prefill", choices=["prefill", "random"],
                     help="random: fill caches without attention (profiling runs only)")
