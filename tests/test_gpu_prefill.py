@@ -75,3 +75,35 @@ def test_chunked_equals_unchunked(mg, kind):
     b = prefill_chunks(mg, kind, k, v, q, 512, capacity=T)
     d = (a.float() - b.float()).abs().max().item()
     assert d <= 2e-2, d
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_prefill_mixed_starts_with_a_rejected_sequence(mg, kind):
+    # One call, three sequences: sequence 0 starts at 0, sequence 1's block
+    # would run past max_len (flagged, its rows written as zeros), sequence 2
+    # starts after 2500 cached positions (the local ring has wrapped).  1200
+    # tokens make 150 query blocks per sequence and KV head.
+    li = 2 if kind == 0 else 3
+    B, n, c0s, max_len = 3, 1200, [0, 3000, 2500], 3700
+    k, v = synth.history(B, 4200, 23, li)
+    q = synth.queries(B, 4200, 23, li)
+    cache = mg.KVCache(kind, B, max_len)
+    lay = mg.make_layer(kind)
+    err = mg.error_word()
+    mg.mg_kv_append(lay, cache, torch.tensor([-1, -1, 0], dtype=torch.int32, device="cuda"),
+                    k[:, :2500].cuda().contiguous(), v[:, :2500].cuda().contiguous(), err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ~mg.DERR_POSITION == 0  # pos -1: the sequences left out
+    qb = torch.stack([q[b, c0:c0 + n] for b, c0 in enumerate(c0s)])
+    kb = torch.stack([k[b, c0:c0 + n] for b, c0 in enumerate(c0s)])
+    vb = torch.stack([v[b, c0:c0 + n] for b, c0 in enumerate(c0s)])
+    o, e = run_prefill(mg, kind, cache, c0s, qb, kb, vb, max_len)
+    assert int(e.item()) == mg.DERR_POSITION, hex(int(e.item()))
+    assert not o[1].float().abs().max().item()
+    olay = orc.layer(oracle_kind(kind))
+    for b in (0, 2):
+        c0 = c0s[b]
+        rows = sorted(set(list(range(0, 24)) + list(range(n - 24, n)) + list(range(0, n, 37))))
+        pos = [c0 + i for i in rows]
+        ref = orc.attention(olay, k[b, :c0 + n], v[b, :c0 + n], pos, q[b, pos])
+        compare(o[b, rows], ref, f"kind {kind} sequence {b} c0 {c0}")
