@@ -31,3 +31,44 @@ def history(batch: int, T: int, seed: int, layer: int, device="cpu"):
 def queries(batch: int, n: int, seed: int, layer: int, device="cpu"):
     """Queries [batch][n][32][128] of one layer."""
     return randn_bf16((batch, n, 32, 128), sub_seed(seed, layer, Q), device)
+
+
+# ---------------------------------------------------------------------------
+# Peaked inputs: the same N(0, 1) draws, reshaped so that softmax rows become
+# sharp.  These only scale or overwrite input values; they hold no attention
+# arithmetic.
+
+# Dimension the sink construction uses.  Its RoPE partner is SINK_DIM + 64;
+# dimension 63 has the lowest rotary frequency, so a key there keeps its
+# direction across a 2048-token window.
+SINK_DIM = 63
+SINK_Q = 8.0     # value written into every query at SINK_DIM
+SINK_K = 64.0    # value of a sink key at SINK_DIM (all its other dims are 0)
+
+
+def scaled(x: torch.Tensor, factor: float) -> torch.Tensor:
+    """x * factor, rounded once to bf16 (round to nearest even)."""
+    return (x.float() * float(factor)).to(torch.bfloat16)
+
+
+def sink_queries(q: torch.Tensor) -> torch.Tensor:
+    """Queries with dimension SINK_DIM set to SINK_Q and its RoPE partner to 0
+    (every head, every token); the other dimensions are kept."""
+    q = q.clone()
+    q[..., SINK_DIM] = SINK_Q
+    q[..., SINK_DIM + 64] = 0.0
+    return q
+
+
+def plant_sinks(k: torch.Tensor, positions, seq=None, values=None) -> torch.Tensor:
+    """Key history [B][T][2][128] with the rows at `positions` (of every
+    sequence, or of sequence `seq`) replaced by value * e_SINK_DIM in both KV
+    heads (value SINK_K unless `values` gives one per position).  Against
+    sink_queries such a key scores SINK_Q * value / sqrt(128) before rotation
+    (about 45 for SINK_K), while ordinary keys score N(0, ~1.5)."""
+    k = k.clone()
+    rows = k if seq is None else k[seq:seq + 1]
+    for n, p in enumerate(positions):
+        rows[:, p] = 0.0
+        rows[:, p, :, SINK_DIM] = SINK_K if values is None else float(values[n])
+    return k

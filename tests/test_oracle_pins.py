@@ -433,3 +433,90 @@ def test_full_attention_pair_count_matches_pages(golden_bytes):
     val, tol, _ = golden_bytes["full_attention_pairs_131k"]
     n = 131072
     assert abs(n * n - val) <= tol * val
+
+
+# --------------------------------------------------------------------------
+# Peaked and flat score distributions: the inputs the GPU parity tests use to
+# reach every softmax branch (queries scaled by 1e-3, 1, 40; a sink key far
+# above the rest).  The oracle is pinned on the same kind of inputs here.
+
+def brute_scores(kind, W, rope, k, qpos, q):
+    """Scaled scores [nq][32][T] with -inf outside the key set, in numpy with
+    complex-number RoPE (the formulation of brute_force above)."""
+    kd, qd = f64(k), f64(q)
+    T = kd.shape[0]
+    qpos = np.asarray(qpos)
+    w = THETA ** (-2.0 * np.arange(64) / 128.0)
+
+    def rot(x, t):
+        z = (x[..., :64] + 1j * x[..., 64:]) * np.exp(1j * t[:, None, None] * w)
+        return np.concatenate([z.real, z.imag], axis=-1)
+
+    if rope:
+        kd = rot(kd, np.arange(T, dtype=np.float64))
+        qd = rot(qd, qpos.astype(np.float64))
+    jj = np.arange(T)[None, :]
+    allowed = jj <= qpos[:, None]
+    if kind == orc.LOCAL:
+        allowed &= jj >= qpos[:, None] - W + 1
+    s = np.einsum("nhd,tgd->nhtg", qd, kd)  # [nq][32][T][2]
+    s = np.stack([s[:, h, :, h // 16] for h in range(32)], axis=1) * SCALE
+    return np.where(allowed[:, None, :], s, -np.inf)
+
+
+@pytest.mark.parametrize("kind", [orc.LOCAL, orc.GLOBAL])
+@pytest.mark.parametrize("factor", [1e-3, 40.0, 400.0])
+def test_scaled_queries_match_brute_force(kind, factor):
+    # x400 puts scores near +-1e3: exp() of them overflows fp64 unless the
+    # running maximum is subtracted first, so a softmax written without it
+    # fails here; x1e-3 makes every row nearly uniform.
+    T = 300
+    k, v = rand_hist(T, 21)
+    qpos = np.array([0, 1, 7, 63, 64, 150, 255, 256, 299], dtype=np.int32)
+    q = synth.scaled(synth.randn_bf16((len(qpos), 32, 128), 22), factor)
+    W = 100 if kind == orc.LOCAL else 0
+    lay = orc.layer(kind, window=max(W, 1))
+    got = orc.attention(lay, k, v, qpos, q)
+    ref = brute_force(kind, W, kind == orc.LOCAL, k, v, qpos, q)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-11)
+    if factor == 1e-3:
+        # nearly uniform: within 1e-2 of the mean of V over the key set
+        for n, p in enumerate(qpos):
+            lo = max(0, p - W + 1) if kind == orc.LOCAL else 0
+            mean = f64(v[lo:p + 1]).mean(axis=0)  # [2][128]
+            for h in range(32):
+                assert np.abs(got[n, h] - mean[h // 16]).max() < 1e-2
+
+
+@pytest.mark.parametrize("kind", [orc.LOCAL, orc.GLOBAL])
+def test_sink_key_closed_form(kind):
+    # A sink key scoring far above every other key: the output is that key's
+    # value row up to (1 - P_sink) * max |v_j - v_sink|, with 1 - P_sink
+    # bounded by sum_j exp(s_j - s_sink) (scores from the numpy formulation).
+    T = 2600
+    k, v = rand_hist(T, 23)
+    sinks = [5, 2400]  # the later one scores ~22 above the earlier one
+    k = synth.plant_sinks(k.unsqueeze(0), sinks, values=[synth.SINK_K, 1.5 * synth.SINK_K])[0]
+    qpos = np.array([0, 4, 5, 6, 300, 2047, 2052, 2399, 2400, 2599], dtype=np.int32)
+    q = synth.sink_queries(synth.randn_bf16((len(qpos), 32, 128), 24))
+    W = 2048 if kind == orc.LOCAL else 0
+    lay = orc.layer(kind)
+    got = orc.attention(lay, k, v, qpos, q)
+    s = brute_scores(kind, W, kind == orc.LOCAL, k, qpos, q)
+    vd = f64(v)
+    checked = 0
+    for n, p in enumerate(qpos):
+        visible = [j for j in sinks if j <= p and (kind == orc.GLOBAL or j > p - W)]
+        if not visible:
+            continue
+        j = max(visible)  # the later sink also wins when both are visible
+        for h in range(32):
+            row = s[n, h]
+            margin = row[j] - np.max(np.delete(row, j))
+            assert margin > 20, (p, h, margin)
+            tail = np.exp(np.delete(row, j) - row[j]).sum()
+            bound = tail * np.abs(vd[:, h // 16] - vd[j, h // 16]).max() + 1e-12
+            assert np.abs(got[n, h] - vd[j, h // 16]).max() <= bound
+            checked += 1
+    assert checked >= 7 * 32
