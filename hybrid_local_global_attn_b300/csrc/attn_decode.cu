@@ -140,7 +140,9 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         int32_t cur_lp = -1, cur_row0 = 0, cur_outer = b * kHkv + g;
         for (int t = 0; t < ntiles; ++t) {
           const int st = t % NS;
-          if (t >= NS && !mbar_wait(bar_empty + 8 * st, ((t / NS) - 1) & 1, &abort_flag)) {
+          if (t == p.stall_tile) break;  // self-test: tiles from here on never arrive
+          if (t >= NS &&
+              !mbar_wait(bar_empty + 8 * st, ((t / NS) - 1) & 1, &abort_flag, p.wait_ns)) {
             abort_flag = 1;
             set_err(p.err, MG_DERR_TIMEOUT);
             break;
@@ -205,7 +207,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     for (int t = 0; t < ntiles; ++t) {
       const int st = t % NS;
       // ldmatrix / mma.sync are warp-collective: the whole warp goes on or stops
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * st, (t / NS) & 1, &abort_flag))) {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bar_full + 8 * st, (t / NS) & 1, &abort_flag, p.wait_ns))) {
         abort_flag = 1;
         set_err(p.err, MG_DERR_TIMEOUT);
         ok = false;

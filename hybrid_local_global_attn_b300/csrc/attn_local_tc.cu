@@ -15,13 +15,20 @@
 //    rows.  The 8 tokens x 16 heads form one M = 128 tcgen05 tile (row =
 //    16 * token + head), so a single Q.K^T (N = 128 or 144 keys) and a
 //    single P.V per CTA cover every token.
-//  * RoPE by slot, as in the single-token ring kernel: slot s holds position
-//    p - ((p - s) mod 2048), so <R(p) q, R(j) k> is <R(b) q, R(s) k> for
-//    s <= b and <R(b + 2048) q, R(s) k> for s > b (b = p mod 2048).  A block
-//    token k sits at slot (p0 + k) mod 2048 under the same rule.  Keys are
-//    rotated in shared memory (ring rows by angles computed before the
-//    dependency wait), each query twice into two A operands; the scores of
-//    both versions land in TMEM and the softmax picks per (row, key).
+//  * RoPE relative to the block start.  <R(p0 + i) q, R(j) k> =
+//    <R(i) q, R(j - p0) k>: token i's query is rotated by R(i), and each key
+//    by its offset from p0 -- a block token k by R(k), ring slot s (which
+//    holds position p0 - ((p0 - s) mod 2048)) by R(s - b) for s < b and
+//    R(s - b - 2048) for s > b (b = p0 mod 2048; slot b itself holds
+//    p0 - 2048, outside every token's window).  R(s) is computed before the
+//    dependency wait, R(-b) and R(-b - 2048) once p0 is known.
+//  * Precision: rotated queries and keys are kept as bf16 pairs hi =
+//    bf16(x), lo = bf16(x - hi), and S accumulates Qhi.Khi + Qhi.Klo +
+//    Qlo.Khi (24 MMAs of K = 16 into one TMEM accumulator): the scores carry
+//    the rounding of the rotated operands at about 2^-17 of |q||k| instead of
+//    2^-9, which keeps sharply peaked softmax rows (large |q|) within
+//    tolerance.  The query halves live in TMEM (the A operand), the key
+//    halves in shared memory.
 //  * Ring slots that the block's tokens up to i are about to overwrite hold
 //    positions outside token i's window and are masked, as are slots past
 //    the last written position.
@@ -46,20 +53,18 @@ constexpr int kTpc = kTcPosPerTile;            // 8 tokens = 128 rows per CTA
 constexpr int kThreads = 256;
 constexpr int kBoxBytes = kKeysMax * 128;      // one 64-dim box of 144 key rows
 constexpr int kKVSmem = 2 * kBoxBytes;         // dims 0-63 box, dims 64-127 box
-constexpr int kQBox = kTcRows * 128;           // 16 KB
-constexpr int kQSmem = 2 * kQBox;              // one rotated query version
-constexpr int kQAngSmem = kTpc * 2 * 64 * 8;   // [token][version][freq] (cos, sin)
+constexpr int kAngSmem = 2 * 64 * 8;           // R(-b), R(-b - 2048) per frequency
 constexpr int kRedSmem = 4 * kTcRows * 4;      // [half][m, l][row]
 // Inbox of the owning CTA: rows [source][token][128] fp32, then lse
 // [source][8 tokens].  One source's rows for one owner are contiguous, so they
 // travel as one bulk copy.
 constexpr int kInboxRows = kLocCluster * kTpc * kD * 4;  // 64 KB
 constexpr int kInboxLse = kLocCluster * kTpc * 4;        // 512 B
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kKVSmem;
-constexpr int kOffQ = kOffV + kKVSmem;         // version 0, then version 1; staging later
-constexpr int kOffQAng = kOffQ + 2 * kQSmem;
-constexpr int kOffRed = kOffQAng + kQAngSmem;
+constexpr int kOffK = 0;                       // rotated keys, hi parts
+constexpr int kOffKl = kOffK + kKVSmem;        // rotated keys, lo parts
+constexpr int kOffV = kOffKl + kKVSmem;
+constexpr int kOffAng = kOffV + kKVSmem;
+constexpr int kOffRed = kOffAng + kAngSmem;
 constexpr int kOffTurn = kOffRed + kRedSmem;   // 64 turns (uint64)
 constexpr int kOffW = kOffTurn + 64 * 8;       // merge weights [token][source]
 constexpr int kOffBars = kOffW + kTpc * kLocCluster * 4;
@@ -67,16 +72,15 @@ constexpr int kOffInbox = kOffBars + 64;
 constexpr int kSmem = kOffInbox + kInboxRows + kInboxLse + 1024;  // + alignment slack
 // Staging of this CTA's normalised rows, [owner][token][128] fp32 with the
 // owner blocks 16 bytes apart beyond their size (so that the 32 rows a warp
-// stores at once fall on different banks), and lse [owner][8]: over the
-// query buffers, free once P.V has run.
+// stores at once fall on different banks), and lse [owner][8]: over the key
+// buffers, free once Q.K^T has run.
 constexpr int kStageOwner = kTpc * kD * 4 + 16;
-constexpr int kOffStage = kOffQ;
-constexpr int kOffStageLse = kOffQ + kLocCluster * kStageOwner;
-static_assert(kLocCluster * kStageOwner + kInboxLse <= 2 * kQSmem + kQAngSmem,
-              "staging fits the query buffers");
-// TMEM columns: scores of the two query versions, then O.  P (bf16 pairs)
-// overwrites the first 72 columns of the first scores.
-constexpr uint32_t kColSlo = 0, kColShi = 160, kColO = 320;
+constexpr int kOffStage = kOffK;
+constexpr int kOffStageLse = kOffK + kLocCluster * kStageOwner;
+static_assert(kLocCluster * kStageOwner + kInboxLse <= 2 * kKVSmem, "staging fits the key buffers");
+// TMEM columns: scores (P as bf16 pairs overwrites their first 72 columns),
+// O, and the rotated queries' hi and lo halves (bf16 pairs, the A operand).
+constexpr uint32_t kColS = 0, kColO = 160, kColQh = 288, kColQl = 352;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -142,17 +146,30 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) {
   return r * 128u + ((c ^ (r & 7u)) << 4);
 }
-// rotate 8 (x, y) pairs held as bf16 in (lo, hi) by the angles a[0..7]
-__device__ __forceinline__ void rot8(uint4 &lo, uint4 &hi, const float2 *a) {
-  uint32_t *l = reinterpret_cast<uint32_t *>(&lo);
-  uint32_t *h = reinterpret_cast<uint32_t *>(&hi);
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+  return make_float2(a.x * b.x - a.y * b.y, a.y * b.x + a.x * b.y);
+}
+// Two fp32 values as bf16 pairs hi = bf16(v) and lo = bf16(v - hi).
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(a - bf16lo(hi), b - bf16hi(hi));
+}
+// Rotate 8 (x, y) pairs held as bf16 in (x8, y8) -- dims i..i+7 and their
+// partners i+64..i+71 -- by the angles a[0..7] in fp32, and split each
+// rotated value into bf16 hi and lo parts.
+__device__ __forceinline__ void rot8_split(uint4 x8, uint4 y8, const float2 *a, uint4 &xh,
+                                           uint4 &xl, uint4 &yh, uint4 &yl) {
+  const uint32_t *x = reinterpret_cast<const uint32_t *>(&x8);
+  const uint32_t *y = reinterpret_cast<const uint32_t *>(&y8);
+  uint32_t *oxh = reinterpret_cast<uint32_t *>(&xh), *oxl = reinterpret_cast<uint32_t *>(&xl);
+  uint32_t *oyh = reinterpret_cast<uint32_t *>(&yh), *oyl = reinterpret_cast<uint32_t *>(&yl);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float x0 = bf16lo(l[e]), x1 = bf16hi(l[e]);
-    const float y0 = bf16lo(h[e]), y1 = bf16hi(h[e]);
+    const float x0 = bf16lo(x[e]), x1 = bf16hi(x[e]);
+    const float y0 = bf16lo(y[e]), y1 = bf16hi(y[e]);
     const float2 a0 = a[2 * e], a1 = a[2 * e + 1];
-    l[e] = pack_bf16x2(x0 * a0.x - y0 * a0.y, x1 * a1.x - y1 * a1.y);
-    h[e] = pack_bf16x2(x0 * a0.y + y0 * a0.x, x1 * a1.y + y1 * a1.x);
+    split2(x0 * a0.x - y0 * a0.y, x1 * a1.x - y1 * a1.y, oxh[e], oxl[e]);
+    split2(x0 * a0.y + y0 * a0.x, x1 * a1.y + y1 * a1.x, oyh[e], oyl[e]);
   }
 }
 
@@ -167,8 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sK = sbase + kOffK, sV = sbase + kOffV, sQ = sbase + kOffQ;
-  float2 *qang = reinterpret_cast<float2 *>(smem + kOffQAng);
+  const uint32_t sK = sbase + kOffK, sKl = sbase + kOffKl, sV = sbase + kOffV;
+  float2 *ang = reinterpret_cast<float2 *>(smem + kOffAng);
   float *red = reinterpret_cast<float *>(smem + kOffRed);
   float *inbox = reinterpret_cast<float *>(smem + kOffInbox);
   uint64_t *turns = reinterpret_cast<uint64_t *>(smem + kOffTurn);
@@ -186,6 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t head = b * kHkv + g;
   const bool blk_here = my_rank == 0;  // the first CTA also scores the block rows
   const int nkeys = blk_here ? kKeysMax : kPiece;
+  // thread roles: row r (TMEM lane, also the query row it rotates), half hh
+  // of the keys (softmax) and of the query's dims (rotation)
+  const int r = 32 * (warp & 3) + lane, hh = warp >> 2;
+  const uint32_t lane_bits = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  const int rt = r >> 4;  // token of the row
 
   // ---- prologue: kernel parameters only (overlaps the previous kernel) ----
   if (tid == 0) {
@@ -211,11 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid < 64) turns[tid] = p.turn[tid];
   __syncthreads();
-  // slot angles of this thread's ring row (krow) at frequencies 32 kh .. 32 kh + 31
+  // slot angles R(s w_f) of this thread's ring row (krow) at frequencies
+  // 32 kh .. 32 kh + 31, and the query angles R(i w_f) of its query row's
+  // token i at frequencies 32 hh .. 32 hh + 31 (neither needs the position)
   const int krow = tid >> 1, kh = tid & 1;
-  float2 kang[32];
+  float2 kang[32], qang[32];
 #pragma unroll
-  for (int f = 0; f < 32; ++f) rope_cos_sin(s0 + krow, turns[32 * kh + f], kang[f].x, kang[f].y);
+  for (int f = 0; f < 32; ++f) {
+    rope_cos_sin(s0 + krow, turns[32 * kh + f], kang[f].x, kang[f].y);
+    rope_cos_sin(i0 + rt, turns[32 * hh + f], qang[f].x, qang[f].y);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -237,15 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sV + x * kBoxBytes, &tv, bar_v, 64 * x, s0, head);
     }
   }
-
-  // raw query of row qr (token qr / 16, head qr % 16), dims 32 kh.. and 64 + 32 kh..
-  const int qr = tid >> 1, qt = qr >> 4;
+  // raw query of row r, dims 32 hh.. and 64 + 32 hh..
   uint4 qx[4], qy[4];
   {
-    const bool live = qt < cnt;
+    const bool live = rt < cnt;
     const __nv_bfloat16 *src =
-        p.q + ((static_cast<size_t>(b) * p.n + i0 + (live ? qt : 0)) * kHq + g * kGroup + (qr & 15)) * kD +
-        32 * kh;
+        p.q + ((static_cast<size_t>(b) * p.n + i0 + (live ? rt : 0)) * kHq + g * kGroup + (r & 15)) * kD +
+        32 * hh;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       qx[c] = live ? __ldg(reinterpret_cast<const uint4 *>(src) + c) : make_uint4(0u, 0u, 0u, 0u);
@@ -253,8 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   // block rows 128..143 of K and V (first CTA): thread tid < 128 takes row
-  // tid / 8, 8-dim chunk tid % 8 (and its partner 64 dims on); K rotated by
-  // its slot's angle
+  // tid / 8, 8-dim chunk tid % 8 (and its partner 64 dims on)
   const int bk = tid >> 3, bc = tid & 7;
   uint4 kx = make_uint4(0u, 0u, 0u, 0u), ky = kx, vx = kx, vy = kx;
   if (blk_here && tid < 128 && bk < p.n) {
@@ -268,100 +292,98 @@ __global__ void __launch_bounds__(kThreads, 1)
   // now the position
   const bool bad = p0 < 0 || static_cast<int64_t>(p0) + p.n > p.max_len;
   if (bad && my_rank == 0 && g == 0 && i0 == 0 && tid == 0) set_err(p.err, MG_DERR_POSITION);
-  // query-version angles: entry (t, v, f) = R((b_t + 2048 v) w_f), b_t the slot of token t
-  for (int e = tid; e < kTpc * 2 * 64; e += kThreads) {
-    const int t = e >> 7, v = (e >> 6) & 1, f = e & 63;
-    float2 a = make_float2(1.f, 0.f);
-    if (t < cnt && !bad)
-      rope_cos_sin(((p0 + i0 + t) & (kWindow - 1)) + kWindow * v, turns[f], a.x, a.y);
-    qang[e] = a;
+  const int32_t b0 = p0 & (kWindow - 1);  // slot of the block start
+  if (tid < 128) {  // R(-b w_f) and R(-(b + 2048) w_f)
+    float cs, sn;
+    rope_cos_sin(-(b0 + kWindow * (tid >> 6)), turns[tid & 63], cs, sn);
+    ang[tid] = make_float2(cs, sn);
   }
-  // which query versions some valid (token, key) pair uses (CTA-uniform)
-  bool need_lo = false, need_hi = false;
-  if (!bad) {
-    for (int t = 0; t < cnt; ++t) {
-      const int32_t bt = (p0 + i0 + t) & (kWindow - 1);
-      need_lo = need_lo || s0 <= bt;
-      need_hi = need_hi || s0 + kPiece - 1 > bt;
+  // rotated query halves into TMEM: row r, dims 32 hh.. (columns 16 hh..)
+  // and 64 + 32 hh.. (columns 32 + 16 hh..)
+  {
+    uint32_t h0[16], l0[16], h1[16], l1[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 xh, xl, yh, yl;
+      rot8_split(qx[c], qy[c], qang + 8 * c, xh, xl, yh, yl);
+      h0[4 * c] = xh.x; h0[4 * c + 1] = xh.y; h0[4 * c + 2] = xh.z; h0[4 * c + 3] = xh.w;
+      l0[4 * c] = xl.x; l0[4 * c + 1] = xl.y; l0[4 * c + 2] = xl.z; l0[4 * c + 3] = xl.w;
+      h1[4 * c] = yh.x; h1[4 * c + 1] = yh.y; h1[4 * c + 2] = yh.z; h1[4 * c + 3] = yh.w;
+      l1[4 * c] = yl.x; l1[4 * c + 1] = yl.y; l1[4 * c + 2] = yl.z; l1[4 * c + 3] = yl.w;
     }
-    if (blk_here) need_lo = need_hi = true;  // block slots may fall on either side
+    tmem_st16(tbase + lane_bits + kColQh + 16 * hh, h0);
+    tmem_st16(tbase + lane_bits + kColQh + 32 + 16 * hh, h1);
+    tmem_st16(tbase + lane_bits + kColQl + 16 * hh, l0);
+    tmem_st16(tbase + lane_bits + kColQl + 32 + 16 * hh, l1);
   }
-
-  if (blk_here && tid < 128) {
+  if (blk_here && tid < 128) {  // block token k at offset k from p0: R(k)
     const int k = bk, c = bc;
-    if (bad) kx = ky = vx = vy = make_uint4(0u, 0u, 0u, 0u);
+    uint4 xh = make_uint4(0u, 0u, 0u, 0u), xl = xh, yh = xh, yl = xh;
     if (k < p.n && !bad) {
       float2 a[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        rope_cos_sin((p0 + k) & (kWindow - 1), turns[8 * c + e], a[e].x, a[e].y);
-      rot8(kx, ky, a);
+      for (int e = 0; e < 8; ++e) rope_cos_sin(k, turns[8 * c + e], a[e].x, a[e].y);
+      rot8_split(kx, ky, a, xh, xl, yh, yl);
+    } else {
+      vx = vy = xh;
     }
     const uint32_t o = swz(kPiece + k, c);
-    sts128(sK + o, kx);
-    sts128(sK + kBoxBytes + o, ky);
+    sts128(sK + o, xh);
+    sts128(sK + kBoxBytes + o, yh);
+    sts128(sKl + o, xl);
+    sts128(sKl + kBoxBytes + o, yl);
     sts128(sV + o, vx);
     sts128(sV + kBoxBytes + o, vy);
   }
-  __syncthreads();  // query angles ready
-
-  // rotated queries, version v at sQ + v * kQSmem (K-major, 128-byte swizzle)
+  __syncthreads();  // R(-b) tables ready
+  // this thread's ring row: R(d) = R(s) R(-b) (s < b) or R(s) R(-b - 2048)
+  {
+    const float2 *a = ang + ((s0 + krow > b0) ? 64 : 0) + 32 * kh;
 #pragma unroll
-  for (int v = 0; v < 2; ++v) {
-    if (v == 0 ? !need_lo : !need_hi) continue;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int cc = 4 * kh + c;  // 8-dim chunk
-      uint4 lo = qx[c], hi = qy[c];
-      rot8(lo, hi, qang + (qt < kTpc ? qt : 0) * 128 + v * 64 + 8 * cc);
-      const uint32_t o = sQ + v * kQSmem + swz(qr, cc);
-      sts128(o, lo);
-      sts128(o + kQBox, hi);
-    }
+    for (int f = 0; f < 32; ++f) kang[f] = cmul(kang[f], a[f]);
   }
-  // ring keys: once the tile has landed, rotate each row by its slot's angle
+  // ring keys: once the tile has landed, rotate each row and split it
   bool ok = mbar_wait(bar_k, 0, &abort_flag);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int cc = 4 * kh + c;
-    const uint32_t o = sK + swz(krow, cc);
-    uint4 lo = lds128(o), hi = lds128(o + kBoxBytes);
-    rot8(lo, hi, kang + 8 * c);
-    sts128(o, lo);
-    sts128(o + kBoxBytes, hi);
+    const uint32_t o = swz(krow, cc);
+    uint4 xh, xl, yh, yl;
+    rot8_split(lds128(sK + o), lds128(sK + kBoxBytes + o), kang + 8 * c, xh, xl, yh, yl);
+    sts128(sK + o, xh);
+    sts128(sK + kBoxBytes + o, yh);
+    sts128(sKl + o, xl);
+    sts128(sKl + kBoxBytes + o, yl);
   }
   fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+  tmem_wait_st();
   tc_fence_before();
   __syncthreads();
 
-  // ------------------------------------------------------------ S = Q K^T ----
+  // --------------------------------- S = Qh Kh^T + Qh Kl^T + Ql Kh^T ----
   if (tid == 0) {
     tc_fence_after();
     const uint32_t idq = idesc_bf16_f32(128, nkeys, 0, 0);
 #pragma unroll
-    for (int v = 0; v < 2; ++v) {
-      if (v == 0 ? !need_lo : !need_hi) continue;
+    for (int part = 0; part < 3; ++part) {
+      const uint32_t qa = tbase + (part == 2 ? kColQl : kColQh);
+      const uint32_t kb = part == 1 ? sKl : sK;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t oq = (kk >> 2) * kQBox + (kk & 3) * 32;
         const uint32_t ok_ = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-        mma_ss(tbase + (v == 0 ? kColSlo : kColShi), smem_desc_sw128(sQ + v * kQSmem + oq, 16, 1024),
-               smem_desc_sw128(sK + ok_, 16, 1024), idq, kk > 0 ? 1u : 0u);
+        mma_ts(tbase + kColS, qa + 8 * kk, smem_desc_sw128(kb + ok_, 16, 1024), idq,
+               (part > 0 || kk > 0) ? 1u : 0u);
       }
     }
     mma_commit(bar_s);
   }
 
   // -------------------------------------------------------------- softmax ----
-  // thread: row r (TMEM lane), half hh of the keys (0: keys 0..63; 1: keys
-  // 64..127 and the block keys 128..143)
-  const int r = 32 * (warp & 3) + lane, hh = warp >> 2;
-  const uint32_t lane_bits = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-  const int rt = r >> 4;                       // token of the row
+  // thread: row r, half hh of the keys (0: keys 0..63; 1: keys 64..127 and
+  // the block keys 128..143)
   const bool row_live = rt < cnt && !bad;
   const int32_t ri = i0 + rt;                  // token index in the block
   const int32_t rp = p0 + ri;                  // its position
-  const int32_t rb = rp & (kWindow - 1);       // its slot
   const int32_t rn = min(rp + 1, kWindow);     // slots holding positions
   ok = __all_sync(0xffffffffu, mbar_wait(bar_s, 0, &abort_flag) && ok);
   tc_fence_after();
@@ -371,33 +393,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int c = 0; c < 2; ++c) {  // ring keys 64 hh + 32 c ..
     const int j0 = 64 * hh + 32 * c;
-    uint32_t lo[32], hi[32];
-    tmem_ld32(tbase + lane_bits + kColSlo + j0, lo);
-    tmem_ld32(tbase + lane_bits + kColShi + j0, hi);
+    uint32_t sc[32];
+    tmem_ld32(tbase + lane_bits + kColS + j0, sc);
     tmem_wait_ld();
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int32_t s = s0 + j0 + j;
       const bool stale = ((s - p0) & (kWindow - 1)) <= ri;  // a block token takes this slot
       const bool valid = row_live && s < rn && !stale;
-      const float x = __uint_as_float(s <= rb ? lo[j] : hi[j]) * sl2;
-      sv[32 * c + j] = valid ? x : -INFINITY;
+      sv[32 * c + j] = valid ? __uint_as_float(sc[j]) * sl2 : -INFINITY;
       mx = fmaxf(mx, sv[32 * c + j]);
     }
   }
   if (hh == 1) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) sv[64 + j] = -INFINITY;
-    if (blk_here) {  // block keys k = 0..15 at slots (p0 + k) mod 2048
-      uint32_t lo[16], hi[16];
-      tmem_ld16(tbase + lane_bits + kColSlo + kPiece, lo);
-      tmem_ld16(tbase + lane_bits + kColShi + kPiece, hi);
+    if (blk_here) {  // block keys k = 0..15
+      uint32_t sc[16];
+      tmem_ld16(tbase + lane_bits + kColS + kPiece, sc);
       tmem_wait_ld();
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const int32_t sk = (p0 + k) & (kWindow - 1);
-        const float x = __uint_as_float(sk <= rb ? lo[k] : hi[k]) * sl2;
-        sv[64 + k] = (row_live && k <= ri) ? x : -INFINITY;
+        sv[64 + k] = (row_live && k <= ri) ? __uint_as_float(sc[k]) * sl2 : -INFINITY;
         mx = fmaxf(mx, sv[64 + k]);
       }
     }
@@ -416,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       l += e0 + e1;
       pk[j >> 1] = pack_bf16x2(e0, e1);
     }
-    tmem_st16(tbase + lane_bits + kColSlo + 32 * hh + 16 * c, pk);
+    tmem_st16(tbase + lane_bits + kColS + 32 * hh + 16 * c, pk);
   }
   if (hh == 1 && blk_here) {  // block keys: columns 64..71
     uint32_t pk[8];
@@ -426,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       l += e0 + e1;
       pk[k >> 1] = pack_bf16x2(e0, e1);
     }
-    tmem_st8(tbase + lane_bits + kColSlo + kPiece / 2, pk);
+    tmem_st8(tbase + lane_bits + kColS + kPiece / 2, pk);
   }
   red[(2 * hh + 1) * kTcRows + r] = l;
   tmem_wait_st();
@@ -440,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
     for (int kk = 0; kk < nkeys / 16; ++kk)
-      mma_ts(tbase + kColO, tbase + kColSlo + 8 * kk,
+      mma_ts(tbase + kColO, tbase + kColS + 8 * kk,
              smem_desc_sw128(sV + kk * 2048, kBoxBytes, 1024), idv, kk > 0 ? 1u : 0u);
     mma_commit(bar_o);
   }
@@ -449,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   // ---------------- send this CTA's normalised rows to the owning CTAs ----
-  // Stage [owner = head][token][128] and lse [owner][8] over the query
+  // Stage [owner = head][token][128] and lse [owner][8] over the key
   // buffers (every MMA has retired), then one bulk copy per owner.
   const bool have = ok && row_live && L > 0.f;
   const float inv = have ? 1.f / L : 0.f;

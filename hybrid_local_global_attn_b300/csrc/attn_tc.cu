@@ -38,6 +38,17 @@
 // O += P V (V as an MN-major operand).
 // Splits (verify): the cache part is cut across CTAs; each writes (o/l, lse)
 // and the combine kernel merges them.
+//
+// Local layers (operands staged by rope_stage, rotated by their absolute
+// positions) run the precise form of the kernel: queries and keys arrive as
+// bf16 pairs hi = bf16(x), lo = bf16(x - hi) of the fp32 rotation, and
+// S = Qhi Khi^T + Qlo Khi^T + Qhi Klo^T (24 MMAs per key tile instead of 8)
+// carries the rounding of the rotated operands at about 2^-17 of |q||k|
+// instead of 2^-9 -- one bf16 rounding moves a score by ~0.04 when scaled
+// scores spread by ~40, enough to shift a peaked softmax row by several
+// 1e-2.  Shared memory then holds Qhi and Qlo (64 KB), one key tile's hi and
+// lo halves (64 KB each, each released as soon as its MMAs have run) and V
+// in a 2-deep ring of 64-key quarter tiles.
 #include "mg_internal.h"
 #include "mg_ptx.cuh"
 
@@ -46,6 +57,17 @@ namespace mg {
 namespace {
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kTcKeys, 0, 0);
+// Shared-memory plan per form: Q bytes (hi, then lo in the precise form) and
+// the V stage (128-key halves, or 64-key quarters in the precise form); the
+// two 64 KB key buffers are K stages (plain) or a tile's hi and lo (precise).
+template <bool kPrecise> struct TcPlan {
+  static constexpr int kQ = kPrecise ? 2 * kTcQBytes : kTcQBytes;
+  static constexpr int kVRows = kPrecise ? kTcKeys / 4 : kTcVRows;  // keys per V stage
+  static constexpr int kVParts = kTcKeys / kVRows;                    // V stages per key tile
+  static constexpr int kVBytes = kVRows * kRowBytes;
+  static constexpr int kSmem = kQ + 2 * kTcKTileBytes + kTcVStages * kVBytes + 1024 + 256;
+};
+static_assert(TcPlan<true>::kSmem <= kTcSmem && TcPlan<false>::kSmem <= kTcSmem, "shared memory");
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -63,11 +85,15 @@ __device__ __forceinline__ int32_t tile_kp0(const TileInfo &ti, int t) {
 
 }  // namespace
 
+template <bool kPrecise>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tq,
                    const __grid_constant__ CUtensorMap tka, const __grid_constant__ CUtensorMap tva,
                    const __grid_constant__ CUtensorMap tkb,
-                   const __grid_constant__ CUtensorMap tvb) {
+                   const __grid_constant__ CUtensorMap tvb,
+                   const __grid_constant__ CUtensorMap tql,
+                   const __grid_constant__ CUtensorMap tkl) {
+  using Plan = TcPlan<kPrecise>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_base_slot;
@@ -75,16 +101,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase;                              // 32 KB
-  const uint32_t sK = sbase + kTcQBytes;                  // K ring: stage s at +64K*s
-  const uint32_t sV = sK + kTcKStages * kTcKTileBytes;    // V ring of half tiles: +32K*s
-  const uint32_t sBar = sV + kTcVStages * kTcVTileBytes;
+  const uint32_t sQ = sbase;                              // Q (precise: hi, then lo)
+  const uint32_t sK = sbase + Plan::kQ;                   // two 64 KB key buffers
+  const uint32_t sV = sK + 2 * kTcKTileBytes;             // V ring: stage s at +kVBytes*s
+  const uint32_t sBar = sV + kTcVStages * Plan::kVBytes;
   // barrier addresses
   const uint32_t bar_q = sBar;                             // Q landed
-  const uint32_t bar_kf = sBar + 8;                        // [kTcKStages] K full
-  const uint32_t bar_ke = bar_kf + 8 * kTcKStages;         // [kTcKStages] K stage free
-  const uint32_t bar_vf = bar_ke + 8 * kTcKStages;         // [kTcVStages] V half full
-  const uint32_t bar_ve = bar_vf + 8 * kTcVStages;         // [kTcVStages] V half free
+  const uint32_t bar_kf = sBar + 8;                        // [2] key buffer full
+  const uint32_t bar_ke = bar_kf + 8 * kTcKStages;         // [2] key buffer free
+  const uint32_t bar_vf = bar_ke + 8 * kTcKStages;         // [kTcVStages] V stage full
+  const uint32_t bar_ve = bar_vf + 8 * kTcVStages;         // [kTcVStages] V stage free
   const uint32_t bar_s = bar_ve + 8 * kTcVStages;          // S ready
   const uint32_t bar_sfree = bar_s + 8;                    // S loaded by the softmax (256)
   const uint32_t bar_p = bar_sfree + 8;                    // P ready (256 arrivals)
@@ -140,9 +166,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     crow0[t & 1] = kp0 - r;
     couter[t & 1] = o;
   };
-  // keys kp0.. (rows) of K or V into dst (two 64-dim boxes), completing on fb
-  auto load = [&](bool is_v, int t, int32_t kp0, uint32_t dst, uint32_t bytes, uint32_t fb) {
-    const CUtensorMap *ma = is_v ? &tva : &tka;
+  // keys kp0.. (rows) of K or V into dst (two 64-dim boxes), completing on
+  // fb; `lo`: the lo halves of staged keys (precise form)
+  auto load = [&](bool is_v, int t, int32_t kp0, uint32_t dst, uint32_t bytes, uint32_t fb,
+                  bool lo = false) {
+    const CUtensorMap *ma = is_v ? &tva : (lo ? &tkl : &tka);
     const CUtensorMap *mb = is_v ? &tvb : &tkb;
     mbar_arrive_expect_tx(fb, bytes);
     for (int x = 0; x < 2; ++x) {
@@ -156,9 +184,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   };
   int issued_k = 0, issued_v = 0;
+  int issued_part[2] = {0, 0};  // precise form: copies issued into each key buffer
   bool ok = true;
-  // K of tile t reuses the stage of tile t - 2 once its S = Q K^T has run
+  // Plain form: K of tile t reuses the stage of tile t - 2 once its
+  // S = Q K^T has run.  Precise form: the hi and lo halves of tile t go to
+  // buffers 0 and 1, each once the MMAs of tile t - 1 that read it have run.
   auto load_k = [&](int t) -> bool {
+    if (kPrecise) {
+      for (int part = 0; part < 2; ++part) {
+        if (t >= 1 && !mbar_wait(bar_ke + 8 * part, (t - 1) & 1, &abort_flag)) return false;
+        load(false, t, tile_kp0(ti, t), sK + part * kTcKTileBytes, kTcKTileBytes,
+             bar_kf + 8 * part, part == 1);
+        ++issued_part[part];
+      }
+      ++issued_k;
+      return true;
+    }
     const int ks = t % kTcKStages;
     if (t >= kTcKStages &&
         !mbar_wait(bar_ke + 8 * ks, ((t / kTcKStages) - 1) & 1, &abort_flag))
@@ -196,12 +237,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tkb);
       tma_prefetch_desc(&tvb);
       const int32_t q_t0 = kTcPosPerCta * qb;  // position index within the block
-      mbar_arrive_expect_tx(bar_q, kTcQBytes);
-      for (int x = 0; x < 2; ++x)
+      mbar_arrive_expect_tx(bar_q, Plan::kQ);
+      for (int x = 0; x < 2; ++x) {
         tma_load_4d(sQ + x * (kTcQBytes / 2), &tq, bar_q, 64 * x, kGroup * g, q_t0, b);
-      (void)load_k(0);  // stage 0: no wait
-      for (int h = 0; h < 2; ++h) {  // V halves 0 and 1: stages 0 and 1, no wait
-        load(true, 0, tile_kp0(ti, 0) + kTcVRows * h, sV + h * kTcVTileBytes, kTcVTileBytes,
+        if (kPrecise)
+          tma_load_4d(sQ + kTcQBytes + x * (kTcQBytes / 2), &tql, bar_q, 64 * x, kGroup * g,
+                      q_t0, b);
+      }
+      (void)load_k(0);  // first use of the key buffers: no wait
+      for (int h = 0; h < kTcVStages; ++h) {  // V stages 0 and 1 of tile 0: no wait
+        load(true, 0, tile_kp0(ti, 0) + Plan::kVRows * h, sV + h * Plan::kVBytes, Plan::kVBytes,
              bar_vf + 8 * h);
         ++issued_v;
       }
@@ -220,21 +265,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------- producer ----
     if (lane == 0 && ntiles > 0) {
-      // K(0), V(0) went out before the CTA barrier
+      // K(0) and the first V stages of tile 0 went out before the CTA barrier
       for (int t = 0; ok && t < ntiles; ++t) {
         if (t + 1 < ntiles && !load_k(t + 1)) {
           ok = false;
           break;
         }
-        for (int h = 0; h < 2 && t > 0; ++h) {
-          const int u = 2 * t + h, vs = u % kTcVStages;
-          if (u >= kTcVStages &&
-              !mbar_wait(bar_ve + 8 * vs, ((u / kTcVStages) - 1) & 1, &abort_flag)) {
+        for (int h = 0; h < Plan::kVParts; ++h) {
+          const int u = Plan::kVParts * t + h, vs = u % kTcVStages;
+          if (u < kTcVStages) continue;  // issued already
+          if (!mbar_wait(bar_ve + 8 * vs, ((u / kTcVStages) - 1) & 1, &abort_flag)) {
             ok = false;
             break;
           }
-          load(true, t, tile_kp0(ti, t) + kTcVRows * h, sV + vs * kTcVTileBytes, kTcVTileBytes,
-               bar_vf + 8 * vs);
+          load(true, t, tile_kp0(ti, t) + Plan::kVRows * h, sV + vs * Plan::kVBytes,
+               Plan::kVBytes, bar_vf + 8 * vs);
           ++issued_v;
         }
       }
@@ -244,8 +289,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // no copies may be in flight when the CTA retires
       (void)mbar_wait(bar_q, 0, nullptr);
-      for (int t = max(0, issued_k - kTcKStages); t < issued_k; ++t)
-        (void)mbar_wait(bar_kf + 8 * (t % kTcKStages), (t / kTcKStages) & 1, nullptr);
+      if (kPrecise) {
+        for (int part = 0; part < 2; ++part)
+          if (issued_part[part] > 0)
+            (void)mbar_wait(bar_kf + 8 * part, (issued_part[part] - 1) & 1, nullptr);
+      } else {
+        for (int t = max(0, issued_k - kTcKStages); t < issued_k; ++t)
+          (void)mbar_wait(bar_kf + 8 * (t % kTcKStages), (t / kTcKStages) & 1, nullptr);
+      }
       for (int u = max(0, issued_v - kTcVStages); u < issued_v; ++u)
         (void)mbar_wait(bar_vf + 8 * (u % kTcVStages), (u / kTcVStages) & 1, nullptr);
     }
@@ -269,34 +320,82 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mma_commit(bar_ke + 8 * st);
         return true;
       };
-      // O += P(t) V(t): two V half tiles of 8 k-steps each
-      auto pv = [&](int t) -> bool {
-        if (!mbar_wait(bar_p, t & 1, &abort_flag)) return false;
-        for (int h = 0; h < 2; ++h) {
-          const int u = 2 * t + h, vs = u % kTcVStages;
+      // Precise form, S(t) in two steps: Qhi.Khi + Qlo.Khi, then release the
+      // Khi buffer; Qhi.Klo, then S is complete and the Klo buffer free.
+      auto qk_hi = [&](int t) -> bool {
+        if (!mbar_wait(bar_kf, t & 1, &abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t qs = sQ + part * kTcQBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tbase, smem_desc_sw128(qs + (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32, 16, 1024),
+                   smem_desc_sw128(sK + (kk >> 2) * (kTcKTileBytes / 2) + (kk & 3) * 32, 16, 1024),
+                   kIdescQK, (part > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar_ke);
+        return true;
+      };
+      auto qk_lo = [&](int t) -> bool {
+        if (!mbar_wait(bar_kf + 8, t & 1, &abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t kl = sK + kTcKTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tbase, smem_desc_sw128(sQ + (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32, 16, 1024),
+                 smem_desc_sw128(kl + (kk >> 2) * (kTcKTileBytes / 2) + (kk & 3) * 32, 16, 1024),
+                 kIdescQK, 1u);
+        mma_commit(bar_s);
+        mma_commit(bar_ke + 8);
+        return true;
+      };
+      // O += P(t) V(t) over V stages [h0, h1) of the tile (halves of 8
+      // k-steps, or quarters of 4); P(t) must be in TMEM
+      auto pv_parts = [&](int t, int h0, int h1) -> bool {
+        constexpr int kSteps = Plan::kVRows / 16;
+        for (int h = h0; h < h1; ++h) {
+          const int u = Plan::kVParts * t + h, vs = u % kTcVStages;
           if (!mbar_wait(bar_vf + 8 * vs, (u / kTcVStages) & 1, &abort_flag)) return false;
           tc_fence_after();
-          const uint32_t v0 = sV + vs * kTcVTileBytes;
+          const uint32_t v0 = sV + vs * Plan::kVBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            mma_ts(tbase + kColO, tbase + kColP + 64 * h + 8 * kk,
-                   smem_desc_sw128(v0 + kk * 2048, kTcVTileBytes / 2, 1024), kIdescPV,
+          for (int kk = 0; kk < kSteps; ++kk) {
+            mma_ts(tbase + kColO, tbase + kColP + (Plan::kVRows / 2) * h + 8 * kk,
+                   smem_desc_sw128(v0 + kk * 2048, Plan::kVBytes / 2, 1024), kIdescPV,
                    (t == 0 && h == 0 && kk == 0) ? 0u : 1u);
           }
           mma_commit(bar_ve + 8 * vs);
         }
+        return true;
+      };
+      auto pv = [&](int t) -> bool {
+        if (!mbar_wait(bar_p, t & 1, &abort_flag) || !pv_parts(t, 0, Plan::kVParts)) return false;
         mma_commit(bar_pfree);
         return true;
       };
       // Issue order: S(0); then for each t: S(t+1) (once the softmax has
       // loaded S(t)) and P.V(t) (once P(t) is in TMEM).
-      ok = ok && qk(0);
-      for (int t = 0; ok && t < ntiles; ++t) {
-        if (t + 1 < ntiles) {
-          ok = mbar_wait(bar_sfree, t & 1, &abort_flag) && qk(t + 1);
-          if (!ok) break;
+      if (kPrecise) {
+        // S(t+1) is split around the first half of P.V(t), so that the V
+        // quarters the second half needs can land while Qhi.Klo(t+1) runs
+        ok = ok && qk_hi(0) && qk_lo(0);
+        for (int t = 0; ok && t < ntiles; ++t) {
+          const bool next = t + 1 < ntiles;
+          ok = (!next || (mbar_wait(bar_sfree, t & 1, &abort_flag) && qk_hi(t + 1))) &&
+               mbar_wait(bar_p, t & 1, &abort_flag) && pv_parts(t, 0, Plan::kVParts / 2) &&
+               (!next || qk_lo(t + 1)) && pv_parts(t, Plan::kVParts / 2, Plan::kVParts);
+          if (ok) mma_commit(bar_pfree);
         }
-        ok = pv(t);
+      } else {
+        ok = ok && qk(0);
+        for (int t = 0; ok && t < ntiles; ++t) {
+          if (t + 1 < ntiles) {
+            ok = mbar_wait(bar_sfree, t & 1, &abort_flag) && qk(t + 1);
+            if (!ok) break;
+          }
+          ok = pv(t);
+        }
       }
       if (!ok) {
         abort_flag = 1;
@@ -393,8 +492,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float x0, x1;
           f32x2_split(x2, x0, x1);
           const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-          ls2[(j >> 1) & 3] = add_f32x2(ls2[(j >> 1) & 3], f32x2(e0, e1));
-          pk[c][j >> 1] = pack_bf16x2(e0, e1);
+          // the row sum adds the bf16 values P.V multiplies, so that the
+          // normalisation matches them: with the running max held up to
+          // 2^8 below the true one, the largest P is not 1 and its rounding
+          // would otherwise scale a peaked row's output by up to 2^-9
+          const uint32_t pr = pack_bf16x2(e0, e1);
+          pk[c][j >> 1] = pr;
+          ls2[(j >> 1) & 3] = add_f32x2(ls2[(j >> 1) & 3], f32x2(bf16lo(pr), bf16hi(pr)));
         }
       }
       {
@@ -494,11 +598,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 cudaError_t launch_attn_tc(const TcParams &p, const CUtensorMap &tq, const CUtensorMap &tka,
                            const CUtensorMap &tva, const CUtensorMap &tkb, const CUtensorMap &tvb,
-                           cudaStream_t s) {
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(attn_tc_kernel), kTcSmem, 1);
-  if (e != cudaSuccess) return e;
+                           const CUtensorMap &tql, const CUtensorMap &tkl, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(p.qblocks * p.splits), kHkv, static_cast<unsigned>(p.batch));
-  return launch_pdl(attn_tc_kernel, grid, dim3(kTcThreads), kTcSmem, s, p, tq, tka, tva, tkb, tvb);
+  if (p.staged) {
+    cudaError_t e =
+        ensure_smem_attr(reinterpret_cast<const void *>(attn_tc_kernel<true>), kTcSmem, 5);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_tc_kernel<true>, grid, dim3(kTcThreads), kTcSmem, s, p, tq, tka, tva,
+                      tkb, tvb, tql, tkl);
+  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(attn_tc_kernel<false>), kTcSmem, 1);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_tc_kernel<false>, grid, dim3(kTcThreads), kTcSmem, s, p, tq, tka, tva, tkb,
+                    tvb, tql, tkl);
 }
 
 }  // namespace mg

@@ -17,8 +17,9 @@
 // next starts elsewhere) use the same memory and race.
 //
 // The first call on each device looks up the array's device address with
-// cudaGetSymbolAddress (with that device current) and remembers it; make
-// that first call before any stream capture begins.
+// cudaGetSymbolAddress (with that device current) and remembers it, with the
+// context it belongs to; make that first call before any stream capture
+// begins, and again the first call after a device reset.
 #include <mutex>
 
 #include "mg_internal.h"
@@ -33,20 +34,54 @@ constexpr size_t kNoAllocScratchBytes = MG_NOALLOC_SCRATCH_BYTES;
 __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[64] = {};
 
-// Device address of the scratch array on the current device (set up once
-// per device).  Returns nullptr on failure.
+// The address is remembered together with the context it was looked up in:
+// after a device reset the runtime creates a new primary context, loads the
+// library's module again and the array gets a new address, so a change of
+// context means looking it up again.
+struct ScratchSlot {
+  CUcontext ctx;
+  void *ptr;
+};
+ScratchSlot g_scratch[64] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+  });
+  return fn;
+}
+
+// Device address of the scratch array on the current device, looked up the
+// first time a device (or a new context of it) is seen.  Returns nullptr on
+// failure.
 void *scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  const CtxGetCurrentFn get_ctx = ctx_get_current();
+  if (get_ctx == nullptr) return nullptr;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return nullptr;
+  ScratchSlot &slot = g_scratch[dev];
+  if (ctx == nullptr || ctx != slot.ctx || slot.ptr == nullptr) {
+    // (the lookup also creates the device's primary context if there is none yet)
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    g_scratch_ptr[dev] = p;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return nullptr;
+    slot.ctx = ctx;
+    slot.ptr = p;
   }
-  return g_scratch_ptr[dev];
+  return slot.ptr;
 }
 
 }  // namespace

@@ -268,7 +268,7 @@ int splits_verify(int32_t kind, int32_t batch, int32_t n, int32_t max_len) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t part_o, part_lse, qs, ks, vs, total;
+  size_t part_o, part_lse, qs, qs_lo, ks, ks_lo, vs, total;
   int splits, R;
 };
 
@@ -309,11 +309,15 @@ bool ws_layout(int32_t op, const mg_layer *L, int32_t batch, int32_t n, int32_t 
       w->part_lse = off;
       off = align256(off + rows * w->splits * sizeof(float));
     }
-    if (local) {
+    if (local) {  // staged operands: rotated q and k as bf16 hi and lo halves, and v
       w->R = kWindow + n;
       w->qs = off;
       off = align256(off + static_cast<size_t>(batch) * n * kHq * kD * 2);
+      w->qs_lo = off;
+      off = align256(off + static_cast<size_t>(batch) * n * kHq * kD * 2);
       w->ks = off;
+      off = align256(off + static_cast<size_t>(batch) * kHkv * w->R * kD * 2);
+      w->ks_lo = off;
       off = align256(off + static_cast<size_t>(batch) * kHkv * w->R * kD * 2);
       w->vs = off;
       off = align256(off + static_cast<size_t>(batch) * kHkv * w->R * kD * 2);
@@ -519,7 +523,8 @@ int mg_kv_commit_layers(int32_t n_layers, const mg_layer *layers, const mg_cache
 
 static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
                        int32_t max_len, const void *q, const void *k_new, const void *v_new,
-                       void *o, void *ws, size_t ws_bytes, uint32_t *d_err, void *stream) {
+                       void *o, void *ws, size_t ws_bytes, uint32_t *d_err, void *stream,
+                       uint64_t wait_ns = kWaitLimitNs, int32_t stall_tile = -1) {
   int st = check_layer(layer);
   if (st != MG_OK) return st;
   if ((st = check_cache(layer, cache)) != MG_OK) return st;
@@ -576,6 +581,8 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
     p.k_scale[g] = e4m3 ? cache->k_scale[g] : 1.0f;
     p.v_scale[g] = e4m3 ? cache->v_scale[g] : 1.0f;
   }
+  p.wait_ns = wait_ns;
+  p.stall_tile = stall_tile;
   cudaError_t e = e4m3 ? launch_decode_e4m3(p, tk, tv, s) : launch_decode(p, tk, tv, s);
   if (e != cudaSuccess) return MG_ERR_CUDA;
   if (!split) return MG_OK;
@@ -593,6 +600,16 @@ int mg_attn_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *
                    uint32_t *d_err, void *stream) {
   return decode_impl(layer, cache, d_pos, max_len, q, nullptr, nullptr, o, ws, ws_bytes, d_err,
                      stream);
+}
+
+int mg_debug_decode_stall(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
+                          int32_t max_len, const void *q, void *o, void *ws, size_t ws_bytes,
+                          uint32_t *d_err, void *stream, uint64_t wait_ns, int32_t stall_tile) {
+  if (layer == nullptr || cache == nullptr) return MG_ERR_INVALID;
+  if (layer->kind != MG_GLOBAL || cache->dtype != MG_BF16) return MG_ERR_UNSUPPORTED;
+  if (stall_tile < 0 || wait_ns == 0 || wait_ns > kWaitLimitNs) return MG_ERR_INVALID;
+  return decode_impl(layer, cache, d_pos, max_len, q, nullptr, nullptr, o, ws, ws_bytes, d_err,
+                     stream, wait_ns, stall_tile);
 }
 
 int mg_append_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
@@ -647,7 +664,7 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
                                       d_err, tk, tv, s));
   }
   const void *qsrc = q;
-  CUtensorMap tq, tka, tva, tkb, tvb;
+  CUtensorMap tq, tka, tva, tkb, tvb, tql, tkl;
   if (local) {
     StageParams sp;
     sp.pos0 = d_pos0;
@@ -657,7 +674,9 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
     sp.k_cache = static_cast<const __nv_bfloat16 *>(cache->k);
     sp.v_cache = static_cast<const __nv_bfloat16 *>(cache->v);
     sp.qs = at<__nv_bfloat16>(ws, w.qs);
+    sp.qs_lo = at<__nv_bfloat16>(ws, w.qs_lo);
     sp.ks = at<__nv_bfloat16>(ws, w.ks);
+    sp.ks_lo = at<__nv_bfloat16>(ws, w.ks_lo);
     sp.vs = at<__nv_bfloat16>(ws, w.vs);
     sp.err = d_err;
     sp.batch = B;
@@ -667,7 +686,9 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
     sp.rope = rope_turns(layer->rope_theta);
     if (launch_rope_stage(sp, s) != cudaSuccess) return MG_ERR_CUDA;
     qsrc = sp.qs;
-    if (!map_rows(&tka, sp.ks, w.R, outer, kTcKeys) || !map_rows(&tva, sp.vs, w.R, outer, kTcVRows))
+    // the precise form streams V in 64-key quarter tiles
+    if (!map_rows(&tka, sp.ks, w.R, outer, kTcKeys) || !map_rows(&tkl, sp.ks_lo, w.R, outer, kTcKeys) ||
+        !map_rows(&tva, sp.vs, w.R, outer, kTcKeys / 4))
       return MG_ERR_CUDA;
     tkb = tka;
     tvb = tva;
@@ -686,6 +707,12 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
                               static_cast<uint64_t>(B)};
     const uint32_t box[4] = {64, kGroup, kTcPosPerTile, 1};
     if (!make_map(&tq, qsrc, 4, dims, box)) return MG_ERR_CUDA;
+    if (!local) {
+      tql = tq;
+      tkl = tka;
+    } else if (!make_map(&tql, at<__nv_bfloat16>(ws, w.qs_lo), 4, dims, box)) {
+      return MG_ERR_CUDA;
+    }
   }
   TcParams p;
   p.pos0 = d_pos0;
@@ -704,7 +731,7 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
   p.slots = cache->slots;
   p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
   p.map = cache_map(cache);
-  if (launch_attn_tc(p, tq, tka, tva, tkb, tvb, s) != cudaSuccess) return MG_ERR_CUDA;
+  if (launch_attn_tc(p, tq, tka, tva, tkb, tvb, tql, tkl, s) != cudaSuccess) return MG_ERR_CUDA;
   if (w.splits > 1) {
     CombineParams c;
     c.part_o = p.part_o;

@@ -45,7 +45,6 @@ constexpr int kE4m3PrefetchTiles = 8;
 // per (sequence, KV head, group of query tokens), 128 ring slots per CTA.
 constexpr int kLocCluster = 16;
 constexpr int kMaxLocalTokens = 16;
-constexpr int kLocMaxTpc = 6;  // query tokens one CTA takes in turn
 
 // tcgen05 attention (verify + prefill): one query tile of 128 rows
 // (8 positions x 16 heads) per CTA, key tiles of 256 (S = Q K^T as
@@ -152,6 +151,12 @@ struct DecodeParams {  // global layers
   float scale_log2;        // softmax scale * log2(e)
   CacheMap map;            // linear or paged rows of the cache
   float k_scale[2], v_scale[2];  // MG_E4M3 caches: per KV head (powers of two)
+  // Failure-detection self-test (bf16 kernel only): limit of the pipeline
+  // waits (kWaitLimitNs normally), and the key tile at which the producer
+  // stops issuing copies (-1: never), so that the consumers' wait for it runs
+  // out.
+  uint64_t wait_ns;
+  int32_t stall_tile;
 };
 
 
@@ -166,7 +171,6 @@ struct LocalParams {  // local layers, n <= kMaxLocalTokens query tokens
   __nv_bfloat16 *o;                  // [B][n][32][128]
   uint32_t *err;
   int32_t batch, n, max_len;
-  int32_t tpc;         // query tokens per CTA (1..kLocMaxTpc)
   int32_t write_new;   // 1: also store the block rows into the ring (fused append, n == 1)
   float scale_log2;
   uint64_t turn[64];   // as in RopeTurns
@@ -185,8 +189,8 @@ struct StageParams {
   const __nv_bfloat16 *q;                 // [B][n][32][128]
   const __nv_bfloat16 *k_new, *v_new;     // [B][n][2][128]
   const __nv_bfloat16 *k_cache, *v_cache; // ring [B][2][2048][128]
-  __nv_bfloat16 *qs;                      // [B][n][32][128]  rotated q
-  __nv_bfloat16 *ks, *vs;                 // [B][2][R][128]  rows = pos - c0 + 2048
+  __nv_bfloat16 *qs, *qs_lo;              // [B][n][32][128]  rotated q (hi, lo)
+  __nv_bfloat16 *ks, *ks_lo, *vs;         // [B][2][R][128]  rows = pos - c0 + 2048
   uint32_t *err;
   int32_t batch, n, R, max_len;
   RopeTurns rope;
@@ -238,7 +242,7 @@ cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &tk, const CU
 // FP8 cache: tk over K codes (128-byte rows), tv over transposed V tiles
 cudaError_t launch_decode_e4m3(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                cudaStream_t s);
-// single-token ring kernel (picks p.tpc itself) and the tcgen05 ring kernel
+// single-token ring kernel and the tcgen05 ring kernel
 // for draft blocks (8 tokens per CTA)
 cudaError_t launch_local_tc(const LocalParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                             cudaStream_t s);
@@ -246,8 +250,10 @@ cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtens
                               cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 cudaError_t launch_rope_stage(const StageParams &p, cudaStream_t s);
+// (tql, tkl: the lo halves of staged queries and keys, read by the precise
+// form that local layers run)
 cudaError_t launch_attn_tc(const TcParams &p, const CUtensorMap &tq, const CUtensorMap &tka,
                            const CUtensorMap &tva, const CUtensorMap &tkb, const CUtensorMap &tvb,
-                           cudaStream_t s);
+                           const CUtensorMap &tql, const CUtensorMap &tkl, cudaStream_t s);
 
 }  // namespace mg

@@ -92,18 +92,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after kWaitLimitNs of
-// wall time or as soon as *abort becomes nonzero.  Returns false when it gave
-// up; the caller then records MG_DERR_TIMEOUT and winds down.
+// Wait for phase `parity` of an mbarrier, giving up after limit_ns of wall
+// time (kWaitLimitNs unless a caller passes less) or as soon as *abort
+// becomes nonzero.  Returns false when it gave up; the caller then records
+// MG_DERR_TIMEOUT and winds down.  Waits for copies or MMAs already issued
+// (the drain before a CTA exits) pass no abort flag and the full limit.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          const volatile int *abort) {
+                                          const volatile int *abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) return false;
+      if (global_ns() - t0 > limit_ns) return false;
     }
   }
 }

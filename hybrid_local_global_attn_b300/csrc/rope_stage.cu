@@ -10,7 +10,10 @@
 // taking positions < c0 from the ring (slot pos mod 2048) and the rest from
 // the chunk's own k_new / v_new; rows of negative positions are zero.  The
 // queries are rotated the same way: qs = R(pos) q.  Rotation is in fp32 with
-// exactly reduced angles (see rope_cos_sin) and rounds to bf16 once.
+// exactly reduced angles (see rope_cos_sin); each rotated value x is stored as
+// two bf16 values, hi = bf16(x) (ks, qs) and lo = bf16(x - hi) (ks_lo,
+// qs_lo), which the tensor-core kernel multiplies as hi.hi + lo.hi + hi.lo so
+// that the scores keep the rotation's fp32 precision.
 #include "mg_internal.h"
 #include "mg_ptx.cuh"
 
@@ -18,10 +21,21 @@ namespace mg {
 
 namespace {
 
-__device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, int32_t pos, int i0,
-                                        const RopeTurns &rt) {
-  uint32_t *l = reinterpret_cast<uint32_t *>(&lo);
-  uint32_t *h = reinterpret_cast<uint32_t *>(&hi);
+// Two fp32 values as bf16 pairs hi = bf16(v) and lo = bf16(v - hi).
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(a - bf16lo(hi), b - bf16hi(hi));
+}
+
+// Rotate dims i0..i0+7 (x) and their partners i0+64.. (y) by position pos;
+// the rotated values come back as hi parts in (x, y) and lo parts in
+// (xl, yl).
+__device__ __forceinline__ void rotate8(uint4 &x, uint4 &y, uint4 &xl, uint4 &yl, int32_t pos,
+                                        int i0, const RopeTurns &rt) {
+  uint32_t *l = reinterpret_cast<uint32_t *>(&x);
+  uint32_t *h = reinterpret_cast<uint32_t *>(&y);
+  uint32_t *ll = reinterpret_cast<uint32_t *>(&xl);
+  uint32_t *hl = reinterpret_cast<uint32_t *>(&yl);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     float c0, s0, c1, s1;
@@ -29,8 +43,8 @@ __device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, int32_t pos, int i
     rope_cos_sin(pos, rt.turn[i0 + 2 * e + 1], c1, s1);
     const float x0 = bf16lo(l[e]), x1 = bf16hi(l[e]);
     const float y0 = bf16lo(h[e]), y1 = bf16hi(h[e]);
-    l[e] = pack_bf16x2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1);
-    h[e] = pack_bf16x2(x0 * s0 + y0 * c0, x1 * s1 + y1 * c1);
+    split2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1, l[e], ll[e]);
+    split2(x0 * s0 + y0 * c0, x1 * s1 + y1 * c1, h[e], hl[e]);
   }
 }
 
@@ -52,7 +66,7 @@ __global__ void __launch_bounds__(256) rope_stage_kernel(const __grid_constant__
     const int32_t c0 = p.pos0[b];
     if (c0 < 0 || static_cast<int64_t>(c0) + p.n > p.max_len) return;  // flagged by the attention kernel
     const int64_t pos = static_cast<int64_t>(c0) - kWindow + r;
-    uint4 klo = make_uint4(0, 0, 0, 0), khi = klo, vlo = klo, vhi = klo;
+    uint4 klo = make_uint4(0, 0, 0, 0), khi = klo, vlo = klo, vhi = klo, klo_l = klo, khi_l = klo;
     if (pos >= 0) {
       const __nv_bfloat16 *ksrc, *vsrc;
       if (pos < c0) {
@@ -68,11 +82,13 @@ __global__ void __launch_bounds__(256) rope_stage_kernel(const __grid_constant__
       khi = __ldg(reinterpret_cast<const uint4 *>(ksrc + 64 + 8 * c));
       vlo = __ldg(reinterpret_cast<const uint4 *>(vsrc + 8 * c));
       vhi = __ldg(reinterpret_cast<const uint4 *>(vsrc + 64 + 8 * c));
-      rotate8(klo, khi, static_cast<int32_t>(pos), 8 * c, p.rope);
+      rotate8(klo, khi, klo_l, khi_l, static_cast<int32_t>(pos), 8 * c, p.rope);
     }
     const size_t dst = ((static_cast<size_t>(b) * kHkv + g) * p.R + r) * kD;
     *reinterpret_cast<uint4 *>(p.ks + dst + 8 * c) = klo;
     *reinterpret_cast<uint4 *>(p.ks + dst + 64 + 8 * c) = khi;
+    *reinterpret_cast<uint4 *>(p.ks_lo + dst + 8 * c) = klo_l;
+    *reinterpret_cast<uint4 *>(p.ks_lo + dst + 64 + 8 * c) = khi_l;
     *reinterpret_cast<uint4 *>(p.vs + dst + 8 * c) = vlo;
     *reinterpret_cast<uint4 *>(p.vs + dst + 64 + 8 * c) = vhi;
   } else {
@@ -85,9 +101,12 @@ __global__ void __launch_bounds__(256) rope_stage_kernel(const __grid_constant__
     const size_t off = ((static_cast<size_t>(b) * p.n + t) * kHq + h) * kD;
     uint4 lo = __ldg(reinterpret_cast<const uint4 *>(p.q + off + 8 * c));
     uint4 hi = __ldg(reinterpret_cast<const uint4 *>(p.q + off + 64 + 8 * c));
-    rotate8(lo, hi, c0 + t, 8 * c, p.rope);
+    uint4 lo_l, hi_l;
+    rotate8(lo, hi, lo_l, hi_l, c0 + t, 8 * c, p.rope);
     *reinterpret_cast<uint4 *>(p.qs + off + 8 * c) = lo;
     *reinterpret_cast<uint4 *>(p.qs + off + 64 + 8 * c) = hi;
+    *reinterpret_cast<uint4 *>(p.qs_lo + off + 8 * c) = lo_l;
+    *reinterpret_cast<uint4 *>(p.qs_lo + off + 64 + 8 * c) = hi_l;
   }
 }
 

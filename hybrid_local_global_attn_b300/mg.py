@@ -70,6 +70,9 @@ lib.mg_attn_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, 
 lib.mg_append_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_verify.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_prefill.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+lib.mg_debug_decode_stall.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, _P, _P,
+                                      ctypes.c_uint64, _i32]
+lib.mg_debug_decode_stall.restype = ctypes.c_int
 for _f in (lib.mg_kv_append, lib.mg_kv_commit, lib.mg_kv_commit_layers, lib.mg_attn_decode, lib.mg_append_decode, lib.mg_attn_verify,
            lib.mg_attn_prefill):
     _f.restype = ctypes.c_int
@@ -242,6 +245,17 @@ def mg_attn_decode(layer, cache: KVCache, pos, max_len, q, o, ws, err, stream=No
           int(max_len), _ptr(q, torch.bfloat16), _ptr(o, torch.bfloat16), _ptr(ws),
           ws.numel() * ws.element_size() if ws is not None else 0, _ptr(err, torch.int32),
           _stream(stream))
+
+
+def mg_debug_decode_stall(layer, cache: KVCache, pos, max_len, q, o, ws, err, wait_ns: int,
+                          stall_tile: int, stream=None):
+    """Self-test of the bounded waits: a global-layer decode whose producer
+    stops at key tile `stall_tile` of every split, with pipeline waits
+    limited to wait_ns; the device error word then reports DERR_TIMEOUT."""
+    _call(lib.mg_debug_decode_stall, ctypes.byref(layer), ctypes.byref(cache.struct),
+          _ptr(pos, torch.int32), int(max_len), _ptr(q, torch.bfloat16), _ptr(o, torch.bfloat16),
+          _ptr(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+          _ptr(err, torch.int32), _stream(stream), int(wait_ns), int(stall_tile))
 
 
 def mg_append_decode(layer, cache: KVCache, pos, max_len, q, k_new, v_new, o, ws, err, stream=None):

@@ -272,6 +272,25 @@ int mg_append_decode(const mg_layer *layer, const mg_cache *cache,
                      size_t ws_bytes, uint32_t *d_err, void *stream);
 
 /*
+ * Failure-detection self-test of the bounded waits (no counterpart on the
+ * pages; test infrastructure exposed through the ABI).  It runs
+ * mg_attn_decode of a global layer with a bf16 linear or paged cache, except
+ * that in every split the producer stops issuing key-tile copies at tile
+ * `stall_tile` (0 = the first tile of the split) and the pipeline waits give
+ * up after `wait_ns` nanoseconds (1 .. 2e9) instead of the normal 2 s.  A
+ * split with more than stall_tile tiles then waits for a tile that never
+ * arrives: its consumers time out, set MG_DERR_TIMEOUT in *d_err, stop, wait
+ * (with the full limit) for the copies already issued, and the kernel
+ * returns; the context stays usable and o holds undefined values.  Nothing
+ * faults, traps or hangs.  Same arguments as mg_attn_decode plus the two
+ * above; MG_ERR_UNSUPPORTED for a local layer or an FP8 cache.
+ */
+int mg_debug_decode_stall(const mg_layer *layer, const mg_cache *cache,
+                          const int32_t *d_pos, int32_t max_len, const void *q,
+                          void *o, void *ws, size_t ws_bytes, uint32_t *d_err,
+                          void *stream, uint64_t wait_ns, int32_t stall_tile);
+
+/*
  * Decode attention without a workspace argument, for callers that cannot
  * allocate device memory: for example a plugin inside a host framework that
  * owns every device buffer and gives plugins none, or a serving loop that
@@ -290,7 +309,9 @@ int mg_append_decode(const mg_layer *layer, const mg_cache *cache,
  * start at zero.  Calls that overlap on the GPU (e.g. on two streams) race on
  * it.  The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, that device current); make that first call before
- * any stream capture.
+ * any stream capture.  The address is kept with the context it was found in;
+ * after a device reset (a new primary context) the next call looks it up
+ * again, so that call too belongs before any capture.
  */
 #define MG_NOALLOC_SCRATCH_BYTES (4u << 20)
 int mg_attn_decode_noalloc(const mg_layer *layer, const mg_cache *cache,
