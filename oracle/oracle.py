@@ -267,3 +267,54 @@ def rope(x, t, theta=THETA):
     assert a.shape == (D,)
     lib().mg_oracle_rope(_ptr(a), float(t), float(theta))
     return a
+
+
+# ------------------------------------------------------ QKV projection ----
+# The step before the attention path: each token's hidden state (hidden size
+# 6656; "深度拆解Muse Glimmer，24 GB显存跑30 B Agent，Meta到底做了什么？", section 01,
+# which also gives the 32 query heads and 2 KV heads of dimension 128) is
+# projected to its query, key and value.  Reading (the pages give only the
+# sizes): one weight matrix W of 4608 x 6656 whose output features are the
+# 32 query heads (features 128 h .. 128 h + 127), then the 2 key heads
+# (4096 + 128 g ..), then the 2 value heads (4352 + 128 g ..); y = x W^T.
+# The projected K and V are appended to the layer's cache exactly as
+# cache_append does.
+
+HIDDEN = 6656
+QKV_FEATURES = (HQ + 2 * HKV) * D  # 4608
+
+
+def _widen(a):
+    """bf16 bit patterns (uint16 array or bf16 tensor) -> float64, exactly."""
+    b = bits(a)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def qkv_project(x, w):
+    """y = x W^T in float64 for x [M][6656] and W [4608][6656] (bf16 bits);
+    every product of two bf16 values is exact in float64 and the sum of 6656
+    of them is within a few units of 2^-53 of the exact value."""
+    xd, wd = _widen(x), _widen(w)
+    assert xd.ndim == 2 and xd.shape[1] == HIDDEN, xd.shape
+    assert wd.shape == (QKV_FEATURES, HIDDEN), wd.shape
+    return xd @ wd.T
+
+
+def qkv_split(y):
+    """[M][4608] -> q [M][32][128], k [M][2][128], v [M][2][128] (views)."""
+    y = np.asarray(y)
+    M = y.shape[0]
+    q = y[:, :HQ * D].reshape(M, HQ, D)
+    k = y[:, HQ * D:(HQ + HKV) * D].reshape(M, HKV, D)
+    v = y[:, (HQ + HKV) * D:].reshape(M, HKV, D)
+    return q, k, v
+
+
+def qkv_abs_bound(x, w):
+    """|x| |W|^T in float64: with it, a sum of the 6656 products accumulated
+    in fp32 in any order lies within gamma_6656 = 6656 u / (1 - 6656 u),
+    u = 2^-24, times this of the exact value."""
+    return np.abs(_widen(x)) @ np.abs(_widen(w)).T
+
+
+FP32_GAMMA_HIDDEN = HIDDEN * 2.0 ** -24 / (1 - HIDDEN * 2.0 ** -24)

@@ -520,3 +520,61 @@ def test_sink_key_closed_form(kind):
             assert np.abs(got[n, h] - vd[j, h // 16]).max() <= bound
             checked += 1
     assert checked >= 7 * 32
+
+
+# --------------------------------------------------------------------------
+# QKV projection (hidden size 6656 -> 32 query heads + 2 key + 2 value heads
+# of 128 [P1 §01]): y = x W^T in fp64, features laid out q | k | v.
+
+def test_qkv_projection_selection_weights_pick_inputs():
+    # W row f = e_{pi(f)}: every output is one input value, exactly, and the
+    # q / k / v split puts feature 128 h + d of q head h, 4096 + 128 g + d of
+    # key head g and 4352 + 128 g + d of value head g where the layout says.
+    rng = np.random.default_rng(5)
+    perm = rng.integers(0, orc.HIDDEN, size=orc.QKV_FEATURES)
+    w = torch.zeros((orc.QKV_FEATURES, orc.HIDDEN), dtype=torch.bfloat16)
+    w[torch.arange(orc.QKV_FEATURES), torch.from_numpy(perm)] = 1.0
+    x = synth.randn_bf16((3, orc.HIDDEN), 61)
+    y = orc.qkv_project(x, w)
+    xd = f64(x)
+    assert np.array_equal(y, xd[:, perm])
+    q, k, v = orc.qkv_split(y)
+    assert q.shape == (3, 32, 128) and k.shape == (3, 2, 128) and v.shape == (3, 2, 128)
+    assert q[1, 5, 7] == xd[1, perm[128 * 5 + 7]]
+    assert k[2, 1, 100] == xd[2, perm[4096 + 128 + 100]]
+    assert v[0, 0, 3] == xd[0, perm[4352 + 3]]
+
+
+def test_qkv_projection_matches_exact_sums():
+    # against math.fsum (a correctly rounded sum of the exact products) on a
+    # sample of outputs, and doubling x doubles y exactly
+    x = synth.randn_bf16((2, orc.HIDDEN), 62)
+    w = synth.scaled(synth.randn_bf16((orc.QKV_FEATURES, orc.HIDDEN), 63), 1.0 / 64)
+    y = orc.qkv_project(x, w)
+    xd, wd = f64(x), f64(w)
+    for m in range(2):
+        for f in [0, 1, 127, 128, 4095, 4096, 4351, 4352, 4607]:
+            exact = math.fsum(xd[m] * wd[f])
+            assert abs(y[m, f] - exact) <= 1e-12 * np.abs(xd[m] * wd[f]).sum()
+    y2 = orc.qkv_project(synth.scaled(x, 2.0), w)
+    assert np.array_equal(y2, 2 * y)
+
+
+def test_qkv_fp32_accumulation_bound_holds():
+    # the tolerance the GPU test uses: an fp32 sum of the 6656 products in
+    # any order stays within gamma_6656 |x| |W|^T of the exact value
+    # (checked here for sequential and pairwise fp32 orders)
+    x = synth.randn_bf16((2, orc.HIDDEN), 64)
+    w = synth.scaled(synth.randn_bf16((16, orc.HIDDEN), 65), 1.0 / 64)
+    wfull = torch.zeros((orc.QKV_FEATURES, orc.HIDDEN), dtype=torch.bfloat16)
+    wfull[:16] = w
+    y = orc.qkv_project(x, wfull)[:, :16]
+    bound = orc.FP32_GAMMA_HIDDEN * orc.qkv_abs_bound(x, wfull)[:, :16]
+    prods = (f64(x)[:, None, :] * f64(w)[None, :, :]).astype(np.float32)  # exact in fp32
+    seq = np.zeros((2, 16), np.float32)
+    for i in range(orc.HIDDEN):
+        seq += prods[:, :, i]
+    pair = prods.sum(axis=2, dtype=np.float32)
+    for s in (seq, pair):
+        assert (np.abs(s.astype(np.float64) - y) <= bound).all()
+    assert bound.max() < 0.05  # outputs here have sigma ~1.3
