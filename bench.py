@@ -311,6 +311,153 @@ def leg_prefill(wl, fill_only=False):
     return res
 
 
+def leg_verify_batches(wl, batches=(2, 8), reps=5):
+    """The verify pass (16 draft tokens per sequence at p0 = 131072, all 52
+    layers, one graph) at larger batches: caches of batch B filled with
+    N(0, 1) values for positions 0 .. 131071 (the prompt's contents do not
+    change the work), every sequence at the same position."""
+    import torch
+    mg, dev, err = wl.mg, wl.dev, wl.err
+    res = {}
+    for B in batches:
+        caches = []
+        for l in range(N_LAYERS):
+            c = mg.KVCache(wl.kinds[l], B, PROMPT + 16, device=dev)
+            c.k.normal_()
+            c.v.normal_()
+            caches.append(c)
+        ws = [mg.workspace(mg.OP_VERIFY, wl.layers[l], B, 16, PROMPT + 16, device=dev)
+              for l in range(N_LAYERS)]
+        q = torch.randn((N_LAYERS, B, 16, 32, 128), device=dev).to(torch.bfloat16)
+        kn = torch.randn((N_LAYERS, B, 16, 2, 128), device=dev).to(torch.bfloat16)
+        vn = torch.randn_like(kn)
+        o = torch.empty_like(q)
+        p0 = torch.full((B,), PROMPT, dtype=torch.int32, device=dev)
+
+        def run():
+            for l in range(N_LAYERS):
+                mg.mg_attn_verify(wl.layers[l], caches[l], p0, PROMPT + 16, q[l], kn[l], vn[l], o[l],
+                                  ws[l], err)
+
+        us = _graph_us(run, reps=reps)
+        nbytes = B * sum(verify_layer_bytes(k, PROMPT, 16) for k in wl.kinds)
+        flops = B * sum(verify_layer_flops(k, PROMPT, 16) for k in wl.kinds)
+        res[f"b{B}"] = {"us_per_pass_52_layers": us, "gbs": nbytes / us / 1e3,
+                        "tflops": flops / us / 1e6}
+        del caches, ws, q, kn, vn, o
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after verify batches"
+    return res
+
+
+def leg_pr1(wl, P0=2000, steps=256):
+    """The two-layer workload: one local (window 2048, RoPE) and one global
+    layer, batch 1, caches filled for positions 0 .. P0-1, then `steps`
+    single-token steps at P0, P0+1, ... (crossing the ring wrap at 2048),
+    each an append of the token's K/V and a decode, in both layers.  The
+    whole sequence of steps is one CUDA graph (so the host launch cost is
+    not timed); reported per step, as two calls per layer (mg_kv_append +
+    mg_attn_decode) and with the append fused (mg_append_decode)."""
+    import torch
+    mg, dev, err = wl.mg, wl.dev, wl.err
+    T = P0 + steps
+    kinds = (mg.LOCAL, mg.GLOBAL)
+    layers = [mg.make_layer(k) for k in kinds]
+    caches = [mg.KVCache(k, 1, T, device=dev) for k in kinds]
+    pos0 = torch.zeros(1, dtype=torch.int32, device=dev)
+    for c, lay in zip(caches, layers):
+        mg.mg_kv_append(lay, c, pos0, wl.randn((1, P0, 2, 128), 7), wl.randn((1, P0, 2, 128), 8), err)
+    ws = [mg.workspace(mg.OP_DECODE, lay, 1, 1, T, device=dev) for lay in layers]
+    q = wl.randn((steps, 2, 1, 32, 128), 9)
+    kn = wl.randn((steps, 2, 1, 1, 2, 128), 10)
+    vn = wl.randn((steps, 2, 1, 1, 2, 128), 11)
+    o = torch.empty((steps, 2, 1, 32, 128), dtype=torch.bfloat16, device=dev)
+    pos = torch.arange(P0, T, dtype=torch.int32, device=dev)
+
+    def separate():
+        for i in range(steps):
+            for j in range(2):
+                mg.mg_kv_append(layers[j], caches[j], pos[i:i + 1], kn[i, j], vn[i, j], err)
+                mg.mg_attn_decode(layers[j], caches[j], pos[i:i + 1], T, q[i, j], o[i, j], ws[j], err)
+
+    def fused():
+        for i in range(steps):
+            for j in range(2):
+                mg.mg_append_decode(layers[j], caches[j], pos[i:i + 1], T, q[i, j], kn[i, j],
+                                    vn[i, j], o[i, j], ws[j], err)
+
+    us_sep = _graph_us(separate, reps=5, calls=steps)
+    us_fused = _graph_us(fused, reps=5, calls=steps)
+    nbytes = sum(decode_layer_bytes(k, p) for p in range(P0, T) for k in kinds) / steps
+    assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after PR1"
+    del caches, ws, q, kn, vn, o
+    torch.cuda.empty_cache()
+    return {"positions": [P0, T - 1], "us_per_step_append_then_decode": us_sep,
+            "us_per_step_fused": us_fused, "bytes_per_step": nbytes,
+            "gbs_fused": nbytes / us_fused / 1e3}
+
+
+def leg_prefill_32k(wl, T=32768, chunk=4096, reps=3):
+    """Causal chunked prefill of a 32768-token prompt in 4096-token chunks
+    (prefill each chunk, then append it), one global and one local layer,
+    batch 1; TFLOP/s of the unmasked (query head, key) pairs."""
+    import torch
+    mg, dev, err = wl.mg, wl.dev, wl.err
+    res = {"prompt": T, "chunk": chunk}
+    for kind in (mg.GLOBAL, mg.LOCAL):
+        lay = mg.make_layer(kind)
+        cache = mg.KVCache(kind, 1, T, device=dev)
+        q = wl.randn((1, T, 32, 128), 20 + kind)
+        k = wl.randn((1, T, 2, 128), 22 + kind)
+        v = wl.randn((1, T, 2, 128), 24 + kind)
+        ws = mg.workspace(mg.OP_PREFILL, lay, 1, chunk, T, device=dev)
+        o = torch.empty((1, chunk, 32, 128), dtype=torch.bfloat16, device=dev)
+        pos = torch.arange(0, T, chunk, dtype=torch.int32, device=dev)
+
+        def run():
+            for ci, c0 in enumerate(range(0, T, chunk)):
+                kc, vc = k[:, c0:c0 + chunk], v[:, c0:c0 + chunk]
+                mg.mg_attn_prefill(lay, cache, pos[ci:ci + 1], c0 + chunk, q[:, c0:c0 + chunk], kc,
+                                   vc, o, ws, err)
+                mg.mg_kv_append(lay, cache, pos[ci:ci + 1], kc, vc, err)
+
+        ms = _graph_us(run, reps=reps) / 1e3
+        f = sum(prefill_layer_flops(kind, c0, chunk) for c0 in range(0, T, chunk))
+        name = "global" if kind == mg.GLOBAL else "local"
+        res[name] = {"ms": ms, "tflops": f / ms / 1e9, "flop": f}
+        del cache, q, k, v, ws, o
+        torch.cuda.empty_cache()
+    assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after 32K prefill"
+    return res
+
+
+def leg_qkv(wl, reps=5):
+    """The QKV projection with the KV append fused into its epilogue
+    (mg_qkv_append): hidden 6656 -> 4608 features (32 q + 2 k + 2 v heads),
+    weights N(0, 1/64^2) in bf16.  A prefill chunk of 8192 tokens (TFLOP/s of
+    2 * M * 6656 * 4608) and decode of 1 and 16 tokens (GB/s of the 61 MB of
+    weights every call streams, plus x and the outputs)."""
+    import torch
+    mg, dev, err = wl.mg, wl.dev, wl.err
+    w = (wl.randn((4608, 6656), 31).float() / 64).to(torch.bfloat16)
+    lay = mg.make_layer(mg.GLOBAL)
+    res = {}
+    for name, B, n in (("prefill_8192", 1, 8192), ("decode_b1", 1, 1), ("decode_b16", 16, 1)):
+        cache = mg.KVCache(mg.GLOBAL, B, 8192 + 8, device=dev)
+        x = wl.randn((B, n, 6656), 32)
+        q = torch.empty((B, n, 32, 128), dtype=torch.bfloat16, device=dev)
+        ws = mg.qkv_workspace(B, n, device=dev)
+        pos = torch.full((B,), 0 if n > 1 else 8192, dtype=torch.int32, device=dev)
+        us = _graph_us(lambda: mg.mg_qkv_append(lay, cache, pos, x, w, q, ws, err), reps=reps)
+        flop = 2 * B * n * 6656 * 4608
+        nbytes = 4608 * 6656 * 2 + B * n * (6656 + 4608) * 2
+        res[name] = {"us": us, "tflops": flop / us / 1e6, "gbs": nbytes / us / 1e3}
+        del cache, x, q, ws
+    assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after qkv"
+    return res
+
+
 def leg_verify(wl):
     import torch
     mg, dev, err = wl.mg, wl.dev, wl.err
@@ -536,7 +683,7 @@ def leg_e4m3(wl, steps=16):
     return res
 
 
-def leg_sweep(wl, hbm_peak, ctx=32768, batches=(1, 4, 16), steps=16):
+def leg_sweep(wl, hbm_peak, ctx=32768, batches=(1, 4, 16), steps=128):
     """The decode sweep: one fused append + decode step through all 52 layers
     at context `ctx` for each batch size, from a CUDA graph (caches filled
     with N(0,1) values; every sequence at the same position).  GB/s of
@@ -575,11 +722,13 @@ def leg_sweep(wl, hbm_peak, ctx=32768, batches=(1, 4, 16), steps=16):
             g.replay()
         e0.record()
         for i in range(steps):
-            g.replay()  # the same position each step: the same bytes
+            pos.fill_(ctx + i)  # positions ctx .. ctx + steps - 1
+            g.replay()
         e1.record()
         e1.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / steps
-        nbytes = B * sum(decode_layer_bytes(mg.mg_layer_kind(l), ctx) for l in range(N_LAYERS))
+        nbytes = B * sum(decode_layer_bytes(mg.mg_layer_kind(l), ctx + i) for l in range(N_LAYERS)
+                         for i in range(steps)) / steps
         res[f"b{B}"] = {"us_per_step": us, "gbs": nbytes / us / 1e3,
                         "frac_of_measured_hbm": nbytes / us / 1e3 / hbm_peak,
                         "tokens_per_s": B * 1e6 / us}
@@ -625,6 +774,26 @@ def run_gpu(args, rank, world):
     if "sweep" in legs:
         line_extra["decode_sweep"] = leg_sweep(wl, hbm_peak)
         log("sweep: " + json.dumps(line_extra["decode_sweep"]))
+    if "verify_batches" in legs:
+        line_extra["verify_batches"] = leg_verify_batches(wl)
+        log("verify batches: " + json.dumps(line_extra["verify_batches"]))
+    if "pr1" in legs:
+        line_extra["pr1"] = leg_pr1(wl)
+        log("pr1: " + json.dumps(line_extra["pr1"]))
+    if "qkv" in legs:
+        line_extra["qkv_projection"] = leg_qkv(wl)
+        d = line_extra["qkv_projection"]
+        d["prefill_8192"]["frac_of_bf16_peak"] = d["prefill_8192"]["tflops"] / tf_peak
+        for nm in ("decode_b1", "decode_b16"):
+            d[nm]["frac_of_measured_hbm"] = d[nm]["gbs"] / hbm_peak
+        log("qkv: " + json.dumps(d))
+    if "prefill32k" in legs:
+        line_extra["prefill_32k"] = leg_prefill_32k(wl)
+        for nm in ("global", "local"):
+            d = line_extra["prefill_32k"][nm]
+            d["frac_of_bf16_peak"] = d["tflops"] / tf_peak
+            d["frac_of_bf16_sustained"] = d["tflops"] / tf_sus if tf_sus else None
+        log("prefill 32k: " + json.dumps(line_extra["prefill_32k"]))
 
     # ------------------------------------------------------------- decode ----
     ws_dec = [mg.workspace(mg.OP_DECODE, layers[l], 1, 1, cap, device=dev) for l in range(N_LAYERS)]
@@ -765,6 +934,7 @@ def run_gpu(args, rank, world):
                                               "layer at context 131072+",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
+                     "frac_nominal": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": kern_bytes, "ms_per_launch": kern_ms,
                      "traffic": traffic},
         **line_extra,
@@ -947,7 +1117,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="mg", choices=["mg", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--legs", default="prefill,verify,paged,e4m3,sweep,decode",
+    ap.add_argument("--legs",
+                    default="prefill,verify,paged,e4m3,sweep,verify_batches,pr1,prefill32k,qkv,decode",
                     help="comma list of legs to run besides decode")
     ap.add_argument("--fill", default="prefill", choices=["prefill", "random"],
                     help="random: fill caches without attention (profiling runs only)")

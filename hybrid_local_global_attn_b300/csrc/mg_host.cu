@@ -602,6 +602,61 @@ int mg_attn_decode(const mg_layer *layer, const mg_cache *cache, const int32_t *
                      stream);
 }
 
+size_t mg_qkv_workspace_bytes(int32_t batch, int32_t n) {
+  if (batch < 1 || n < 1) return static_cast<size_t>(-1);
+  const int64_t M = static_cast<int64_t>(batch) * n;
+  if (M > 0x7fffffff / kQkvFeatures) return static_cast<size_t>(-1);
+  const int splits = qkv_splits(static_cast<int32_t>(M));
+  return splits > 1 ? align256(static_cast<size_t>(splits) * M * kQkvFeatures * sizeof(float)) : 0;
+}
+
+int mg_qkv_append(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos0, int32_t n,
+                  const void *x, const void *w, void *q_out, void *k_out, void *v_out, void *ws,
+                  size_t ws_bytes, uint32_t *d_err, void *stream) {
+  int st = check_layer(layer);
+  if (st != MG_OK) return st;
+  if ((st = check_cache(layer, cache)) != MG_OK) return st;
+  if (cache->dtype != MG_BF16) return MG_ERR_UNSUPPORTED;
+  if (d_pos0 == nullptr || d_err == nullptr || x == nullptr || w == nullptr || q_out == nullptr)
+    return MG_ERR_INVALID;
+  if ((k_out == nullptr) != (v_out == nullptr)) return MG_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(q_out) ||
+      (k_out != nullptr && (!aligned16(k_out) || !aligned16(v_out))))
+    return MG_ERR_INVALID;
+  if (n < 1) return MG_ERR_INVALID;
+  const size_t need = mg_qkv_workspace_bytes(cache->batch, n);
+  if (need == static_cast<size_t>(-1)) return MG_ERR_INVALID;
+  if (ws_bytes < need || (need > 0 && ws == nullptr)) return MG_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(ws)) return MG_ERR_INVALID;
+  const int32_t M = cache->batch * n;
+  CUtensorMap tx, tw;
+  {
+    const uint64_t xd[2] = {static_cast<uint64_t>(kHidden), static_cast<uint64_t>(M)};
+    const uint32_t xb[2] = {64, 128};
+    const uint64_t wd[2] = {static_cast<uint64_t>(kHidden), static_cast<uint64_t>(kQkvFeatures)};
+    const uint32_t wb[2] = {64, 256};
+    if (!make_map(&tx, x, 2, xd, xb) || !make_map(&tw, w, 2, wd, wb)) return MG_ERR_CUDA;
+  }
+  QkvParams p;
+  std::memset(&p, 0, sizeof p);
+  p.pos0 = d_pos0;
+  p.q_out = static_cast<__nv_bfloat16 *>(q_out);
+  p.k_out = static_cast<__nv_bfloat16 *>(k_out);
+  p.v_out = static_cast<__nv_bfloat16 *>(v_out);
+  p.k_cache = static_cast<__nv_bfloat16 *>(cache->k);
+  p.v_cache = static_cast<__nv_bfloat16 *>(cache->v);
+  p.part = static_cast<float *>(ws);
+  p.err = d_err;
+  p.M = M;
+  p.n = n;
+  p.batch = cache->batch;
+  p.kind = layer->kind;
+  p.slots = cache->slots;
+  p.splits = qkv_splits(M);
+  p.map = cache_map(cache);
+  return launch_status(launch_qkv(p, tx, tw, static_cast<cudaStream_t>(stream)));
+}
+
 int mg_debug_decode_stall(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
                           int32_t max_len, const void *q, void *o, void *ws, size_t ws_bytes,
                           uint32_t *d_err, void *stream, uint64_t wait_ns, int32_t stall_tile) {

@@ -21,6 +21,9 @@ constexpr int kD = 128;
 constexpr int kGroup = kHq / kHkv;  // 16 query heads per KV head
 constexpr int kWindow = 2048;
 constexpr int kRowBytes = kD * 2;   // one bf16 head row
+// Hidden size of a token and the projected features (32 q + 2 k + 2 v heads)
+constexpr int kHidden = 6656;
+constexpr int kQkvFeatures = (kHq + 2 * kHkv) * kD;  // 4608
 
 // Every pipeline wait gives up after this much wall time (ns).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -210,6 +213,17 @@ struct TcParams {
   CacheMap map;
 };
 
+struct QkvParams {  // fused QKV projection + append
+  const int32_t *pos0;               // [B]: position of each sequence's first token
+  __nv_bfloat16 *q_out;              // [B][n][32][128]
+  __nv_bfloat16 *k_out, *v_out;      // [B][n][2][128] or nullptr
+  __nv_bfloat16 *k_cache, *v_cache;  // the layer's cache (ring, linear or paged)
+  float *part;                       // split-K partials [splits][M][4608]
+  uint32_t *err;
+  int32_t M, n, batch, kind, slots, splits, ksteps;
+  CacheMap map;
+};
+
 // Launch with programmatic stream serialization, so the kernel may be
 // scheduled while the previous kernel in the stream drains; every kernel of
 // the library calls pdl_wait() before reading anything an earlier kernel
@@ -250,6 +264,10 @@ cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtens
                               cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 cudaError_t launch_rope_stage(const StageParams &p, cudaStream_t s);
+// K-range splits the projection uses for M tokens (1 when the output tiles
+// fill the GPU), and the launch (the GEMM, then the split reduction)
+int qkv_splits(int32_t M);
+cudaError_t launch_qkv(QkvParams p, const CUtensorMap &tx, const CUtensorMap &tw, cudaStream_t s);
 // (tql, tkl: the lo halves of staged queries and keys, read by the precise
 // form that local layers run)
 cudaError_t launch_attn_tc(const TcParams &p, const CUtensorMap &tq, const CUtensorMap &tka,

@@ -70,6 +70,10 @@ lib.mg_attn_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, 
 lib.mg_append_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_verify.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_prefill.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+lib.mg_qkv_workspace_bytes.argtypes = [_i32, _i32]
+lib.mg_qkv_workspace_bytes.restype = ctypes.c_size_t
+lib.mg_qkv_append.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+lib.mg_qkv_append.restype = ctypes.c_int
 lib.mg_debug_decode_stall.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, _P, _P,
                                       ctypes.c_uint64, _i32]
 lib.mg_debug_decode_stall.restype = ctypes.c_int
@@ -245,6 +249,32 @@ def mg_attn_decode(layer, cache: KVCache, pos, max_len, q, o, ws, err, stream=No
           int(max_len), _ptr(q, torch.bfloat16), _ptr(o, torch.bfloat16), _ptr(ws),
           ws.numel() * ws.element_size() if ws is not None else 0, _ptr(err, torch.int32),
           _stream(stream))
+
+
+HIDDEN = 6656
+QKV_FEATURES = (HQ + 2 * HKV) * D
+
+
+def mg_qkv_workspace_bytes(batch: int, n: int) -> int:
+    v = int(lib.mg_qkv_workspace_bytes(batch, n))
+    if v == ctypes.c_size_t(-1).value:
+        raise MgError(1)
+    return v
+
+
+def qkv_workspace(batch, n, device="cuda"):
+    return torch.empty(max(mg_qkv_workspace_bytes(batch, n), 256), dtype=torch.uint8, device=device)
+
+
+def mg_qkv_append(layer, cache, pos0, x, w, q_out, ws, err, k_out=None, v_out=None, stream=None):
+    """Project x [B][n][6656] with w [4608][6656] to q_out [B][n][32][128] and
+    append the key / value rows to `cache` at pos0[b] ..; k_out / v_out
+    [B][n][2][128] optionally receive them too."""
+    _call(lib.mg_qkv_append, ctypes.byref(layer), ctypes.byref(cache.struct), _ptr(pos0, torch.int32),
+          int(x.shape[1]), _ptr(x, torch.bfloat16), _ptr(w, torch.bfloat16),
+          _ptr(q_out, torch.bfloat16), _ptr(k_out, torch.bfloat16), _ptr(v_out, torch.bfloat16),
+          _ptr(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+          _ptr(err, torch.int32), _stream(stream))
 
 
 def mg_debug_decode_stall(layer, cache: KVCache, pos, max_len, q, o, ws, err, wait_ns: int,

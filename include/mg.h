@@ -272,6 +272,38 @@ int mg_append_decode(const mg_layer *layer, const mg_cache *cache,
                      size_t ws_bytes, uint32_t *d_err, void *stream);
 
 /*
+ * Fused QKV projection with the KV append in its epilogue: the step before
+ * the attention calls.  [P1 §01] gives the hidden size (6656), 32 query heads
+ * and 2 KV heads of dimension 128, so each token's hidden state projects to
+ * 4096 query and 2 x 256 key / value features; the weight layout is this
+ * library's reading (the pages give none).  For the n tokens of sequence b,
+ * at positions pos0[b] .. pos0[b]+n-1:
+ *   y = x W^T  (bf16 products, fp32 accumulation, rounded once to bf16)
+ * with output feature f = 128 h + d of query head h (f < 4096), then
+ * 4096 + 128 g + d of key head g, then 4352 + 128 g + d of value head g.
+ * The query rows go to q_out; the key and value rows are stored in the
+ * layer's cache exactly as mg_kv_append stores k_new / v_new (ring slot
+ * pos mod 2048 -- of n > 2048 tokens only the last 2048 -- or row pos of a
+ * linear or paged global cache), and also to k_out / v_out when given.
+ *   x            : bf16 [batch][n][6656] (device, 16-byte aligned)
+ *   w            : bf16 [4608][6656] (device): row f holds output feature f's weights
+ *   q_out        : bf16 [batch][n][32][128] (device)
+ *   k_out, v_out : bf16 [batch][n][2][128] (device), or both NULL
+ *   ws           : >= mg_qkv_workspace_bytes(batch, n) bytes (device; with
+ *                  few tokens the K range is split and fp32 partials meet
+ *                  there; 0 bytes when the output tiles fill the GPU)
+ * bf16 caches only (MG_ERR_UNSUPPORTED for MG_E4M3).  A negative pos0[b], or
+ * a global position >= slots, flags MG_DERR_POSITION and that row is not
+ * stored (q_out / k_out / v_out are still written).
+ */
+#define MG_HIDDEN 6656       /* hidden size [P1 §01] */
+#define MG_QKV_FEATURES 4608 /* (32 + 2 + 2) x 128 */
+size_t mg_qkv_workspace_bytes(int32_t batch, int32_t n);
+int mg_qkv_append(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos0, int32_t n,
+                  const void *x, const void *w, void *q_out, void *k_out, void *v_out, void *ws,
+                  size_t ws_bytes, uint32_t *d_err, void *stream);
+
+/*
  * Failure-detection self-test of the bounded waits (no counterpart on the
  * pages; test infrastructure exposed through the ABI).  It runs
  * mg_attn_decode of a global layer with a bf16 linear or paged cache, except

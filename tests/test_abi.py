@@ -183,3 +183,31 @@ def test_noalloc_scratch_covers_every_decode_batch(mg):
         for max_len in (1, 4096, 131072, 1 << 20):
             need = mg.mg_workspace_bytes(mg.OP_DECODE, lay, B, 1, max_len)
             assert need <= 4 << 20, (B, max_len, need)
+
+
+def test_qkv_append_host_checks(mg):
+    """mg_qkv_append: workspace sizes and argument checks, before any CUDA call."""
+    lib = mg.lib
+    by = ctypes.byref
+    fake = ctypes.c_void_p(0x1000)
+    # few tokens: the K range is split and fp32 partials need room; a full
+    # grid of output tiles needs none
+    assert mg.mg_qkv_workspace_bytes(1, 1) == 8 * 1 * mg.QKV_FEATURES * 4
+    assert mg.mg_qkv_workspace_bytes(4, 40) == 4 * 160 * mg.QKV_FEATURES * 4  # 36 tiles, 4 splits
+    assert mg.mg_qkv_workspace_bytes(1, 8192) == 0
+    with pytest.raises(mg.MgError):
+        mg.mg_qkv_workspace_bytes(0, 1)
+    L, G = mg.make_layer(mg.LOCAL), mg.make_layer(mg.GLOBAL)
+    ring = mg.mg_cache(0x10000, 0x20000, 1, 2048)
+    args = lambda lay, c, n=1, x=fake, q=fake, k=None, v=None, ws=fake, wsb=1 << 30: (
+        by(lay), by(c), fake, n, x, fake, q, k, v, ws, wsb, fake, None)
+    assert lib.mg_qkv_append(*args(L, ring, x=None)) == 1             # no input
+    assert lib.mg_qkv_append(*args(L, ring, q=None)) == 1             # no query output
+    assert lib.mg_qkv_append(*args(L, ring, k=fake)) == 1             # k_out without v_out
+    assert lib.mg_qkv_append(*args(L, ring, n=0)) == 1
+    assert lib.mg_qkv_append(*args(L, ring, x=ctypes.c_void_p(0x1008))) == 1  # misaligned
+    assert lib.mg_qkv_append(*args(L, ring, wsb=100)) == 4            # workspace too small
+    e4 = mg.mg_cache(0x10000, 0x20000, 1, 4096, None, 0, 0, mg.E4M3,
+                     (ctypes.c_float * 2)(1.0, 1.0), (ctypes.c_float * 2)(1.0, 1.0))
+    assert lib.mg_qkv_append(*args(G, e4)) == 2                       # FP8 cache
+    assert lib.mg_qkv_append(*args(L, mg.mg_cache(0x10000, 0x20000, 1, 4096))) == 2  # not a ring
