@@ -1103,6 +1103,37 @@ def run_ncu_case(name):
         pos = torch.tensor([c0], dtype=torch.int32, device=dev)
         for _ in range(4):
             mg.mg_attn_prefill(lay, cache, pos, c0 + n, q, kn, vn, o, ws, err)
+    elif name in ("qkv_prefill", "qkv_decode"):
+        # the fused projection: an 8192-token chunk (x 109 MB + W 61 MB, more
+        # than L2), or one decode token (W streamed from HBM)
+        n = 8192 if name == "qkv_prefill" else 1
+        lay = mg.make_layer(mg.GLOBAL)
+        cache = mg.KVCache(mg.GLOBAL, 1, 8192 + 8)
+        w = (torch.randn((4608, 6656), device=dev) / 64).to(bf)
+        x = torch.randn((1, n, 6656), device=dev).to(bf)
+        q = torch.empty((1, n, 32, 128), dtype=bf, device=dev)
+        ws = mg.qkv_workspace(1, n)
+        pos = torch.tensor([0 if n > 1 else 8192], dtype=torch.int32, device=dev)
+        for _ in range(4):
+            mg.mg_qkv_append(lay, cache, pos, x, w, q, ws, err)
+    elif name in ("append_chunk", "commit_layers"):
+        if name == "append_chunk":  # an 8192-token chunk into a global cache (16 MB moved)
+            lay = mg.make_layer(mg.GLOBAL)
+            cache = mg.KVCache(mg.GLOBAL, 1, 131072)
+            kn = torch.randn((1, 8192, 2, 128), device=dev).to(bf)
+            vn = torch.randn_like(kn)
+            pos = torch.tensor([65536], dtype=torch.int32, device=dev)
+            for _ in range(4):
+                mg.mg_kv_append(lay, cache, pos, kn, vn, err)
+        else:  # a verified 16-token block into all 52 caches in one launch
+            layers = [mg.make_layer(mg.mg_layer_kind(l)) for l in range(52)]
+            caches = [mg.KVCache(mg.mg_layer_kind(l), 1, 4096) for l in range(52)]
+            kn = torch.randn((52, 1, 16, 2, 128), device=dev).to(bf)
+            vn = torch.randn_like(kn)
+            pos = torch.tensor([3000], dtype=torch.int32, device=dev)
+            cnt = torch.tensor([11], dtype=torch.int32, device=dev)
+            for _ in range(4):
+                mg.mg_kv_commit_layers(layers, caches, pos, cnt, kn, vn, err)
     else:
         raise SystemExit(f"unknown ncu case {name}")
     torch.cuda.synchronize()
@@ -1124,7 +1155,8 @@ def main():
                     help="random: fill caches without attention (profiling runs only)")
     ap.add_argument("--ncu-case", default=None,
                     help="decode_global | decode_global_e4m3 | verify_global | decode_local | verify_local | "
-                         "prefill_global | prefill_local")
+                         "prefill_global | prefill_local | qkv_prefill | qkv_decode | append_chunk | "
+                         "commit_layers")
     ap.add_argument("--micro", action="store_true",
                     help="per-call cost of each entry point in graphs of back-to-back calls")
     args = ap.parse_args()
