@@ -142,18 +142,20 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def profile_traffic(kernel_file, profile_name):
-    """DRAM traffic per launch from a committed ncu summary, if it was taken
-    on the current kernel source (sha256 recorded in the summary)."""
+def profile_traffic(kernel_file, profile_name, keys):
+    """DRAM traffic of one launch over `keys` keys, from the per-key traffic
+    a committed ncu summary measured (K/V traffic grows in proportion to the
+    keys), if that summary was taken on the current kernel source (sha256
+    recorded in the summary)."""
     src = os.path.join(ROOT, "hybrid_local_global_attn_b300", "csrc", kernel_file)
     prof = os.path.join(ROOT, "profiles", profile_name)
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
         text = open(prof).read()
         m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-        m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        m_tr = re.search(r"traffic_bytes_per_key:\s*([0-9.eE+]+)", text)
         if m_sha and m_tr and m_sha.group(1) == sha:
-            return float(m_tr.group(1))
+            return float(m_tr.group(1)) * keys
     except OSError:
         pass
     return None
@@ -884,7 +886,7 @@ def run_gpu(args, rank, world):
     kern_ms = e0.elapsed_time(e1) / (reps * len(glob))
     kern_bytes = decode_layer_bytes(1, p_last)
     achieved = kern_bytes / (kern_ms / 1e3) / 1e9
-    traffic = profile_traffic("attn_decode.cu", "attn_decode_global_262k.md")
+    traffic = profile_traffic("attn_decode.cu", "attn_decode_global_262k.md", p_last + 1)
 
     # ---------------------------------------------------------------- e2e ----
     # Inputs in pinned host memory; every step copies its inputs in, replays
