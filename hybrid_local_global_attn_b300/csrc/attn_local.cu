@@ -154,7 +154,13 @@ __device__ __forceinline__ void zero4(float (&a)[4]) { a[0] = a[1] = a[2] = a[3]
 
 }  // namespace
 
-__global__ void __launch_bounds__(kLocThreads, 1)
+// kMinCtas = 2 caps the registers at 128 per thread so that two CTAs share
+// an SM: a 16-CTA cluster then needs 8 SMs of a GPC instead of 16, and
+// twice as many clusters run at once (14 instead of 7 on this B300).  One
+// CTA per SM keeps each cluster's latency chain shortest when the batch's
+// clusters fit in one wave anyway.
+template <int kMinCtas>
+__global__ void __launch_bounds__(kLocThreads, kMinCtas)
     local_attn_kernel(const __grid_constant__ LocalParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv) {
   extern __shared__ uint8_t smem_raw[];
@@ -495,7 +501,12 @@ cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtens
   static_assert(kGroup == kLocCluster, "CTA r of a cluster owns head r of the group");
   static_assert(kLocSmem <= 227 * 1024, "shared memory");
   if (p.n != 1 || p.batch < 1) return cudaErrorInvalidValue;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(local_attn_kernel), kLocSmem, 2);
+  // one cluster per (sequence, KV head): up to 7 run at once with one CTA
+  // per SM, 14 with two
+  const bool two = p.batch * kHkv > 7;
+  const void *kern = two ? reinterpret_cast<const void *>(local_attn_kernel<2>)
+                         : reinterpret_cast<const void *>(local_attn_kernel<1>);
+  cudaError_t e = ensure_smem_attr(kern, kLocSmem, two ? 7 : 2);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kLocCluster, kHkv, p.batch);
@@ -511,7 +522,8 @@ cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtens
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, local_attn_kernel, p, tk, tv);
+  return two ? cudaLaunchKernelEx(&cfg, local_attn_kernel<2>, p, tk, tv)
+             : cudaLaunchKernelEx(&cfg, local_attn_kernel<1>, p, tk, tv);
 }
 
 }  // namespace mg

@@ -129,7 +129,7 @@ cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id) {
   std::lock_guard<std::mutex> lk(mu);
   if (done[kernel_id] & (1ull << dev)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && (kernel_id == 2 || kernel_id == 3))  // local layers: 16-CTA clusters
+  if (e == cudaSuccess && (kernel_id == 2 || kernel_id == 3 || kernel_id == 7))  // 16-CTA clusters
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[kernel_id] |= 1ull << dev;
   return e;
