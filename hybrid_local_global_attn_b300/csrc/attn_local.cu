@@ -37,11 +37,18 @@
 //  * A single new token (decode with fused append, or the block of a
 //    one-token verify) replaces the ring row of its slot in the owning CTA's
 //    shared-memory copy; decode also writes it to the ring.
-//  * Cluster merge: CTA r owns head r of the group; every CTA pushes its
-//    normalised partial row and its log-sum-exp into the owner's shared
-//    memory with st.async, whose bytes complete on the owner's mbarrier; the
-//    owner merges as soon as its own inbox is full (no cluster-wide barrier
-//    at the end) and writes the bf16 output.
+//  * Cluster merge: each CTA owns 16 / (cluster size) heads of the group;
+//    every CTA pushes its normalised partial rows and log-sum-exps into the
+//    owners' shared memory with st.async, whose bytes complete on the
+//    owner's mbarrier; an owner merges as soon as its own inbox is full (no
+//    cluster-wide barrier at the end) and writes the bf16 output.
+//  * Cluster size by batch: a 16-CTA cluster needs 16 SMs of one GPC, so at
+//    most 7 run at once.  With more (sequence, KV head) pairs than that, the
+//    window is cut into 8 or 4 pieces of 256 or 512 slots and each CTA walks
+//    its piece in rounds of 128 slots (2 tiles): the next round's copies are
+//    in flight while a round computes, and an online softmax (running max,
+//    rescaled sum and output) carries the rounds.  15 clusters of 8 or 33 of
+//    4 run at once.
 #include "mg_internal.h"
 #include "mg_ptx.cuh"
 #include "mma_frag.cuh"
@@ -52,22 +59,33 @@ namespace {
 
 constexpr int kLocWarps = 8;                      // consumer warps
 constexpr int kLocThreads = kLocWarps * 32;
-constexpr int kPiece = kWindow / kLocCluster;     // 128 ring slots per CTA
-constexpr int kLocTiles = kPiece / kDecTile;      // 2 tiles of 64 slots
-constexpr int kTileSmem = kLocTiles * kDecStageBytes;  // K + V of the piece
-constexpr int kPRow = kPiece + 8;                 // padded bf16 row of P
+constexpr int kRound = 128;                       // ring slots per round (2 tiles)
+constexpr int kLocTiles = kRound / kDecTile;      // 2 tiles of 64 slots per round
+constexpr int kRoundSmem = kLocTiles * kDecStageBytes;  // K + V of a round
+constexpr int kPRow = kRound + 8;                 // padded bf16 row of P
 constexpr int kPSmem = kGroup * kPRow * 2;
 constexpr int kAngSmem = 2 * 64 * 8;              // R(-b), R(-b - 2048) per frequency
 constexpr int kRedSmem = 2 * kLocWarps * kGroup * 4;
-constexpr int kConstSmem = 64 * 8 + 64 * 8;       // turns, step of 8 slots
-constexpr int kInboxBytes = (kLocCluster * kD + kLocCluster) * 4;  // o rows, then lse
-constexpr int kOffP = kTileSmem;
-constexpr int kOffAng = kOffP + (kPSmem + 255) / 256 * 256;
-constexpr int kOffRed = kOffAng + kAngSmem;
-constexpr int kOffConst = kOffRed + kRedSmem;
-constexpr int kOffBars = kOffConst + kConstSmem;
-constexpr int kOffInbox = kOffBars + 64;
-constexpr int kLocSmem = kOffInbox + kInboxBytes + 1024;  // + alignment slack
+constexpr int kConstSmem = 3 * 64 * 8;            // turns, step of 8 slots, step of a round
+
+// Shared-memory plan of the kernel whose CTAs take `kRounds` rounds (cluster
+// of 16 / kRounds CTAs): round buffers, P, the R(-b) table, reductions,
+// constants, barriers, then the inbox [heads owned][sources][128] + lse
+// [heads owned][sources].
+template <int kRounds> struct LocPlan {
+  static constexpr int kCl = kLocCluster / kRounds;  // CTAs per cluster
+  static constexpr int kHeadsOwned = kGroup / kCl;   // heads each CTA merges
+  static constexpr int kSlots = kRound * kRounds;    // ring slots per CTA
+  static constexpr int kBufs = kRounds < 2 ? kRounds : 2;
+  static constexpr int kInboxBytes = kHeadsOwned * kCl * (kD + 1) * 4;
+  static constexpr int kOffP = kBufs * kRoundSmem;
+  static constexpr int kOffAng = kOffP + (kPSmem + 255) / 256 * 256;
+  static constexpr int kOffRed = kOffAng + kAngSmem;
+  static constexpr int kOffConst = kOffRed + kRedSmem;
+  static constexpr int kOffBars = kOffConst + kConstSmem;
+  static constexpr int kOffInbox = kOffBars + 64;
+  static constexpr int kSmem = kOffInbox + kInboxBytes + 1024;  // + alignment slack
+};
 
 __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
   return make_float2(a.x * b.x - a.y * b.y, a.y * b.x + a.x * b.y);
@@ -154,72 +172,95 @@ __device__ __forceinline__ void zero4(float (&a)[4]) { a[0] = a[1] = a[2] = a[3]
 
 }  // namespace
 
-// kMinCtas = 2 caps the registers at 128 per thread so that two CTAs share
-// an SM: a 16-CTA cluster then needs 8 SMs of a GPC instead of 16, and
-// twice as many clusters run at once (14 instead of 7 on this B300).  One
-// CTA per SM keeps each cluster's latency chain shortest when the batch's
-// clusters fit in one wave anyway.
-template <int kMinCtas>
-__global__ void __launch_bounds__(kLocThreads, kMinCtas)
+template <int kRounds>
+__global__ void __launch_bounds__(kLocThreads, 1)
     local_attn_kernel(const __grid_constant__ LocalParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv) {
+  using Plan = LocPlan<kRounds>;
+  constexpr int kCl = Plan::kCl, kOwned = Plan::kHeadsOwned, kBufs = Plan::kBufs;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  uint32_t *pmat = reinterpret_cast<uint32_t *>(smem + kOffP);  // [16 rows][kPRow/2] bf16 pairs
-  float2 *ang = reinterpret_cast<float2 *>(smem + kOffAng);    // [2 versions][64]
-  float *red_m = reinterpret_cast<float *>(smem + kOffRed);    // [8 warps][16 rows]
+  uint32_t *pmat = reinterpret_cast<uint32_t *>(smem + Plan::kOffP);  // [16 rows][kPRow/2] bf16 pairs
+  float2 *ang = reinterpret_cast<float2 *>(smem + Plan::kOffAng);    // [2 versions][64]
+  float *red_m = reinterpret_cast<float *>(smem + Plan::kOffRed);    // [8 warps][16 rows]
   float *red_l = red_m + kLocWarps * kGroup;
-  uint64_t *turns = reinterpret_cast<uint64_t *>(smem + kOffConst);
-  float2 *step8 = reinterpret_cast<float2 *>(smem + kOffConst + 64 * 8);
-  float *inbox = reinterpret_cast<float *>(smem + kOffInbox);  // [16 sources][128], lse [16]
+  uint64_t *turns = reinterpret_cast<uint64_t *>(smem + Plan::kOffConst);
+  float2 *step8 = reinterpret_cast<float2 *>(smem + Plan::kOffConst + 64 * 8);
+  float2 *step_round = step8 + 64;                                    // R(128 w_f)
+  float *inbox = reinterpret_cast<float *>(smem + Plan::kOffInbox);  // [owned][sources][128], lse
   const uint32_t smem_base = smem_u32(smem);
-  const uint32_t bar_full = smem_u32(smem + kOffBars);  // 2 tiles
-  const uint32_t bar_inbox = bar_full + 8 * kLocTiles;   // the pushes into this CTA's inbox
+  const uint32_t bar_full = smem_u32(smem + Plan::kOffBars);  // [buffer][tile]
+  const uint32_t bar_inbox = bar_full + 8 * kBufs * kLocTiles; // the pushes into this CTA's inbox
 
   const int g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gr = lane >> 2, tq = lane & 3;
-  const int th = warp >> 2, ws = warp & 3;  // tile and 16-key slice of this warp
+  const int th = warp >> 2, ws = warp & 3;  // tile and 16-key slice of this warp in a round
   const uint32_t my_rank = cluster_rank();
-  const int32_t s0 = static_cast<int32_t>(my_rank) * kPiece;
+  const int32_t s0 = static_cast<int32_t>(my_rank) * Plan::kSlots;  // this CTA's first slot
   const int32_t head = b * kHkv + g;  // (sequence, KV head) index of the cache
   const bool patch_mode = p.k_new != nullptr;  // the token's own row comes from k_new / v_new
+  // the round's two tiles into buffer u % kBufs
+  auto issue_round = [&](int u) {
+    const uint32_t buf = smem_base + (u % kBufs) * kRoundSmem;
+    for (int t = 0; t < kLocTiles; ++t) {
+      const uint32_t dst = buf + t * kDecStageBytes;
+      const uint32_t fb = bar_full + 8 * ((u % kBufs) * kLocTiles + t);
+      const int32_t row = s0 + u * kRound + t * kDecTile;
+      mbar_arrive_expect_tx(fb, kDecStageBytes);
+      tma_load_3d(dst, &tk, fb, 0, row, head);
+      tma_load_3d(dst + 8192, &tk, fb, 64, row, head);
+      tma_load_3d(dst + 16384, &tv, fb, 0, row, head);
+      tma_load_3d(dst + 24576, &tv, fb, 64, row, head);
+    }
+  };
+  auto wait_round = [&](int u, const volatile int *abort) -> bool {
+    bool w = true;
+    for (int t = 0; t < kLocTiles; ++t)
+      w = mbar_wait(bar_full + 8 * ((u % kBufs) * kLocTiles + t), (u / kBufs) & 1, abort) && w;
+    return w;
+  };
 
   // ---- prologue: reads only kernel parameters, so it overlaps the previous
   // kernel under programmatic dependent launch ----
   if (tid == 0) {
     abort_flag = 0;
-    for (int t = 0; t < kLocTiles; ++t) mbar_init(bar_full + 8 * t, 1);
+    for (int t = 0; t < kBufs * kLocTiles; ++t) mbar_init(bar_full + 8 * t, 1);
     mbar_init(bar_inbox, 1);
     fence_mbar_init();
-    // every CTA of the cluster pushes one row and one lse
-    mbar_arrive_expect_tx(bar_inbox, kInboxBytes);
+    // every CTA of the cluster pushes one row and one lse per owned head
+    mbar_arrive_expect_tx(bar_inbox, Plan::kInboxBytes);
   }
   if (tid < 64) {
     turns[tid] = p.turn[tid];
     step8[tid] = p.step[0][tid];
+    if (kRounds > 1) {
+      float cs, sn;
+      rope_cos_sin(kRound, p.turn[tid], cs, sn);
+      step_round[tid] = make_float2(cs, sn);
+    }
   }
   if (tid == 0) {
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
-    for (int t = 0; t < kLocTiles; ++t)
+    for (int t = 0; t < kBufs * kLocTiles; ++t)
       for (int x = 0; x < 2; ++x) {
         tma_prefetch_l2_3d(&tk, 64 * x, s0 + t * kDecTile, head);
         tma_prefetch_l2_3d(&tv, 64 * x, s0 + t * kDecTile, head);
       }
   }
   __syncthreads();
-  // Slot angles R(s w_f) of this thread's 2 keys (slots sb and sb + 8) at
-  // its 16 frequencies: entry 16 sel + f.
-  const int32_t key0 = s0 + th * kDecTile + ws * 16;  // first slot of this warp's 16 keys
-  const int32_t sb = key0 + gr;
+  // Slot angles R(s w_f) of this thread's 2 keys of round 0 (slots sb and
+  // sb + 8) at its 16 frequencies: entry 16 sel + f; each later round's
+  // slots are kRound further on.
+  const int32_t key_in_round = th * kDecTile + ws * 16;  // this warp's first slot in a round
   float2 tab[32];
 #pragma unroll
   for (int f = 0; f < 16; ++f) {
     const int fr = freq_of(f, tq);
-    rope_cos_sin(sb, turns[fr], tab[f].x, tab[f].y);
+    rope_cos_sin(s0 + key_in_round + gr, turns[fr], tab[f].x, tab[f].y);
     tab[16 + f] = cmul(tab[f], step8[fr]);
   }
   // First half of a cluster barrier whose wait (before the first store into
@@ -229,22 +270,13 @@ __global__ void __launch_bounds__(kLocThreads, kMinCtas)
   pdl_launch_dependents();
 
   // The position is loaded first, but nothing below waits for it until the
-  // loads that do not depend on it are in flight: the piece's tiles, the
-  // query and the new row (for an invalid position they are read and then
-  // dropped).
+  // loads that do not depend on it are in flight: the first rounds' tiles,
+  // the query and the new row (for an invalid position they are read and
+  // then dropped).
   const int32_t pq = p.pos[b];
-  if (tid == 0) {  // the piece's two tiles
-    for (int t = 0; t < kLocTiles; ++t) {
-      const uint32_t dst = smem_base + t * kDecStageBytes;
-      const uint32_t fb = bar_full + 8 * t;
-      const int32_t row = s0 + t * kDecTile;
-      mbar_arrive_expect_tx(fb, kDecStageBytes);
-      tma_load_3d(dst, &tk, fb, 0, row, head);
-      tma_load_3d(dst + 8192, &tk, fb, 64, row, head);
-      tma_load_3d(dst + 16384, &tv, fb, 0, row, head);
-      tma_load_3d(dst + 24576, &tv, fb, 64, row, head);
-    }
-  }
+  if (tid == 0)
+    for (int u = 0; u < kBufs; ++u) issue_round(u);
+  int issued = kBufs;  // rounds whose copies went out (thread 0's count)
   // Q fragments (A operand, 16 heads x 128 dims) straight from memory
   uint32_t qf[8][4];
   {
@@ -260,7 +292,7 @@ __global__ void __launch_bounds__(kLocThreads, kMinCtas)
     }
   }
   uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
-  if (patch_mode) {  // the row's address needs no position; only patch_here uses it
+  if (patch_mode) {  // the row's address needs no position; only the owning warp uses it
     const size_t src = (static_cast<size_t>(b) * kHkv + g) * kD;
     new_row = lane < 16 ? __ldg(reinterpret_cast<const uint4 *>(p.k_new + src) + (lane & 15))
                         : __ldg(reinterpret_cast<const uint4 *>(p.v_new + src) + (lane & 15));
@@ -270,7 +302,7 @@ __global__ void __launch_bounds__(kLocThreads, kMinCtas)
   if (bad && my_rank == 0 && g == 0 && tid == 0) set_err(p.err, MG_DERR_POSITION);
   const int32_t n_slots = bad ? 0 : min(pq + 1, kWindow);
   const int32_t bq = pq & (kWindow - 1);  // the query's slot
-  const uint32_t kbase = smem_base + th * kDecStageBytes;
+  const int32_t rounds = s0 >= n_slots ? 0 : min(kRounds, (n_slots - s0 + kRound - 1) / kRound);
   const uint32_t k_row = ws * 16 + ((lane >> 4) << 3) + (lane & 7);
   const uint32_t k_chi = (lane >> 3) & 1;
   const uint32_t v_sub = (((lane >> 3) & 1) << 3) + (lane & 7);
@@ -278,12 +310,13 @@ __global__ void __launch_bounds__(kLocThreads, kMinCtas)
   const uint32_t a_row = ((lane & 7) + 8 * ((lane >> 3) & 1));
   const uint32_t p_addr = smem_u32(pmat) + a_row * (kPRow * 2) + 16 * (lane >> 4);
   bool ok = true;
-  float oacc[2][4];
+  float oacc[2][4];  // running P.V of rows gr / gr + 8, scaled to the running max
   zero4(oacc[0]);
   zero4(oacc[1]);
+  float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;  // running max and sum
   float lse0 = -INFINITY, lse1 = -INFINITY;
 
-  if (s0 < n_slots) {  // CTA-uniform: the piece holds keys of this query
+  if (rounds > 0) {  // CTA-uniform: the piece holds keys of this query
     // R(-b w_f) and R(-(b + 2048) w_f), one per thread
     if (tid < 128) {
       float cs, sn;
@@ -291,27 +324,32 @@ __global__ void __launch_bounds__(kLocThreads, kMinCtas)
       ang[tid] = make_float2(cs, sn);
     }
     consumers_sync();
+  }
+  for (int u = 0; u < rounds; ++u) {
+    const int32_t r0 = s0 + u * kRound;  // first slot of the round
+    const int32_t key0 = r0 + key_in_round;
+    const int32_t sb = key0 + gr;
+    const uint32_t kbase = smem_base + (u % kBufs) * kRoundSmem + th * kDecStageBytes;
     // the keys' offsets from the query: R(d) = R(s) R(-b) (s <= b) or
     // R(s) R(-b - 2048) (s > b)
+    float2 kang[32];
 #pragma unroll
     for (int sel = 0; sel < 2; ++sel) {
       const float2 *a = ang + ((sb + 8 * sel > bq) ? 64 : 0);
 #pragma unroll
-      for (int f = 0; f < 16; ++f) tab[16 * sel + f] = cmul(tab[16 * sel + f], a[freq_of(f, tq)]);
+      for (int f = 0; f < 16; ++f) kang[16 * sel + f] = cmul(tab[16 * sel + f], a[freq_of(f, tq)]);
     }
-
-    // tiles in shared memory
     {
-      bool w = mbar_wait(bar_full, 0, &abort_flag);
-      w = mbar_wait(bar_full + 8, 0, &abort_flag) && w;
-      ok = __all_sync(0xffffffffu, w) && !abort_flag;
-      if (!ok && lane == 0) set_err(p.err, MG_DERR_TIMEOUT);
+      const bool w = wait_round(u, &abort_flag);
+      const bool okw = __all_sync(0xffffffffu, w) && !abort_flag;
+      if (!okw && lane == 0) set_err(p.err, MG_DERR_TIMEOUT);
+      ok = ok && okw;
     }
     // the new token's row replaces the ring row of its slot: lane c writes
     // 16-byte chunk c of K (c < 16) or of V, and decode also stores it in the ring
     const bool patch_here = patch_mode && !bad && bq >= key0 && bq < key0 + 16;
     if (patch_here && ok) {
-      const uint32_t r = static_cast<uint32_t>(bq - s0 - th * kDecTile);
+      const uint32_t r = static_cast<uint32_t>(bq - r0 - th * kDecTile);
       const int c = lane & 15;
       const uint32_t addr = kbase + (lane < 16 ? 0 : 16384) + (c >> 3) * 8192 + sw128(r, c & 7);
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(new_row.x),
@@ -345,7 +383,7 @@ __global__ void __launch_bounds__(kLocThreads, kMinCtas)
 #pragma unroll
           for (int h8 = 0; h8 < 2; ++h8) {
             const int r = 2 * sel + h8, j = 16 * sel + 4 * ks + 2 * h8;
-            rot_split(kx[r], ky[r], tab[j], tab[j + 1], xh[r], xl[r], yh[r], yl[r]);
+            rot_split(kx[r], ky[r], kang[j], kang[j + 1], xh[r], xl[r], yh[r], yl[r]);
           }
         mma_16816(acc[0], qf[ks], xh[0], xh[1]);
         mma_16816(acc[1], qf[ks], xh[2], xh[3]);
@@ -377,13 +415,13 @@ __global__ void __launch_bounds__(kLocThreads, kMinCtas)
       red_m[warp * kGroup + gr + 8] = mx1;
     }
     consumers_sync();
-    float M0 = -INFINITY, M1 = -INFINITY;
+    float Mn0 = M0, Mn1 = M1;  // the running max after this round
 #pragma unroll
     for (int w = 0; w < kLocWarps; ++w) {
-      M0 = fmaxf(M0, red_m[w * kGroup + gr]);
-      M1 = fmaxf(M1, red_m[w * kGroup + gr + 8]);
+      Mn0 = fmaxf(Mn0, red_m[w * kGroup + gr]);
+      Mn1 = fmaxf(Mn1, red_m[w * kGroup + gr + 8]);
     }
-    const float Ms0 = M0 == -INFINITY ? 0.f : M0, Ms1 = M1 == -INFINITY ? 0.f : M1;
+    const float Ms0 = Mn0 == -INFINITY ? 0.f : Mn0, Ms1 = Mn1 == -INFINITY ? 0.f : Mn1;
     float l0 = 0.f, l1 = 0.f;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -391,8 +429,8 @@ __global__ void __launch_bounds__(kLocThreads, kMinCtas)
       const float e2 = fast_exp2(sacc[j][2] - Ms1), e3 = fast_exp2(sacc[j][3] - Ms1);
       l0 += e0 + e1;
       l1 += e2 + e3;
-      // key column in P: the slot's offset in the piece
-      const int kc = th * kDecTile + ws * 16 + 8 * j + 2 * tq;
+      // key column in P: the slot's offset in the round
+      const int kc = key_in_round + 8 * j + 2 * tq;
       pmat[gr * (kPRow / 2) + kc / 2] = pack_bf16x2(e0, e1);
       pmat[(gr + 8) * (kPRow / 2) + kc / 2] = pack_bf16x2(e2, e3);
     }
@@ -405,125 +443,179 @@ __global__ void __launch_bounds__(kLocThreads, kMinCtas)
       red_l[warp * kGroup + gr + 8] = l1;
     }
     consumers_sync();
-    float L0 = 0.f, L1 = 0.f;
+    // rescale what earlier rounds accumulated to the new running max
+    const float a0 = M0 == -INFINITY ? 0.f : fast_exp2(M0 - Ms0);
+    const float a1 = M1 == -INFINITY ? 0.f : fast_exp2(M1 - Ms1);
+    M0 = Mn0;
+    M1 = Mn1;
+    L0 *= a0;
+    L1 *= a1;
 #pragma unroll
     for (int w = 0; w < kLocWarps; ++w) {
       L0 += red_l[w * kGroup + gr];
       L1 += red_l[w * kGroup + gr + 8];
     }
-    // --------------------------------- O[:, 16 w .. 16 w + 16) = P V ----
-    float pacc[2][2][4];  // [k-step parity][n8 tile]
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      zero4(pacc[u][0]);
-      zero4(pacc[u][1]);
+    for (int n = 0; n < 2; ++n) {
+      oacc[n][0] *= a0;
+      oacc[n][1] *= a0;
+      oacc[n][2] *= a1;
+      oacc[n][3] *= a1;
     }
-    constexpr int kKk = kPiece / 16;  // k-steps over the piece's keys
-    uint32_t pa[kKk][4], vb[kKk][4];
+    // --------------------------------- O[:, 16 w .. 16 w + 16) += P V ----
+    {
+      float pacc[2][2][4];  // [k-step parity][n8 tile]
 #pragma unroll
-    for (int kk = 0; kk < kKk; ++kk) {
-      ldsm_x4(p_addr + kk * 32, pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3]);
-      ldsm_x4_t(smem_base + (kk >> 2) * kDecStageBytes + 16384 + (v_chunk >> 3) * 8192 +
-                    sw128(16 * (kk & 3) + v_sub, v_chunk & 7),
-                vb[kk][0], vb[kk][1], vb[kk][2], vb[kk][3]);
-    }
-#pragma unroll
-    for (int kk = 0; kk < kKk; ++kk) {
-      mma_16816(pacc[kk & 1][0], pa[kk], vb[kk][0], vb[kk][1]);
-      mma_16816(pacc[kk & 1][1], pa[kk], vb[kk][2], vb[kk][3]);
-    }
-    if (ok && L0 > 0.f && L1 > 0.f) {
-      const float i0f = 1.f / L0, i1f = 1.f / L1;
-#pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        oacc[n][0] = (pacc[0][n][0] + pacc[1][n][0]) * i0f;
-        oacc[n][1] = (pacc[0][n][1] + pacc[1][n][1]) * i0f;
-        oacc[n][2] = (pacc[0][n][2] + pacc[1][n][2]) * i1f;
-        oacc[n][3] = (pacc[0][n][3] + pacc[1][n][3]) * i1f;
+      for (int v = 0; v < 2; ++v) {
+        zero4(pacc[v][0]);
+        zero4(pacc[v][1]);
       }
-      lse0 = M0 + __log2f(L0);
-      lse1 = M1 + __log2f(L1);
+      constexpr int kKk = kRound / 16;  // k-steps over the round's keys
+      const uint32_t vround = smem_base + (u % kBufs) * kRoundSmem;
+      uint32_t pa[kKk][4], vb[kKk][4];
+#pragma unroll
+      for (int kk = 0; kk < kKk; ++kk) {
+        ldsm_x4(p_addr + kk * 32, pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3]);
+        ldsm_x4_t(vround + (kk >> 2) * kDecStageBytes + 16384 + (v_chunk >> 3) * 8192 +
+                      sw128(16 * (kk & 3) + v_sub, v_chunk & 7),
+                  vb[kk][0], vb[kk][1], vb[kk][2], vb[kk][3]);
+      }
+#pragma unroll
+      for (int kk = 0; kk < kKk; ++kk) {
+        mma_16816(pacc[kk & 1][0], pa[kk], vb[kk][0], vb[kk][1]);
+        mma_16816(pacc[kk & 1][1], pa[kk], vb[kk][2], vb[kk][3]);
+      }
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[n][e] += pacc[0][n][e] + pacc[1][n][e];
     }
-  } else if (tid == 0) {
-    // no keys here: never leave the CTA with copies in flight
-    bool w = mbar_wait(bar_full, 0, nullptr);
-    w = mbar_wait(bar_full + 8, 0, nullptr) && w;
-    if (!w) set_err(p.err, MG_DERR_TIMEOUT);
+    if (kRounds > 1) {
+      // every warp is past its reads of this round's buffer and of P
+      consumers_sync();
+      if (tid == 0 && ok && u + kBufs < rounds) {
+        issue_round(u + kBufs);
+        ++issued;
+      }
+#pragma unroll
+      for (int f = 0; f < 32; ++f) tab[f] = cmul(tab[f], step_round[freq_of(f & 15, tq)]);
+    }
+  }
+  // Never leave the CTA with copies in flight: wait (full limit, no abort)
+  // for the last round issued into each buffer -- a round without keys, or
+  // one the loop gave up on after a timeout; a round already waited for
+  // passes at once.
+  if (tid == 0)
+    for (int u = issued - 1; u >= 0 && u >= issued - kBufs; --u)
+      if (!wait_round(u, nullptr)) set_err(p.err, MG_DERR_TIMEOUT);
+  if (rounds > 0 && ok && L0 > 0.f && L1 > 0.f) {
+    const float i0f = 1.f / L0, i1f = 1.f / L1;
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+      oacc[n][0] *= i0f;
+      oacc[n][1] *= i0f;
+      oacc[n][2] *= i1f;
+      oacc[n][3] *= i1f;
+    }
+    lse0 = M0 + __log2f(L0);
+    lse1 = M1 + __log2f(L1);
+  } else {
+    zero4(oacc[0]);
+    zero4(oacc[1]);
   }
 
   // -------------- push this CTA's partial rows to the CTAs that own them ----
+  // Head h belongs to CTA h / kOwned, which keeps it at inbox row
+  // (h % kOwned) * kCl + source.
   __syncwarp();
   cluster_wait();  // every CTA of the cluster runs, its inbox barrier is set
   {
     const uint32_t inbox_s = smem_u32(inbox);
-    const uint32_t bar0 = map_to_rank(bar_inbox, gr), bar1 = map_to_rank(bar_inbox, gr + 8);
+    const uint32_t own0 = gr / kOwned, own1 = (gr + 8) / kOwned;
+    const uint32_t row0 = (gr % kOwned) * kCl + my_rank, row1 = ((gr + 8) % kOwned) * kCl + my_rank;
+    const uint32_t bar0 = map_to_rank(bar_inbox, own0), bar1 = map_to_rank(bar_inbox, own1);
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
       const int d = 16 * warp + 8 * n + 2 * tq;
-      const uint32_t a = inbox_s + 4 * (my_rank * kD + d);
-      st_async_f32x2(map_to_rank(a, gr), oacc[n][0], oacc[n][1], bar0);
-      st_async_f32x2(map_to_rank(a, gr + 8), oacc[n][2], oacc[n][3], bar1);
+      st_async_f32x2(map_to_rank(inbox_s + 4 * (row0 * kD + d), own0), oacc[n][0], oacc[n][1], bar0);
+      st_async_f32x2(map_to_rank(inbox_s + 4 * (row1 * kD + d), own1), oacc[n][2], oacc[n][3], bar1);
     }
     if (warp == 0 && tq == 0) {
-      const uint32_t a = inbox_s + 4 * (kLocCluster * kD + my_rank);
-      st_async_f32(map_to_rank(a, gr), lse0, bar0);
-      st_async_f32(map_to_rank(a, gr + 8), lse1, bar1);
+      const uint32_t lse_s = inbox_s + 4 * (kOwned * kCl * kD);
+      st_async_f32(map_to_rank(lse_s + 4 * row0, own0), lse0, bar0);
+      st_async_f32(map_to_rank(lse_s + 4 * row1, own1), lse1, bar1);
     }
   }
 
-  // ------------- merge the rows this CTA owns (head my_rank of the group) ----
+  // ---------- merge the rows this CTA owns (heads kOwned * rank + j) ----
   // Every push into this CTA has landed once its inbox barrier completes;
   // the CTA reads and writes no other CTA's memory after its own pushes.
   const bool all_in = mbar_wait_cluster(bar_inbox, 0);
   if (!all_in && tid == 0) set_err(p.err, MG_DERR_TIMEOUT);
-  if (all_in && tid < kD) {
-    const int d = tid;
-    const float *lse = inbox + kLocCluster * kD;
-    float M = -INFINITY;
+  if (all_in) {
+    for (int i = tid; i < kOwned * kD; i += kLocThreads) {
+      const int j = i / kD, d = i % kD;
+      const float *rows = inbox + j * kCl * kD;
+      const float *lse = inbox + kOwned * kCl * kD + j * kCl;
+      float M = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kLocCluster; ++j) M = fmaxf(M, lse[j]);
-    float acc = 0.f, den = 0.f;
-    if (M != -INFINITY) {
+      for (int c = 0; c < kCl; ++c) M = fmaxf(M, lse[c]);
+      float acc = 0.f, den = 0.f;
+      if (M != -INFINITY) {
 #pragma unroll
-      for (int j = 0; j < kLocCluster; ++j) {
-        const float w = lse[j] == -INFINITY ? 0.f : fast_exp2(lse[j] - M);
-        den += w;
-        acc = fmaf(w, inbox[j * kD + d], acc);
+        for (int c = 0; c < kCl; ++c) {
+          const float w = lse[c] == -INFINITY ? 0.f : fast_exp2(lse[c] - M);
+          den += w;
+          acc = fmaf(w, rows[c * kD + d], acc);
+        }
       }
+      const size_t orow = static_cast<size_t>(b) * kHq + g * kGroup + my_rank * kOwned + j;
+      p.o[orow * kD + d] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
     }
-    const size_t orow = static_cast<size_t>(b) * kHq + g * kGroup + my_rank;
-    p.o[orow * kD + d] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
   }
 }
 
-cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtensorMap &tv,
-                              cudaStream_t s) {
-  static_assert(kGroup == kLocCluster, "CTA r of a cluster owns head r of the group");
-  static_assert(kLocSmem <= 227 * 1024, "shared memory");
-  if (p.n != 1 || p.batch < 1) return cudaErrorInvalidValue;
-  // one cluster per (sequence, KV head): up to 7 run at once with one CTA
-  // per SM, 14 with two
-  const bool two = p.batch * kHkv > 7;
-  const void *kern = two ? reinterpret_cast<const void *>(local_attn_kernel<2>)
-                         : reinterpret_cast<const void *>(local_attn_kernel<1>);
-  cudaError_t e = ensure_smem_attr(kern, kLocSmem, two ? 7 : 2);
+namespace {
+
+template <int kRounds>
+cudaError_t launch_local_rounds(const LocalParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                                cudaStream_t s, int kernel_id) {
+  using Plan = LocPlan<kRounds>;
+  static_assert(Plan::kSmem <= 227 * 1024, "shared memory");
+  static_assert(kGroup % Plan::kCl == 0, "the cluster's CTAs share the group's heads evenly");
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(local_attn_kernel<kRounds>),
+                                   Plan::kSmem, kernel_id);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kLocCluster, kHkv, p.batch);
+  cfg.gridDim = dim3(Plan::kCl, kHkv, p.batch);
   cfg.blockDim = dim3(kLocThreads);
-  cfg.dynamicSmemBytes = kLocSmem;
+  cfg.dynamicSmemBytes = Plan::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = kLocCluster;
+  attr[1].val.clusterDim.x = Plan::kCl;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return two ? cudaLaunchKernelEx(&cfg, local_attn_kernel<2>, p, tk, tv)
-             : cudaLaunchKernelEx(&cfg, local_attn_kernel<1>, p, tk, tv);
+  return cudaLaunchKernelEx(&cfg, local_attn_kernel<kRounds>, p, tk, tv);
+}
+
+}  // namespace
+
+cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtensorMap &tv,
+                              cudaStream_t s) {
+  static_assert(kGroup == kLocCluster, "a 16-CTA cluster gives each CTA one head to merge");
+  if (p.n != 1 || p.batch < 1) return cudaErrorInvalidValue;
+  // One cluster per (sequence, KV head).  On this B300 at most 7 clusters of
+  // 16 CTAs run at once (one per GPC), 15 of 8, 33 of 4: the fewest rounds
+  // per CTA that put every pair in one wave.
+  const int pairs = p.batch * kHkv;
+  if (pairs <= 7) return launch_local_rounds<1>(p, tk, tv, s, 2);
+  if (pairs <= 15) return launch_local_rounds<2>(p, tk, tv, s, 7);
+  return launch_local_rounds<4>(p, tk, tv, s, 8);
 }
 
 }  // namespace mg

@@ -121,15 +121,15 @@ bool map_rows(CUtensorMap *m, const void *base, uint64_t rows, uint64_t outer, u
 
 cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id) {
   static std::mutex mu;
-  static uint64_t done[8] = {};  // bit d: set on device d
+  static uint64_t done[16] = {};  // bit d: set on device d
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || kernel_id < 0 || kernel_id >= 8) return cudaErrorInvalidValue;
+  if (dev < 0 || dev >= 64 || kernel_id < 0 || kernel_id >= 16) return cudaErrorInvalidValue;
   std::lock_guard<std::mutex> lk(mu);
   if (done[kernel_id] & (1ull << dev)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && (kernel_id == 2 || kernel_id == 3 || kernel_id == 7))  // 16-CTA clusters
+  if (e == cudaSuccess && (kernel_id == 2 || kernel_id == 3))  // 16-CTA clusters: non-portable size
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[kernel_id] |= 1ull << dev;
   return e;

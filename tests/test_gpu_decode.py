@@ -207,3 +207,82 @@ def test_global_decode_repeats_exactly(mg, B, T):
         p = positions[b]
         ref = orc.attention(olay, k[b, :p + 1], v[b, :p + 1], [p], q[b:b + 1])[0]
         compare(o[b], ref, f"B {B} b {b} p {p}")
+
+
+@pytest.mark.parametrize("B", [4, 9, 16])
+@pytest.mark.parametrize("fused", [False, True])
+def test_local_decode_larger_batches(mg, B, fused):
+    """Local decode with more (sequence, KV head) pairs than one wave of
+    16-CTA clusters holds: clusters of 8 or 4 CTAs walking their ring piece
+    in rounds of 128 slots (online softmax across rounds).  Ragged
+    positions leave some CTAs and rounds without keys and some rounds partly
+    filled; fused=True also appends the token's own row."""
+    positions = [0, 1, 100, 127, 128, 255, 256, 511, 513, 1023, 1024, 2047, 2048, 3000, 4095,
+                 5000][:B]
+    T = max(positions) + 1
+    k, v = synth.history(B, T, 13, 2)
+    q = synth.queries(B, 1, 13, 2)[:, 0]
+    lay = mg.make_layer(0)
+    cache = mg.KVCache(0, B, T)
+    err = mg.error_word()
+    # the ring of each sequence: positions up to p - 1 (fused) or p
+    for b, p in enumerate(positions):
+        top = p if fused else p + 1
+        lo = max(0, top - 2048)
+        if top > lo:
+            one = mg.KVCache(0, 1, T)
+            mg.mg_kv_append(lay, one, torch.tensor([lo], dtype=torch.int32, device="cuda"),
+                            k[b:b + 1, lo:top].cuda().contiguous(), v[b:b + 1, lo:top].cuda().contiguous(),
+                            err)
+            cache.k[b].copy_(one.k[0])
+            cache.v[b].copy_(one.v[0])
+    pos = torch.tensor(positions, dtype=torch.int32, device="cuda")
+    ws = mg.workspace(mg.OP_DECODE, lay, B, 1, T)
+    o = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    if fused:
+        kn = torch.stack([k[b, p:p + 1] for b, p in enumerate(positions)]).cuda().contiguous()
+        vn = torch.stack([v[b, p:p + 1] for b, p in enumerate(positions)]).cuda().contiguous()
+        mg.mg_append_decode(lay, cache, pos, T, q.cuda().contiguous(), kn, vn, o, ws, err)
+    else:
+        mg.mg_attn_decode(lay, cache, pos, T, q.cuda().contiguous(), o, ws, err)
+    torch.cuda.synchronize()
+    check_err(err)
+    olay = orc.layer(orc.LOCAL)
+    for b, p in enumerate(positions):
+        ref = orc.attention(olay, k[b, :p + 1], v[b, :p + 1], [p], q[b:b + 1])[0]
+        compare(o[b], ref, f"B {B} b {b} p {p}")
+    if fused:  # the ring holds each token's own row now
+        for b, p in enumerate(positions):
+            assert torch.equal(cache.k[b, :, p % 2048], k[b, p].cuda())
+            assert torch.equal(cache.v[b, :, p % 2048], v[b, p].cuda())
+
+
+@pytest.mark.parametrize("B,case", [(8, "x40"), (16, "sink")])
+def test_local_decode_rounds_peaked(mg, B, case):
+    """Peaked rows through the multi-round form: queries x40 (the running
+    max moves between rounds), or a sink key in the last round of a CTA's
+    piece (slots 1920..2047 in the 4-CTA clusters' last piece)."""
+    p = 5000
+    k, v = synth.history(B, p + 1, 14, 2)
+    q = synth.queries(B, 1, 14, 2)[:, 0]
+    if case == "x40":
+        q = synth.scaled(q, 40.0)
+    else:
+        sink = p - ((p - 1990) % 2048)  # the position held in ring slot 1990
+        k = synth.plant_sinks(k, [sink])
+        q = synth.sink_queries(q)
+    lay = mg.make_layer(0)
+    cache = mg.KVCache(0, B, p + 1)
+    err = mg.error_word()
+    mg.mg_kv_append(lay, cache, torch.tensor([p - 2047] * B, dtype=torch.int32, device="cuda"),
+                    k[:, p - 2047:].cuda().contiguous(), v[:, p - 2047:].cuda().contiguous(), err)
+    ws = mg.workspace(mg.OP_DECODE, lay, B, 1, p + 1)
+    o = torch.empty((B, 32, 128), dtype=torch.bfloat16, device="cuda")
+    mg.mg_attn_decode(lay, cache, torch.tensor([p] * B, dtype=torch.int32, device="cuda"), p + 1,
+                      q.cuda().contiguous(), o, ws, err)
+    torch.cuda.synchronize()
+    check_err(err)
+    olay = orc.layer(orc.LOCAL)
+    for b in range(B):
+        ref = orc.attention(olay, k[b], v[b], [p], q[b:b + 1])[0]
+        compare(o[b], ref, f"{case} B {B} b {b}")
