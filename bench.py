@@ -905,9 +905,13 @@ def run_gpu(args, rank, world):
 
     # ---------------------------------------------------------------- e2e ----
     # Inputs in pinned host memory; every step copies its inputs in, replays
-    # the captured C-ABI calls, copies its outputs back and waits for them.
-    # Each step's inputs are packed as the device staging buffer lays them
-    # out, so one copy per step brings them in.
+    # the captured C-ABI calls and copies its outputs back to the host.  Each
+    # step's inputs are packed as a device staging buffer lays them out, so
+    # one copy per step brings them in.  Two staging / output buffers (and
+    # one graph over each) let a copy stream bring step j+1's inputs in and
+    # take step j's outputs out while step j+1 computes, as a serving loop
+    # would; every step's copies are inside the timed region, which ends when
+    # the last step's outputs are on the host.
     ee = K
     h_stage = torch.zeros((ee, stage_bytes), dtype=torch.uint8).pin_memory()
     for j, i in enumerate(range(W + K, W + K + ee)):
@@ -915,14 +919,49 @@ def run_gpu(args, rank, world):
         h_stage[j, qb:qb + kvb] = wl.dec_k[i].cpu().contiguous().view(torch.uint8).reshape(-1)
         h_stage[j, qb + kvb:qb + 2 * kvb] = wl.dec_v[i].cpu().contiguous().view(torch.uint8).reshape(-1)
         h_stage[j, qb + 2 * kvb:qb + 2 * kvb + 4] = torch.tensor([PROMPT + i], dtype=torch.int32).view(torch.uint8)
-    h_o = torch.empty((N_LAYERS, 1, 32, 128), dtype=torch.bfloat16).pin_memory()
+    h_o = torch.empty((ee, N_LAYERS, 1, 32, 128), dtype=torch.bfloat16).pin_memory()
+    stage2 = [stage_dev, torch.zeros(stage_bytes, dtype=torch.uint8, device=dev)]
+    out2 = [o_cur, torch.empty_like(o_cur)]
+    graphs2 = [g_dec]
+    with torch.cuda.graph(g2 := torch.cuda.CUDAGraph()):
+        sd = stage2[1]
+        q2 = sd[0:qb].view(torch.bfloat16).view(N_LAYERS, 1, 32, 128)
+        k2 = sd[qb:qb + kvb].view(torch.bfloat16).view(N_LAYERS, 1, 1, 2, 128)
+        v2 = sd[qb + kvb:qb + 2 * kvb].view(torch.bfloat16).view(N_LAYERS, 1, 1, 2, 128)
+        p2 = sd[qb + 2 * kvb:qb + 2 * kvb + 4].view(torch.int32)
+        for l in range(N_LAYERS):
+            mg.mg_append_decode(layers[l], caches[l], p2, cap, q2[l], k2[l], v2[l], out2[1][l],
+                                ws_dec[l], err)
+    graphs2.append(g2)
+    main = torch.cuda.current_stream()
+    copy_s = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_out = [torch.cuda.Event(), torch.cuda.Event()]
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    with torch.cuda.stream(copy_s):
+        stage2[0].copy_(h_stage[0], non_blocking=True)
+        ev_in[0].record(copy_s)
     for j in range(ee):
-        stage_dev.copy_(h_stage[j], non_blocking=True)
-        g_dec.replay()
-        h_o.copy_(o_cur, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        s_ = j % 2
+        if j + 1 < ee:  # the next step's inputs, once step j-1 has released that buffer
+            with torch.cuda.stream(copy_s):
+                if j >= 1:
+                    copy_s.wait_event(ev_done[1 - s_])
+                stage2[1 - s_].copy_(h_stage[j + 1], non_blocking=True)
+                ev_in[1 - s_].record(copy_s)
+        main.wait_event(ev_in[s_])
+        if j >= 2:
+            main.wait_event(ev_out[s_])  # step j-2's outputs have left this buffer
+        graphs2[s_].replay()
+        ev_done[s_].record(main)
+        with torch.cuda.stream(copy_s):
+            copy_s.wait_event(ev_done[s_])
+            h_o[j].copy_(out2[s_], non_blocking=True)
+            ev_out[s_].record(copy_s)
+    copy_s.synchronize()
+    main.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev, world)
     e2e_bytes = sum(decode_layer_bytes(kinds[l], PROMPT + i) for i in range(W + K, W + K + ee)
                     for l in range(N_LAYERS))
