@@ -34,11 +34,18 @@
 //    the last written position.
 //  * Softmax: thread = (row, half of the keys); maxima and sums meet in
 //    shared memory; P goes back to TMEM (bf16) as the A operand of P.V.
-//  * Cluster merge: CTA r owns head r; every CTA stages its normalised rows
-//    and log-sum-exps per owner in shared memory and sends each owner one
-//    bulk copy (cp.async.bulk into the owner's shared memory), whose bytes
-//    complete on the owner's mbarrier; the owner merges the 16 partials per
-//    token.
+//  * Cluster merge: each CTA owns 16 / (cluster size) heads; every CTA
+//    stages its normalised rows and log-sum-exps per head in shared memory
+//    and sends each one bulk copy (cp.async.bulk into the owner's shared
+//    memory), whose bytes complete on the owner's mbarrier; the owner merges
+//    the partials per token.
+//  * Cluster size by batch: at most 7 clusters of 16 CTAs run at once on
+//    this B300 (a 16-CTA cluster takes 16 SMs of one GPC), 15 of 8, 33 of 4.
+//    With more (sequence, KV head, token group) triples than one wave of 16,
+//    the window is cut into 8 or 4 pieces and each CTA walks its piece in
+//    rounds of 128 slots: S of a round in TMEM, an online softmax (running
+//    max; the P.V accumulator in TMEM rescaled when the max moves), the next
+//    round's keys loading while a round's softmax runs and V double-buffered.
 #include "mg_internal.h"
 #include "mg_ptx.cuh"
 
@@ -46,8 +53,8 @@ namespace mg {
 
 namespace {
 
-constexpr int kPiece = kWindow / kLocCluster;  // 128 ring slots per CTA
-constexpr int kBlk = kMaxLocalTokens;          // block rows (first CTA)
+constexpr int kPiece = kWindow / kLocCluster;  // 128 ring slots per round
+constexpr int kBlk = kMaxLocalTokens;          // block rows (first CTA, first round)
 constexpr int kKeysMax = kPiece + kBlk;        // 144
 constexpr int kTpc = kTcPosPerTile;            // 8 tokens = 128 rows per CTA
 constexpr int kThreads = 256;
@@ -55,29 +62,35 @@ constexpr int kBoxBytes = kKeysMax * 128;      // one 64-dim box of 144 key rows
 constexpr int kKVSmem = 2 * kBoxBytes;         // dims 0-63 box, dims 64-127 box
 constexpr int kAngSmem = 2 * 64 * 8;           // R(-b), R(-b - 2048) per frequency
 constexpr int kRedSmem = 4 * kTcRows * 4;      // [half][m, l][row]
-// Inbox of the owning CTA: rows [source][token][128] fp32, then lse
-// [source][8 tokens].  One source's rows for one owner are contiguous, so they
-// travel as one bulk copy.
+// Inbox of an owning CTA: rows [head owned][source][token][128] fp32, then
+// lse [head owned][source][8 tokens] -- 16 (head, source) blocks in all.
+// One source's rows of one head are contiguous: they travel as one bulk copy.
 constexpr int kInboxRows = kLocCluster * kTpc * kD * 4;  // 64 KB
 constexpr int kInboxLse = kLocCluster * kTpc * 4;        // 512 B
-constexpr int kOffK = 0;                       // rotated keys, hi parts
-constexpr int kOffKl = kOffK + kKVSmem;        // rotated keys, lo parts
-constexpr int kOffV = kOffKl + kKVSmem;
-constexpr int kOffAng = kOffV + kKVSmem;
-constexpr int kOffRed = kOffAng + kAngSmem;
-constexpr int kOffTurn = kOffRed + kRedSmem;   // 64 turns (uint64)
-constexpr int kOffW = kOffTurn + 64 * 8;       // merge weights [token][source]
-constexpr int kOffBars = kOffW + kTpc * kLocCluster * 4;
-constexpr int kOffInbox = kOffBars + 64;
-constexpr int kSmem = kOffInbox + kInboxRows + kInboxLse + 1024;  // + alignment slack
-// Staging of this CTA's normalised rows, [owner][token][128] fp32 with the
-// owner blocks 16 bytes apart beyond their size (so that the 32 rows a warp
-// stores at once fall on different banks), and lse [owner][8]: over the key
-// buffers, free once Q.K^T has run.
+// Staging of this CTA's normalised rows, [head][token][128] fp32 with the
+// head blocks 16 bytes apart beyond their size (so that the 32 rows a warp
+// stores at once fall on different banks), and lse [head][8]: over the key
+// buffers, free once the last Q.K^T has run.
 constexpr int kStageOwner = kTpc * kD * 4 + 16;
-constexpr int kOffStage = kOffK;
-constexpr int kOffStageLse = kOffK + kLocCluster * kStageOwner;
 static_assert(kLocCluster * kStageOwner + kInboxLse <= 2 * kKVSmem, "staging fits the key buffers");
+
+template <int kRounds> struct TcLocPlan {
+  static constexpr int kCl = kLocCluster / kRounds;  // CTAs per cluster
+  static constexpr int kOwned = kGroup / kCl;        // heads each CTA merges
+  static constexpr int kVBufs = kRounds > 1 ? 2 : 1;
+  static constexpr int kOffK = 0;                    // rotated keys, hi parts
+  static constexpr int kOffKl = kOffK + kKVSmem;     // rotated keys, lo parts
+  static constexpr int kOffV = kOffKl + kKVSmem;     // V, one buffer per round in flight
+  static constexpr int kOffAng = kOffV + kVBufs * kKVSmem;
+  static constexpr int kOffRed = kOffAng + kAngSmem;
+  static constexpr int kOffTurn = kOffRed + kRedSmem;  // 64 turns (uint64), then R(128 w_f)
+  static constexpr int kOffW = kOffTurn + 64 * 8 + 64 * 8;  // merge weights [head][token][source]
+  static constexpr int kOffBars = kOffW + kLocCluster * kTpc * 4;
+  static constexpr int kOffInbox = kOffBars + 64;
+  static constexpr int kSmem = kOffInbox + kInboxRows + kInboxLse + 1024;  // + alignment slack
+  static constexpr int kOffStage = kOffK;
+  static constexpr int kOffStageLse = kOffK + kLocCluster * kStageOwner;
+};
 // TMEM columns: scores (P as bf16 pairs overwrites their first 72 columns),
 // O, and the rotated queries' hi and lo halves (bf16 pairs, the A operand).
 constexpr uint32_t kColS = 0, kColO = 160, kColQh = 288, kColQl = 352;
@@ -175,23 +188,27 @@ __device__ __forceinline__ void rot8_split(uint4 x8, uint4 y8, const float2 *a, 
 
 }  // namespace
 
+template <int kRounds>
 __global__ void __launch_bounds__(kThreads, 1)
     local_tc_kernel(const __grid_constant__ LocalParams p, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv) {
+  using Plan = TcLocPlan<kRounds>;
+  constexpr int kCl = Plan::kCl, kOwned = Plan::kOwned, kVBufs = Plan::kVBufs;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_slot;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sK = sbase + kOffK, sKl = sbase + kOffKl, sV = sbase + kOffV;
-  float2 *ang = reinterpret_cast<float2 *>(smem + kOffAng);
-  float *red = reinterpret_cast<float *>(smem + kOffRed);
-  float *inbox = reinterpret_cast<float *>(smem + kOffInbox);
-  uint64_t *turns = reinterpret_cast<uint64_t *>(smem + kOffTurn);
-  float *wts = reinterpret_cast<float *>(smem + kOffW);
-  const uint32_t bar_k = sbase + kOffBars, bar_v = bar_k + 8, bar_s = bar_k + 16;
-  const uint32_t bar_o = bar_k + 24, bar_inbox = bar_k + 32;
+  const uint32_t sK = sbase + Plan::kOffK, sKl = sbase + Plan::kOffKl, sV0 = sbase + Plan::kOffV;
+  float2 *ang = reinterpret_cast<float2 *>(smem + Plan::kOffAng);
+  float *red = reinterpret_cast<float *>(smem + Plan::kOffRed);
+  float *inbox = reinterpret_cast<float *>(smem + Plan::kOffInbox);
+  uint64_t *turns = reinterpret_cast<uint64_t *>(smem + Plan::kOffTurn);
+  float2 *step_round = reinterpret_cast<float2 *>(smem + Plan::kOffTurn + 64 * 8);  // R(128 w_f)
+  float *wts = reinterpret_cast<float *>(smem + Plan::kOffW);
+  const uint32_t bar_k = sbase + Plan::kOffBars, bar_s = bar_k + 8, bar_o = bar_k + 16;
+  const uint32_t bar_inbox = bar_k + 24, bar_v = bar_k + 32;  // bar_v: one per V buffer
 
   const int nq = (p.n + kTpc - 1) / kTpc;  // token groups per sequence
   const int g = blockIdx.y, b = blockIdx.z / nq;
@@ -199,26 +216,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cnt = min(kTpc, p.n - i0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t my_rank = cluster_rank();
-  const int32_t s0 = static_cast<int32_t>(my_rank) * kPiece;
+  const int32_t s0 = static_cast<int32_t>(my_rank) * (kPiece * kRounds);  // first slot of the piece
   const int32_t head = b * kHkv + g;
-  const bool blk_here = my_rank == 0;  // the first CTA also scores the block rows
-  const int nkeys = blk_here ? kKeysMax : kPiece;
+  const bool blk_here = my_rank == 0;  // the first CTA also scores the block rows (round 0)
   // thread roles: row r (TMEM lane, also the query row it rotates), half hh
   // of the keys (softmax) and of the query's dims (rotation)
   const int r = 32 * (warp & 3) + lane, hh = warp >> 2;
   const uint32_t lane_bits = static_cast<uint32_t>(32 * (warp & 3)) << 16;
   const int rt = r >> 4;  // token of the row
+  auto issue_k = [&](int u) {  // the round's 128 ring rows of K, raw, into the hi buffer
+    mbar_arrive_expect_tx(bar_k, kPiece * kRowBytes);
+    for (int x = 0; x < 2; ++x) tma_load_3d(sK + x * kBoxBytes, &tk, bar_k, 64 * x, s0 + kPiece * u, head);
+  };
+  auto issue_v = [&](int u) {
+    const uint32_t sv = sV0 + (u % kVBufs) * kKVSmem, bv = bar_v + 8 * (u % kVBufs);
+    mbar_arrive_expect_tx(bv, kPiece * kRowBytes);
+    for (int x = 0; x < 2; ++x) tma_load_3d(sv + x * kBoxBytes, &tv, bv, 64 * x, s0 + kPiece * u, head);
+  };
 
   // ---- prologue: kernel parameters only (overlaps the previous kernel) ----
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(bar_k, 1);
-    mbar_init(bar_v, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
     mbar_init(bar_inbox, 1);
+    for (int i = 0; i < kVBufs; ++i) mbar_init(bar_v + 8 * i, 1);
     fence_mbar_init();
-    // from each CTA: cnt rows and the lse block
+    // from each (head, source) block of the inbox: cnt rows and 8 lse
     mbar_arrive_expect_tx(bar_inbox, kLocCluster * (cnt * kD * 4 + kTpc * 4));
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
@@ -231,11 +256,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tmem_relinquish();
   }
-  if (tid < 64) turns[tid] = p.turn[tid];
+  if (tid < 64) {
+    turns[tid] = p.turn[tid];
+    if (kRounds > 1) {
+      float cs, sn;
+      rope_cos_sin(kPiece, p.turn[tid], cs, sn);
+      step_round[tid] = make_float2(cs, sn);
+    }
+  }
   __syncthreads();
-  // slot angles R(s w_f) of this thread's ring row (krow) at frequencies
-  // 32 kh .. 32 kh + 31, and the query angles R(i w_f) of its query row's
-  // token i at frequencies 32 hh .. 32 hh + 31 (neither needs the position)
+  // slot angles R(s w_f) of this thread's ring row (krow) of round 0 at
+  // frequencies 32 kh .. 32 kh + 31, and the query angles R(i w_f) of its
+  // query row's token i at frequencies 32 hh .. 32 hh + 31 (neither needs
+  // the position)
   const int krow = tid >> 1, kh = tid & 1;
   float2 kang[32], qang[32];
 #pragma unroll
@@ -252,18 +285,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
 
   // The position is loaded first, but nothing waits for it until the loads
-  // that do not depend on it are in flight: the piece's tiles, the raw
+  // that do not depend on it are in flight: the first rounds' tiles, the raw
   // queries and the block's rows (for an invalid position they are read and
   // then dropped).
   const int32_t p0 = p.pos[b];
-  if (tid == 0) {  // the piece's 128 K and V rows
-    mbar_arrive_expect_tx(bar_k, kPiece * kRowBytes);
-    mbar_arrive_expect_tx(bar_v, kPiece * kRowBytes);
-    for (int x = 0; x < 2; ++x) {
-      tma_load_3d(sK + x * kBoxBytes, &tk, bar_k, 64 * x, s0, head);
-      tma_load_3d(sV + x * kBoxBytes, &tv, bar_v, 64 * x, s0, head);
-    }
+  if (tid == 0) {
+    issue_k(0);
+    for (int u = 0; u < kVBufs; ++u) issue_v(u);
   }
+  int issued_k = 1, issued_v = kVBufs;  // (thread 0's counts)
   // raw query of row r, dims 32 hh.. and 64 + 32 hh..
   uint4 qx[4], qy[4];
   {
@@ -332,154 +362,206 @@ __global__ void __launch_bounds__(kThreads, 1)
     sts128(sK + kBoxBytes + o, yh);
     sts128(sKl + o, xl);
     sts128(sKl + kBoxBytes + o, yl);
-    sts128(sV + o, vx);
-    sts128(sV + kBoxBytes + o, vy);
+    sts128(sV0 + o, vx);  // the first round's V buffer
+    sts128(sV0 + kBoxBytes + o, vy);
   }
   __syncthreads();  // R(-b) tables ready
-  // this thread's ring row: R(d) = R(s) R(-b) (s < b) or R(s) R(-b - 2048)
-  {
-    const float2 *a = ang + ((s0 + krow > b0) ? 64 : 0) + 32 * kh;
-#pragma unroll
-    for (int f = 0; f < 32; ++f) kang[f] = cmul(kang[f], a[f]);
-  }
-  // ring keys: once the tile has landed, rotate each row and split it
-  bool ok = mbar_wait(bar_k, 0, &abort_flag);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int cc = 4 * kh + c;
-    const uint32_t o = swz(krow, cc);
-    uint4 xh, xl, yh, yl;
-    rot8_split(lds128(sK + o), lds128(sK + kBoxBytes + o), kang + 8 * c, xh, xl, yh, yl);
-    sts128(sK + o, xh);
-    sts128(sK + kBoxBytes + o, yh);
-    sts128(sKl + o, xl);
-    sts128(sKl + kBoxBytes + o, yl);
-  }
-  fence_proxy_async_smem();  // the tensor core reads what the threads wrote
-  tmem_wait_st();
-  tc_fence_before();
-  __syncthreads();
 
-  // --------------------------------- S = Qh Kh^T + Qh Kl^T + Ql Kh^T ----
-  if (tid == 0) {
-    tc_fence_after();
-    const uint32_t idq = idesc_bf16_f32(128, nkeys, 0, 0);
-#pragma unroll
-    for (int part = 0; part < 3; ++part) {
-      const uint32_t qa = tbase + (part == 2 ? kColQl : kColQh);
-      const uint32_t kb = part == 1 ? sKl : sK;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t ok_ = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-        mma_ts(tbase + kColS, qa + 8 * kk, smem_desc_sw128(kb + ok_, 16, 1024), idq,
-               (part > 0 || kk > 0) ? 1u : 0u);
-      }
-    }
-    mma_commit(bar_s);
-  }
-
-  // -------------------------------------------------------------- softmax ----
-  // thread: row r, half hh of the keys (0: keys 0..63; 1: keys 64..127 and
-  // the block keys 128..143)
+  // ------------------------------------------------------------- rounds ----
   const bool row_live = rt < cnt && !bad;
   const int32_t ri = i0 + rt;                  // token index in the block
   const int32_t rp = p0 + ri;                  // its position
   const int32_t rn = min(rp + 1, kWindow);     // slots holding positions
-  ok = __all_sync(0xffffffffu, mbar_wait(bar_s, 0, &abort_flag) && ok);
-  tc_fence_after();
   const float sl2 = p.scale_log2;
-  float sv[80];  // this thread's scores (scaled, masked)
-  float mx = -INFINITY;
+  bool ok = true;
+  float m_run = -INFINITY, l_half = 0.f;  // running max (same in both halves), this half's sum
+  for (int u = 0; u < kRounds; ++u) {
+    const int32_t rs0 = s0 + kPiece * u;           // first slot of the round
+    const bool blk_round = blk_here && u == 0;
+    const int nkeys = blk_round ? kKeysMax : kPiece;
+    // ring keys: once the round's tile has landed, rotate this thread's row
+    // by R(s) R(-b) or R(s) R(-b - 2048) and split it
+    {
+      float2 a[32];
+      const float2 *ab = ang + ((rs0 + krow > b0) ? 64 : 0) + 32 * kh;
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {  // ring keys 64 hh + 32 c ..
-    const int j0 = 64 * hh + 32 * c;
-    uint32_t sc[32];
-    tmem_ld32(tbase + lane_bits + kColS + j0, sc);
-    tmem_wait_ld();
+      for (int f = 0; f < 32; ++f) a[f] = cmul(kang[f], ab[f]);
+      ok = mbar_wait(bar_k, u & 1, &abort_flag) && ok;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int32_t s = s0 + j0 + j;
-      const bool stale = ((s - p0) & (kWindow - 1)) <= ri;  // a block token takes this slot
-      const bool valid = row_live && s < rn && !stale;
-      sv[32 * c + j] = valid ? __uint_as_float(sc[j]) * sl2 : -INFINITY;
-      mx = fmaxf(mx, sv[32 * c + j]);
+      for (int c = 0; c < 4; ++c) {
+        const int cc = 4 * kh + c;
+        const uint32_t o = swz(krow, cc);
+        uint4 xh, xl, yh, yl;
+        rot8_split(lds128(sK + o), lds128(sK + kBoxBytes + o), a + 8 * c, xh, xl, yh, yl);
+        sts128(sK + o, xh);
+        sts128(sK + kBoxBytes + o, yh);
+        sts128(sKl + o, xl);
+        sts128(sKl + kBoxBytes + o, yl);
+      }
+      if (kRounds > 1)
+#pragma unroll
+        for (int f = 0; f < 32; ++f) kang[f] = cmul(kang[f], step_round[32 * kh + f]);
     }
-  }
-  if (hh == 1) {
+    fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+    tc_fence_before();
+    __syncthreads();
+
+    // ------------------------------- S = Qh Kh^T + Qh Kl^T + Ql Kh^T ----
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t idq = idesc_bf16_f32(128, nkeys, 0, 0);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) sv[64 + j] = -INFINITY;
-    if (blk_here) {  // block keys k = 0..15
-      uint32_t sc[16];
-      tmem_ld16(tbase + lane_bits + kColS + kPiece, sc);
+      for (int part = 0; part < 3; ++part) {
+        const uint32_t qa = tbase + (part == 2 ? kColQl : kColQh);
+        const uint32_t kb = part == 1 ? sKl : sK;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t ok_ = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ts(tbase + kColS, qa + 8 * kk, smem_desc_sw128(kb + ok_, 16, 1024), idq,
+                 (part > 0 || kk > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(bar_s);
+    }
+    ok = __all_sync(0xffffffffu, mbar_wait(bar_s, u & 1, &abort_flag) && ok);
+    tc_fence_after();
+    if (tid == 0 && u + 1 < kRounds) {  // the key buffer is free: the next round's keys
+      issue_k(u + 1);
+      ++issued_k;
+    }
+
+    // ------------------------------------------------------ softmax ----
+    // thread: row r, half hh of the keys (0: keys 0..63; 1: keys 64..127
+    // and, in the first CTA's first round, the block keys 128..143)
+    float sv[80];  // this thread's scores (scaled, masked)
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {  // ring keys 64 hh + 32 c ..
+      const int j0 = 64 * hh + 32 * c;
+      uint32_t sc[32];
+      tmem_ld32(tbase + lane_bits + kColS + j0, sc);
       tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        sv[64 + k] = (row_live && k <= ri) ? __uint_as_float(sc[k]) * sl2 : -INFINITY;
-        mx = fmaxf(mx, sv[64 + k]);
+      for (int j = 0; j < 32; ++j) {
+        const int32_t sl = rs0 + j0 + j;
+        const bool stale = ((sl - p0) & (kWindow - 1)) <= ri;  // a block token takes this slot
+        const bool valid = row_live && sl < rn && !stale;
+        sv[32 * c + j] = valid ? __uint_as_float(sc[j]) * sl2 : -INFINITY;
+        mx = fmaxf(mx, sv[32 * c + j]);
       }
     }
-  }
-  red[(2 * hh + 0) * kTcRows + r] = mx;
-  __syncthreads();  // every S value is read before P overwrites it
-  const float M = fmaxf(red[0 * kTcRows + r], red[2 * kTcRows + r]);
-  const float Ms = M == -INFINITY ? 0.f : M;
-  float l = 0.f;
+    if (hh == 1) {
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {  // P of ring keys 64 hh + 32 c .. : TMEM columns 32 hh + 16 c ..
-    uint32_t pk[16];
+      for (int j = 0; j < 16; ++j) sv[64 + j] = -INFINITY;
+      if (blk_round) {  // block keys k = 0..15
+        uint32_t sc[16];
+        tmem_ld16(tbase + lane_bits + kColS + kPiece, sc);
+        tmem_wait_ld();
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const float e0 = fast_exp2(sv[32 * c + j] - Ms), e1 = fast_exp2(sv[32 * c + j + 1] - Ms);
-      l += e0 + e1;
-      pk[j >> 1] = pack_bf16x2(e0, e1);
+        for (int k = 0; k < 16; ++k) {
+          sv[64 + k] = (row_live && k <= ri) ? __uint_as_float(sc[k]) * sl2 : -INFINITY;
+          mx = fmaxf(mx, sv[64 + k]);
+        }
+      }
     }
-    tmem_st16(tbase + lane_bits + kColS + 32 * hh + 16 * c, pk);
-  }
-  if (hh == 1 && blk_here) {  // block keys: columns 64..71
-    uint32_t pk[8];
+    red[(2 * hh + 0) * kTcRows + r] = mx;
+    __syncthreads();  // every S value is read before P overwrites it
+    const float m_new = fmaxf(m_run, fmaxf(red[0 * kTcRows + r], red[2 * kTcRows + r]));
+    const float Ms = m_new == -INFINITY ? 0.f : m_new;
+    const float alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - Ms);
+    m_run = m_new;
+    float l = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; k += 2) {
-      const float e0 = fast_exp2(sv[64 + k] - Ms), e1 = fast_exp2(sv[64 + k + 1] - Ms);
-      l += e0 + e1;
-      pk[k >> 1] = pack_bf16x2(e0, e1);
+    for (int c = 0; c < 2; ++c) {  // P of ring keys 64 hh + 32 c .. : TMEM columns 32 hh + 16 c ..
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float e0 = fast_exp2(sv[32 * c + j] - Ms), e1 = fast_exp2(sv[32 * c + j + 1] - Ms);
+        l += e0 + e1;
+        pk[j >> 1] = pack_bf16x2(e0, e1);
+      }
+      tmem_st16(tbase + lane_bits + kColS + 32 * hh + 16 * c, pk);
     }
-    tmem_st8(tbase + lane_bits + kColS + kPiece / 2, pk);
+    if (hh == 1 && blk_round) {  // block keys: columns 64..71
+      uint32_t pk[8];
+#pragma unroll
+      for (int k = 0; k < 16; k += 2) {
+        const float e0 = fast_exp2(sv[64 + k] - Ms), e1 = fast_exp2(sv[64 + k + 1] - Ms);
+        l += e0 + e1;
+        pk[k >> 1] = pack_bf16x2(e0, e1);
+      }
+      tmem_st8(tbase + lane_bits + kColS + kPiece / 2, pk);
+    }
+    l_half = l_half * alpha + l;
+    if (u > 0) {
+      // the previous round's P.V has retired: rescale this half's 64
+      // columns of O to the new running max, and the V buffer it read is free
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (u - 1) & 1, &abort_flag) && ok);
+      tc_fence_after();
+      if (tid == 0 && u + 1 < kRounds) {
+        issue_v(u + 1);
+        ++issued_v;
+      }
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t o32[32];
+          tmem_ld32(tbase + lane_bits + kColO + 64 * hh + 32 * c, o32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o32[j] = __float_as_uint(__uint_as_float(o32[j]) * alpha);
+          tmem_st32(tbase + lane_bits + kColO + 64 * hh + 32 * c, o32);
+        }
+      }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+
+    // ------------------------------------------------------ O += P V ----
+    if (tid == 0) {
+      ok = mbar_wait(bar_v + 8 * (u % kVBufs), (u / kVBufs) & 1, &abort_flag) && ok;
+      tc_fence_after();
+      const uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
+      const uint32_t sv_ = sV0 + (u % kVBufs) * kKVSmem;
+      for (int kk = 0; kk < nkeys / 16; ++kk)
+        mma_ts(tbase + kColO, tbase + kColS + 8 * kk,
+               smem_desc_sw128(sv_ + kk * 2048, kBoxBytes, 1024), idv, (u > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(bar_o);
+    }
   }
-  red[(2 * hh + 1) * kTcRows + r] = l;
-  tmem_wait_st();
-  tc_fence_before();
+  ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (kRounds - 1) & 1, &abort_flag) && ok && !abort_flag);
+  if (!ok && lane == 0) set_err(p.err, MG_DERR_TIMEOUT);
+  if (tid == 0) {
+    // Never leave TMEM or shared memory to work still in flight (after a
+    // timeout some of it was not waited for): the last MMAs, and the last
+    // copies issued into each buffer, with the full wait limit.
+    bool w = mbar_wait(bar_o, (kRounds - 1) & 1, nullptr);
+    w = mbar_wait(bar_k, (issued_k - 1) & 1, nullptr) && w;
+    for (int u = issued_v - 1; u >= 0 && u >= issued_v - kVBufs; --u)
+      w = mbar_wait(bar_v + 8 * (u % kVBufs), (u / kVBufs) & 1, nullptr) && w;
+    if (!w) set_err(p.err, MG_DERR_TIMEOUT);
+  }
+  tc_fence_after();
+  red[(2 * hh + 1) * kTcRows + r] = l_half;
   __syncthreads();
   const float L = red[1 * kTcRows + r] + red[3 * kTcRows + r];
 
-  // ------------------------------------------------------------- O = P V ----
-  if (tid == 0) {
-    ok = mbar_wait(bar_v, 0, &abort_flag) && ok;
-    tc_fence_after();
-    const uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
-    for (int kk = 0; kk < nkeys / 16; ++kk)
-      mma_ts(tbase + kColO, tbase + kColS + 8 * kk,
-             smem_desc_sw128(sV + kk * 2048, kBoxBytes, 1024), idv, kk > 0 ? 1u : 0u);
-    mma_commit(bar_o);
-  }
-  ok = __all_sync(0xffffffffu, mbar_wait(bar_o, 0, &abort_flag) && ok && !abort_flag);
-  if (!ok && lane == 0) set_err(p.err, MG_DERR_TIMEOUT);
-  tc_fence_after();
-
   // ---------------- send this CTA's normalised rows to the owning CTAs ----
-  // Stage [owner = head][token][128] and lse [owner][8] over the key
-  // buffers (every MMA has retired), then one bulk copy per owner.
+  // Stage [head][token][128] and lse [head][8] over the key buffers (every
+  // MMA has retired), then one bulk copy per head.
   const bool have = ok && row_live && L > 0.f;
   const float inv = have ? 1.f / L : 0.f;
-  const int owner = r & 15;
-  float *stage = reinterpret_cast<float *>(smem + kOffStage);
-  float *stage_lse = reinterpret_cast<float *>(smem + kOffStageLse);
+  const int hd = r & 15;
+  float *stage = reinterpret_cast<float *>(smem + Plan::kOffStage);
+  float *stage_lse = reinterpret_cast<float *>(smem + Plan::kOffStageLse);
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const int d0 = 64 * hh + 32 * c;
     uint32_t ov[32];
     tmem_ld32(tbase + lane_bits + kColO + d0, ov);
     tmem_wait_ld();
-    float4 *dst = reinterpret_cast<float4 *>(stage + (owner * kStageOwner) / 4 + rt * kD + d0);
+    float4 *dst = reinterpret_cast<float4 *>(stage + (hd * kStageOwner) / 4 + rt * kD + d0);
 #pragma unroll
     for (int j = 0; j < 32; j += 4)
       dst[j / 4] = make_float4(have ? __uint_as_float(ov[j]) * inv : 0.f,
@@ -487,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                have ? __uint_as_float(ov[j + 2]) * inv : 0.f,
                                have ? __uint_as_float(ov[j + 3]) * inv : 0.f);
   }
-  if (hh == 0) stage_lse[owner * kTpc + rt] = have ? M + __log2f(L) : -INFINITY;
+  if (hh == 0) stage_lse[hd * kTpc + rt] = have ? m_run + __log2f(L) : -INFINITY;
   fence_proxy_async_smem();  // the bulk copies read what the threads wrote
   tc_fence_before();
   __syncthreads();  // staging complete; TMEM reads done
@@ -496,72 +578,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tbase, 512);
   }
   cluster_wait();  // every CTA of the cluster runs, its inbox barrier is set
-  if (tid < kLocCluster) {  // thread h sends owner h its rows and lse
-    const uint32_t own = static_cast<uint32_t>(tid);
+  if (tid < kLocCluster) {  // thread h sends head h's rows and lse to its owner
+    const uint32_t h = static_cast<uint32_t>(tid);
+    const uint32_t own = h / kOwned, blk = (h % kOwned) * kCl + my_rank;  // (head owned, source)
     const uint32_t inbox_s = smem_u32(inbox);
     const uint32_t obar = map_to_rank(bar_inbox, own);
-    bulk_to_cta(map_to_rank(inbox_s + my_rank * (kTpc * kD * 4), own),
-                sbase + kOffStage + own * kStageOwner, cnt * kD * 4, obar);
-    bulk_to_cta(map_to_rank(inbox_s + kInboxRows + my_rank * (kTpc * 4), own),
-                sbase + kOffStageLse + own * (kTpc * 4), kTpc * 4, obar);
+    bulk_to_cta(map_to_rank(inbox_s + blk * (kTpc * kD * 4), own),
+                sbase + Plan::kOffStage + h * kStageOwner, cnt * kD * 4, obar);
+    bulk_to_cta(map_to_rank(inbox_s + kInboxRows + blk * (kTpc * 4), own),
+                sbase + Plan::kOffStageLse + h * (kTpc * 4), kTpc * 4, obar);
     bulk_commit_wait_read();  // the staging is not reused, but copies finish reading first
   }
 
-  // ------------- merge the rows this CTA owns (head my_rank of the group) ----
+  // -- merge the rows this CTA owns (heads kOwned * rank + j of the group) ----
   // (CTA-uniform: the block below has a barrier)
   const bool all_in = __syncthreads_and(mbar_wait_cluster(bar_inbox, 0));
   if (!all_in && tid == 0) set_err(p.err, MG_DERR_TIMEOUT);
   if (all_in) {
-    const float *lse = inbox + kInboxRows / 4;  // [source][8]
-    if (tid < cnt * kLocCluster) {  // weight of source j for token t, normalised
-      const int t = tid >> 4, j = tid & 15;
+    const float *lse = inbox + kInboxRows / 4;  // [head owned][source][8]
+    for (int i = tid; i < kOwned * cnt * kCl; i += kThreads) {  // weights, normalised
+      const int j = i / (cnt * kCl), t = (i / kCl) % cnt, c = i % kCl;
+      const float *lj = lse + j * kCl * kTpc;
       float Mx = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < kLocCluster; ++k) Mx = fmaxf(Mx, lse[k * kTpc + t]);
+      for (int k = 0; k < kCl; ++k) Mx = fmaxf(Mx, lj[k * kTpc + t]);
       float den = 0.f;
 #pragma unroll
-      for (int k = 0; k < kLocCluster; ++k)
-        den += (Mx == -INFINITY || lse[k * kTpc + t] == -INFINITY) ? 0.f : fast_exp2(lse[k * kTpc + t] - Mx);
-      const float mine = lse[j * kTpc + t];
-      wts[t * kLocCluster + j] =
+      for (int k = 0; k < kCl; ++k)
+        den += (Mx == -INFINITY || lj[k * kTpc + t] == -INFINITY) ? 0.f : fast_exp2(lj[k * kTpc + t] - Mx);
+      const float mine = lj[c * kTpc + t];
+      wts[(j * kTpc + t) * kCl + c] =
           (den > 0.f && mine != -INFINITY) ? fast_exp2(mine - Mx) / den : 0.f;
     }
     __syncthreads();
-    const int d = tid & (kD - 1);
-    for (int t = tid >> 7; t < cnt; t += kThreads / kD) {
+    for (int i = tid; i < kOwned * cnt * kD; i += kThreads) {
+      const int j = i / (cnt * kD), t = (i / kD) % cnt, d = i % kD;
       float acc = 0.f;
 #pragma unroll
-      for (int j = 0; j < kLocCluster; ++j)
-        acc = fmaf(wts[t * kLocCluster + j], inbox[(j * kTpc + t) * kD + d], acc);
-      const size_t orow = (static_cast<size_t>(b) * p.n + i0 + t) * kHq + g * kGroup + my_rank;
+      for (int c = 0; c < kCl; ++c)
+        acc = fmaf(wts[(j * kTpc + t) * kCl + c], inbox[((j * kCl + c) * kTpc + t) * kD + d], acc);
+      const size_t orow = (static_cast<size_t>(b) * p.n + i0 + t) * kHq + g * kGroup + my_rank * kOwned + j;
       p.o[orow * kD + d] = __float2bfloat16_rn(acc);
     }
   }
 }
 
-cudaError_t launch_local_tc(const LocalParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                            cudaStream_t s) {
-  static_assert(kGroup == kLocCluster, "CTA r of a cluster owns head r of the group");
-  static_assert(kSmem <= 227 * 1024, "shared memory");
-  if (p.n < 1 || p.n > kMaxLocalTokens || p.batch < 1 || p.k_new == nullptr)
-    return cudaErrorInvalidValue;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(local_tc_kernel), kSmem, 3);
+namespace {
+
+template <int kRounds>
+cudaError_t launch_local_tc_rounds(const LocalParams &p, const CUtensorMap &tk,
+                                   const CUtensorMap &tv, cudaStream_t s, int kernel_id) {
+  using Plan = TcLocPlan<kRounds>;
+  static_assert(Plan::kSmem <= 227 * 1024, "shared memory");
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(local_tc_kernel<kRounds>),
+                                   Plan::kSmem, kernel_id);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kLocCluster, kHkv, p.batch * ((p.n + kTpc - 1) / kTpc));
+  cfg.gridDim = dim3(Plan::kCl, kHkv, p.batch * ((p.n + kTpc - 1) / kTpc));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = Plan::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = kLocCluster;
+  attr[1].val.clusterDim.x = Plan::kCl;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, local_tc_kernel, p, tk, tv);
+  return cudaLaunchKernelEx(&cfg, local_tc_kernel<kRounds>, p, tk, tv);
+}
+
+}  // namespace
+
+cudaError_t launch_local_tc(const LocalParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                            cudaStream_t s) {
+  static_assert(kGroup == kLocCluster, "a 16-CTA cluster gives each CTA one head to merge");
+  if (p.n < 1 || p.n > kMaxLocalTokens || p.batch < 1 || p.k_new == nullptr)
+    return cudaErrorInvalidValue;
+  // One cluster per (sequence, KV head, group of 8 tokens).  On this B300 at
+  // most 7 clusters of 16 CTAs run at once, 15 of 8, 33 of 4: the fewest
+  // rounds per CTA that put every triple in one wave.
+  const int triples = p.batch * kHkv * ((p.n + kTpc - 1) / kTpc);
+  if (triples <= 7) return launch_local_tc_rounds<1>(p, tk, tv, s, 3);
+  if (triples <= 15) return launch_local_tc_rounds<2>(p, tk, tv, s, 9);
+  return launch_local_tc_rounds<4>(p, tk, tv, s, 10);
 }
 
 }  // namespace mg

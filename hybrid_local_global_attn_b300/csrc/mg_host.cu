@@ -129,7 +129,7 @@ cudaError_t ensure_smem_attr(const void *kernel, int bytes, int kernel_id) {
   std::lock_guard<std::mutex> lk(mu);
   if (done[kernel_id] & (1ull << dev)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && (kernel_id == 2 || kernel_id == 3))  // 16-CTA clusters: non-portable size
+  if (e == cudaSuccess && (kernel_id == 2 || kernel_id == 3))  // 16-CTA clusters: a non-portable size
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done[kernel_id] |= 1ull << dev;
   return e;

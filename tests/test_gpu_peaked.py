@@ -205,3 +205,22 @@ def test_prefill_sink_keys(mg, kind, T, chunk, sinks):
     k = synth.plant_sinks(k, sinks, values=[synth.SINK_K, 1.5 * synth.SINK_K])
     q = synth.sink_queries(synth.queries(1, T, 46, li))
     prefill_case(mg, kind, k, v, q, chunk)
+
+
+@pytest.mark.parametrize("case", ["x40", "sink"])
+def test_local_verify_rounds_peaked(mg, case):
+    """A local verify batch large enough for the 4-CTA clusters whose CTAs
+    walk their ring piece in rounds (8 sequences x 2 KV heads x 2 token
+    groups), with queries x40 or a sink key held in a CTA's last round
+    (ring slot 1990)."""
+    B, n = 8, 16
+    p0s = [5000 + 37 * b for b in range(B)]
+    k, v = synth.history(B, max(p0s) + n, 47, 2)
+    q = synth.queries(B, n, 47, 2)
+    if case == "x40":
+        q = synth.scaled(q, 40.0)
+    else:
+        for b, p0 in enumerate(p0s):  # the position each sequence's ring holds in slot 1990
+            k = synth.plant_sinks(k, [(p0 - 1) - ((p0 - 1 - 1990) % 2048)], seq=b)
+        q = synth.sink_queries(q)
+    verify_case(mg, 0, k, v, q, p0s, n)
