@@ -403,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int f = 0; f < 32; ++f) kang[f] = cmul(kang[f], step_round[32 * kh + f]);
     }
     fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+    if (u == 0) tmem_wait_st();  // and the rotated queries are in TMEM
     tc_fence_before();
     __syncthreads();
 
@@ -493,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st8(tbase + lane_bits + kColS + kPiece / 2, pk);
     }
     l_half = l_half * alpha + l;
+    if (u + 1 == kRounds) red[(2 * hh + 1) * kTcRows + r] = l_half;  // read after the P.V barrier
     if (u > 0) {
       // the previous round's P.V has retired: rescale this half's 64
       // columns of O to the new running max, and the V buffer it read is free
@@ -543,8 +545,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!w) set_err(p.err, MG_DERR_TIMEOUT);
   }
   tc_fence_after();
-  red[(2 * hh + 1) * kTcRows + r] = l_half;
-  __syncthreads();
   const float L = red[1 * kTcRows + r] + red[3 * kTcRows + r];
 
   // ---------------- send this CTA's normalised rows to the owning CTAs ----
@@ -596,8 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!all_in && tid == 0) set_err(p.err, MG_DERR_TIMEOUT);
   if (all_in) {
     const float *lse = inbox + kInboxRows / 4;  // [head owned][source][8]
-    for (int i = tid; i < kOwned * cnt * kCl; i += kThreads) {  // weights, normalised
-      const int j = i / (cnt * kCl), t = (i / kCl) % cnt, c = i % kCl;
+    for (int i = tid; i < kOwned * kTpc * kCl; i += kThreads) {  // weights, normalised
+      const int j = i / (kTpc * kCl), t = (i / kCl) % kTpc, c = i % kCl;
+      if (t >= cnt) continue;
       const float *lj = lse + j * kCl * kTpc;
       float Mx = -INFINITY;
 #pragma unroll
@@ -611,8 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           (den > 0.f && mine != -INFINITY) ? fast_exp2(mine - Mx) / den : 0.f;
     }
     __syncthreads();
-    for (int i = tid; i < kOwned * cnt * kD; i += kThreads) {
-      const int j = i / (cnt * kD), t = (i / kD) % cnt, d = i % kD;
+    const int d = tid & (kD - 1);
+    for (int i = tid >> 7; i < kOwned * kTpc; i += kThreads / kD) {
+      const int j = i / kTpc, t = i % kTpc;
+      if (t >= cnt) continue;
       float acc = 0.f;
 #pragma unroll
       for (int c = 0; c < kCl; ++c)
