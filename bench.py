@@ -383,20 +383,21 @@ def leg_pr1(wl, P0=2000, steps=256):
                 mg.mg_kv_append(layers[j], caches[j], pos[i:i + 1], kn[i, j], vn[i, j], err)
                 mg.mg_attn_decode(layers[j], caches[j], pos[i:i + 1], T, q[i, j], o[i, j], ws[j], err)
 
-    def fused():
+    def fused(early=False):
         for i in range(steps):
             for j in range(2):
-                mg.mg_append_decode(layers[j], caches[j], pos[i:i + 1], T, q[i, j], kn[i, j],
-                                    vn[i, j], o[i, j], ws[j], err)
+                append_decode(early, layers[j], caches[j], pos[i:i + 1], T, q[i, j], kn[i, j],
+                              vn[i, j], o[i, j], ws[j], err)
 
     us_sep = _graph_us(separate, reps=5, calls=steps)
     us_fused = _graph_us(fused, reps=5, calls=steps)
+    us_early = _graph_us(lambda: fused(True), reps=5, calls=steps)
     nbytes = sum(decode_layer_bytes(k, p) for p in range(P0, T) for k in kinds) / steps
     assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after PR1"
     del caches, ws, q, kn, vn, o
     torch.cuda.empty_cache()
     return {"positions": [P0, T - 1], "us_per_step_append_then_decode": us_sep,
-            "us_per_step_fused": us_fused, "bytes_per_step": nbytes,
+            "us_per_step_fused": us_fused, "us_per_step_fused_early": us_early, "bytes_per_step": nbytes,
             "gbs_fused": nbytes / us_fused / 1e3}
 
 
@@ -539,6 +540,16 @@ def leg_verify(wl):
             "global_layer_gbs": verify_layer_bytes(1, PROMPT, 16) / g_ms / 1e6,
             "global_layer_tflops": verify_layer_flops(1, PROMPT, 16) / g_ms / 1e9,
             "commit_us_52_layers": c1_ms * 1e3, "commit_us_52_layers_per_layer_calls": c_ms * 1e3}
+
+
+def append_decode(early, *args):
+    """mg_append_decode, or mg_append_decode_ex with MG_EARLY_START when the
+    previous kernel is known to leave this call's cache and position alone."""
+    from hybrid_local_global_attn_b300 import mg
+    if early:
+        mg.mg_append_decode_ex(*args, mg.EARLY_START)
+    else:
+        mg.mg_append_decode(*args)
 
 
 def _graph_us(fn, reps=8, calls=1):
@@ -712,7 +723,7 @@ def leg_sweep(wl, hbm_peak, ctx=32768, batches=(1, 4, 16), steps=128):
 
         def step():
             for l in range(N_LAYERS):
-                mg.mg_append_decode(layers[l], caches[l], pos, cap, q[l], kn[l], vn[l], o[l], ws[l], err)
+                append_decode(True, layers[l], caches[l], pos, cap, q[l], kn[l], vn[l], o[l], ws[l], err)
 
         step()
         torch.cuda.synchronize()
@@ -815,10 +826,14 @@ def run_gpu(args, rank, world):
     pos_cur = stage_view(qb + 2 * kvb, 4, torch.int32, (1,))
     o_cur = torch.empty((N_LAYERS, 1, 32, 128), dtype=torch.bfloat16, device=dev)
 
-    def decode_step():
+    # Every decode call of a step follows another layer's kernels, which
+    # write neither its cache nor the position: the calls pass
+    # MG_EARLY_START, so each layer's cache loads start under the previous
+    # layer's tail (the plain-call step is timed too, below).
+    def decode_step(early=True):
         for l in range(N_LAYERS):
-            mg.mg_append_decode(layers[l], caches[l], pos_cur, cap, q_cur[l], k_cur[l], v_cur[l],
-                                o_cur[l], ws_dec[l], err)
+            append_decode(early, layers[l], caches[l], pos_cur, cap, q_cur[l], k_cur[l], v_cur[l],
+                          o_cur[l], ws_dec[l], err)
 
     def stage(i):
         pos_cur.fill_(PROMPT + i)
@@ -841,10 +856,10 @@ def run_gpu(args, rank, world):
     # the position), so nothing but the 52 layers' kernels runs per step.
     pos_steps = torch.arange(PROMPT, PROMPT + W + K, dtype=torch.int32, device=dev)
 
-    def decode_step_at(i):
+    def decode_step_at(i, early=True):
         for l in range(N_LAYERS):
-            mg.mg_append_decode(layers[l], caches[l], pos_steps[i:i + 1], cap, wl.dec_q[i, l],
-                                wl.dec_k[i, l], wl.dec_v[i, l], o_cur[l], ws_dec[l], err)
+            append_decode(early, layers[l], caches[l], pos_steps[i:i + 1], cap, wl.dec_q[i, l],
+                          wl.dec_k[i, l], wl.dec_v[i, l], o_cur[l], ws_dec[l], err)
 
     step_graphs = []
     for i in range(W + K):
@@ -872,6 +887,22 @@ def run_gpu(args, rank, world):
     clocks = clk.stop()
     del step_graphs
     dec_ms = max_over_ranks(e0.elapsed_time(e1), dev, world)
+    # the same steps through plain mg_append_decode calls (no early start)
+    plain_graphs = []
+    for i in range(W, W + K):
+        gi = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gi):
+            decode_step_at(i, early=False)
+        plain_graphs.append(gi)
+    plain_graphs[0].replay()
+    torch.cuda.synchronize()
+    e0.record()
+    for gi in plain_graphs:
+        gi.replay()
+    e1.record()
+    e1.synchronize()
+    plain_us = e0.elapsed_time(e1) / K * 1e3
+    del plain_graphs
     dec_bytes = sum(decode_layer_bytes(kinds[l], PROMPT + i) for i in range(W, W + K)
                     for l in range(N_LAYERS))
     gbs = job_throughput(dec_bytes, dec_ms / 1e3, world) / 1e9
@@ -930,8 +961,8 @@ def run_gpu(args, rank, world):
         v2 = sd[qb + kvb:qb + 2 * kvb].view(torch.bfloat16).view(N_LAYERS, 1, 1, 2, 128)
         p2 = sd[qb + 2 * kvb:qb + 2 * kvb + 4].view(torch.int32)
         for l in range(N_LAYERS):
-            mg.mg_append_decode(layers[l], caches[l], p2, cap, q2[l], k2[l], v2[l], out2[1][l],
-                                ws_dec[l], err)
+            append_decode(True, layers[l], caches[l], p2, cap, q2[l], k2[l], v2[l], out2[1][l],
+                          ws_dec[l], err)
     graphs2.append(g2)
     main = torch.cuda.current_stream()
     copy_s = torch.cuda.Stream(device=dev)
@@ -986,6 +1017,8 @@ def run_gpu(args, rank, world):
             "cache_fill": "prefill" if args.fill != "random" else "random (profiling run)"},
         "pct_of_8tbs": gbs / world / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": gbs / world / hbm_peak,
+        "decode_calls": "mg_append_decode_ex with MG_EARLY_START (cache loads start under the previous layer)",
+        "plain_calls_us_per_step": plain_us,
         "roofline": {"bound": "hbm", "kernel": "attn_decode (split-KV pass + combine), global "
                                               "layer at context 131072+",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
@@ -1124,21 +1157,24 @@ def run_ncu_case(name):
             pos = torch.tensor([T - n], dtype=torch.int32, device=dev)
             for _ in range(4):
                 mg.mg_attn_verify(lay, cache, pos, T, q, kn, vn, o, ws, err)
-    elif name in ("decode_local", "verify_local"):
-        # one local layer at context 131072 (a full 2048-slot ring), batch 1
+    elif name in ("decode_local", "verify_local", "decode_local_b16", "verify_local_b8"):
+        # one local layer at context 131072 (a full 2048-slot ring), batch 1;
+        # batch 16 (decode) and 8 (verify) run the kernels whose CTAs walk
+        # their ring piece in rounds
         T = 131072
-        cache = mg.KVCache(mg.LOCAL, 1, T + 16)
+        B = 16 if name == "decode_local_b16" else 8 if name == "verify_local_b8" else 1
+        cache = mg.KVCache(mg.LOCAL, B, T + 16)
         cache.k.normal_()
         cache.v.normal_()
         lay = mg.make_layer(mg.LOCAL)
-        n = 1 if name == "decode_local" else 16
+        n = 1 if name.startswith("decode") else 16
         op = mg.OP_DECODE if n == 1 else mg.OP_VERIFY
-        ws = mg.workspace(op, lay, 1, n, T + 16)
-        q = torch.randn((1, n, 32, 128), device=dev).to(bf)
-        kn = torch.randn((1, n, 2, 128), device=dev).to(bf)
-        vn = torch.randn((1, n, 2, 128), device=dev).to(bf)
+        ws = mg.workspace(op, lay, B, n, T + 16)
+        q = torch.randn((B, n, 32, 128), device=dev).to(bf)
+        kn = torch.randn((B, n, 2, 128), device=dev).to(bf)
+        vn = torch.randn((B, n, 2, 128), device=dev).to(bf)
         o = torch.empty_like(q)
-        pos = torch.tensor([T], dtype=torch.int32, device=dev)
+        pos = torch.full((B,), T, dtype=torch.int32, device=dev)
         for _ in range(4):
             if n == 1:
                 mg.mg_append_decode(lay, cache, pos, T + 16, q[:, 0], kn, vn, o[:, 0], ws, err)
@@ -1211,6 +1247,7 @@ def main():
                     help="random: fill caches without attention (profiling runs only)")
     ap.add_argument("--ncu-case", default=None,
                     help="decode_global | decode_global_e4m3 | verify_global | decode_local | verify_local | "
+                         "decode_local_b16 | verify_local_b8 | "
                          "prefill_global | prefill_local | qkv_prefill | qkv_decode | append_chunk | "
                          "commit_layers")
     ap.add_argument("--micro", action="store_true",

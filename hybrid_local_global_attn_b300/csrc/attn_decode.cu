@@ -90,8 +90,15 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     }
   }
   __syncthreads();
-  pdl_wait();
-  pdl_launch_dependents();
+  // Early start (caller's promise that the kernel before this one writes
+  // neither the cache nor the positions): the position is read and the
+  // first stages are issued before the dependency wait; everything that
+  // kernel may produce (q, the new row) and every write come after it.
+  const bool early = p.early != 0;
+  if (!early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   const int32_t pq = p.pos[b];
   const bool bad = pq < 0 || pq >= p.max_len || pq >= p.slots;
@@ -103,6 +110,32 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const bool empty = bad || s0 >= s1;
   const int ntiles = empty ? 0 : (s1 - s0 + kDecTile - 1) / kDecTile;
   const size_t row0 = static_cast<size_t>(b) * kHq + g * kGroup;  // first query row of the group
+  const bool fused_here = p.k_new != nullptr && !empty && pq >= s0 && pq < s1;
+  // tiles issued before the wait (early start, linear cache): the first
+  // stages, short of the tile that will hold the new row
+  int npre = 0;
+  if (early && warp == kDecWarps && lane == 0 && !empty && p.map.table == nullptr) {
+    npre = min(NS, ntiles);
+    if (fused_here) npre = min(npre, (pq - s0) / kDecTile);
+    for (int t = 0; t < npre; ++t) {
+      if (t == p.stall_tile) {
+        npre = t;
+        break;
+      }
+      const uint32_t dst = smem_base + t * kDecStageBytes;
+      const uint32_t fb = bar_full + 8 * t;
+      const int32_t row = s0 + t * kDecTile;
+      mbar_arrive_expect_tx(fb, kDecStageBytes);
+      tma_load_3d(dst, &tk, fb, 0, row, b * kHkv + g);
+      tma_load_3d(dst + 8192, &tk, fb, 64, row, b * kHkv + g);
+      tma_load_3d(dst + 16384, &tv, fb, 0, row, b * kHkv + g);
+      tma_load_3d(dst + 24576, &tv, fb, 64, row, b * kHkv + g);
+    }
+  }
+  if (early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   if (bad && split == 0 && threadIdx.x == 0) set_err(p.err, MG_DERR_POSITION);
   // this CTA's partial of row r: o already divided by its softmax sum, and lse
   auto part_o = [&](int r, int d) -> float & {
@@ -110,7 +143,6 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   };
   auto part_lse = [&](int r) -> float & { return p.part_lse[(row0 + r) * p.splits + split]; };
 
-  const bool fused_here = p.k_new != nullptr && !empty && pq >= s0 && pq < s1;
   bool ok = true;
   if (warp == kDecWarps) {
     // ------------------------------------------------ TMA producer warp ----
@@ -134,11 +166,11 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         __syncwarp();
       }
       if (lane == 0) {
-        int issued = 0;
+        int issued = npre;
         // a tile never straddles two pages (64 | split start, 256 | page size);
         // the page entry is reloaded only when the tile enters a new page
         int32_t cur_lp = -1, cur_row0 = 0, cur_outer = b * kHkv + g;
-        for (int t = 0; t < ntiles; ++t) {
+        for (int t = npre; t < ntiles; ++t) {
           const int st = t % NS;
           if (t == p.stall_tile) break;  // self-test: tiles from here on never arrive
           if (t >= NS &&

@@ -21,7 +21,13 @@
 //    R(d) is composed from the slot angle R(s) -- each thread computes those
 //    of its keys before the dependency wait, while the previous kernel is
 //    still running -- and R(-b) or R(-b - 2048), 64 frequencies each, which
-//    the CTA computes once the position is known.
+//    the CTA computes once the position is known; the key in the query's own
+//    slot (d = 0) enters unrotated.
+//  * Early start (MG_EARLY_START, batch 1): when the caller
+//    promises that the previous kernel writes neither the ring nor the
+//    positions, the position, the tiles, R(-b) and the rotated key
+//    fragments are all ready before the dependency wait; the query and the
+//    new row are read after it, the new key entering the fragments as is.
 //  * Precision: the rotated key k' is kept as two bf16 values, hi = bf16(k')
 //    and lo = bf16(k' - hi), and Q.K^T accumulates q.hi + q.lo (two
 //    mma.sync m16n8k16 per fragment, fp32 accumulate).  The score then
@@ -266,8 +272,17 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   // First half of a cluster barrier whose wait (before the first store into
   // another CTA's shared memory) proves every CTA of the cluster is running.
   cluster_arrive_relaxed();
-  pdl_wait();
-  pdl_launch_dependents();
+  // Early start (single-round kernel, caller's promise that the kernel
+  // before this one writes neither the ring nor the positions): the
+  // position, the ring tiles, the R(-b) table and the rotated keys are all
+  // prepared before the dependency wait; only the query and the new row --
+  // which that kernel may produce -- are read after it.
+  bool early = false;
+  if constexpr (kRounds == 1) early = p.early != 0;
+  if (!early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   // The position is loaded first, but nothing below waits for it until the
   // loads that do not depend on it are in flight: the first rounds' tiles,
@@ -279,7 +294,9 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   int issued = kBufs;  // rounds whose copies went out (thread 0's count)
   // Q fragments (A operand, 16 heads x 128 dims) straight from memory
   uint32_t qf[8][4];
-  {
+  uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
+  const size_t new_src = (static_cast<size_t>(b) * kHkv + g) * kD;  // the new row of (b, g)
+  auto load_query = [&]() {
     const __nv_bfloat16 *q0 = p.q + (static_cast<size_t>(b) * kHq + g * kGroup + gr) * kD;
     const __nv_bfloat16 *q1 = q0 + 8 * kD;
 #pragma unroll
@@ -290,16 +307,13 @@ __global__ void __launch_bounds__(kLocThreads, 1)
       qf[ks][2] = __ldg(reinterpret_cast<const unsigned int *>(q0 + c + 8));
       qf[ks][3] = __ldg(reinterpret_cast<const unsigned int *>(q1 + c + 8));
     }
-  }
-  uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
-  if (patch_mode) {  // the row's address needs no position; only the owning warp uses it
-    const size_t src = (static_cast<size_t>(b) * kHkv + g) * kD;
-    new_row = lane < 16 ? __ldg(reinterpret_cast<const uint4 *>(p.k_new + src) + (lane & 15))
-                        : __ldg(reinterpret_cast<const uint4 *>(p.v_new + src) + (lane & 15));
-  }
+    if (patch_mode)  // the row's address needs no position; only the owning warp uses it
+      new_row = lane < 16 ? __ldg(reinterpret_cast<const uint4 *>(p.k_new + new_src) + (lane & 15))
+                          : __ldg(reinterpret_cast<const uint4 *>(p.v_new + new_src) + (lane & 15));
+  };
+  if (!early) load_query();
 
   const bool bad = pq < 0 || pq >= p.max_len;
-  if (bad && my_rank == 0 && g == 0 && tid == 0) set_err(p.err, MG_DERR_POSITION);
   const int32_t n_slots = bad ? 0 : min(pq + 1, kWindow);
   const int32_t bq = pq & (kWindow - 1);  // the query's slot
   const int32_t rounds = s0 >= n_slots ? 0 : min(kRounds, (n_slots - s0 + kRound - 1) / kRound);
@@ -325,21 +339,62 @@ __global__ void __launch_bounds__(kLocThreads, 1)
     }
     consumers_sync();
   }
+  // Early start: round 0's keys rotated and split into B fragments before
+  // the dependency wait, [k-step][hi x, lo x, hi y, lo y][fragment].
+  uint32_t kfr[4][4][4];
+  if (early) {
+    if (rounds > 0) {
+      const int32_t sb = s0 + key_in_round + gr;
+      float2 kang[32];
+#pragma unroll
+      for (int sel = 0; sel < 2; ++sel) {
+        const float2 *a = ang + ((sb + 8 * sel > bq) ? 64 : 0);
+        const bool self = sb + 8 * sel == bq;  // offset 0: exactly the identity
+#pragma unroll
+        for (int f = 0; f < 16; ++f)
+          kang[16 * sel + f] = self ? make_float2(1.f, 0.f) : cmul(tab[16 * sel + f], a[freq_of(f, tq)]);
+      }
+      const bool w = wait_round(0, &abort_flag);
+      const bool okw = __all_sync(0xffffffffu, w) && !abort_flag;
+      if (!okw && lane == 0) set_err(p.err, MG_DERR_TIMEOUT);
+      ok = ok && okw;
+      const uint32_t kbase = smem_base + th * kDecStageBytes;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t kx[4], ky[4];
+        const uint32_t off = sw128(k_row, 2 * ks + k_chi);
+        ldsm_x4(kbase + off, kx[0], kx[1], kx[2], kx[3]);
+        ldsm_x4(kbase + 8192 + off, ky[0], ky[1], ky[2], ky[3]);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int j = 16 * (r >> 1) + 4 * ks + 2 * (r & 1);
+          rot_split(kx[r], ky[r], kang[j], kang[j + 1], kfr[ks][0][r], kfr[ks][1][r], kfr[ks][2][r],
+                    kfr[ks][3][r]);
+        }
+      }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    load_query();
+  }
+  if (bad && my_rank == 0 && g == 0 && tid == 0) set_err(p.err, MG_DERR_POSITION);
   for (int u = 0; u < rounds; ++u) {
     const int32_t r0 = s0 + u * kRound;  // first slot of the round
     const int32_t key0 = r0 + key_in_round;
     const int32_t sb = key0 + gr;
     const uint32_t kbase = smem_base + (u % kBufs) * kRoundSmem + th * kDecStageBytes;
     // the keys' offsets from the query: R(d) = R(s) R(-b) (s <= b) or
-    // R(s) R(-b - 2048) (s > b)
+    // R(s) R(-b - 2048) (s > b), and R(0) = I exactly for the query's own slot
     float2 kang[32];
+    if (!early) {
 #pragma unroll
-    for (int sel = 0; sel < 2; ++sel) {
-      const float2 *a = ang + ((sb + 8 * sel > bq) ? 64 : 0);
+      for (int sel = 0; sel < 2; ++sel) {
+        const float2 *a = ang + ((sb + 8 * sel > bq) ? 64 : 0);
+        const bool self = sb + 8 * sel == bq;  // offset 0: exactly the identity
 #pragma unroll
-      for (int f = 0; f < 16; ++f) kang[16 * sel + f] = cmul(tab[16 * sel + f], a[freq_of(f, tq)]);
-    }
-    {
+        for (int f = 0; f < 16; ++f)
+          kang[16 * sel + f] = self ? make_float2(1.f, 0.f) : cmul(tab[16 * sel + f], a[freq_of(f, tq)]);
+      }
       const bool w = wait_round(u, &abort_flag);
       const bool okw = __all_sync(0xffffffffu, w) && !abort_flag;
       if (!okw && lane == 0) set_err(p.err, MG_DERR_TIMEOUT);
@@ -348,7 +403,52 @@ __global__ void __launch_bounds__(kLocThreads, 1)
     // the new token's row replaces the ring row of its slot: lane c writes
     // 16-byte chunk c of K (c < 16) or of V, and decode also stores it in the ring
     const bool patch_here = patch_mode && !bad && bq >= key0 && bq < key0 + 16;
-    if (patch_here && ok) {
+    if (early && patch_here && ok) {
+      // The keys are already rotated: the new key sits at offset 0 from the
+      // query (no rotation), so the fragments of its row take k_new as the
+      // hi part and zero as the lo part; its V row goes into shared memory
+      // (read by P.V after the softmax barriers).
+      const int rr = bq - key0;  // row among the warp's 16 keys: gr + 8 sel
+      const bool mine = gr == (rr & 7);
+      uint32_t nx[4][2], ny[4][2];  // the new key's dims 16 ks + 8 h8 + 2 tq (+ 64)
+      const __nv_bfloat16 *kn = p.k_new + new_src;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+        for (int h8 = 0; h8 < 2; ++h8) {
+          const int d = 16 * ks + 8 * h8 + 2 * tq;
+          nx[ks][h8] = mine ? __ldg(reinterpret_cast<const unsigned int *>(kn + d)) : 0u;
+          ny[ks][h8] = mine ? __ldg(reinterpret_cast<const unsigned int *>(kn + 64 + d)) : 0u;
+        }
+#pragma unroll
+      for (int sel = 0; sel < 2; ++sel) {
+        const bool hit = mine && sel == (rr >> 3);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+          for (int h8 = 0; h8 < 2; ++h8) {
+            uint32_t(&f)[4][4] = kfr[ks];
+            f[0][2 * sel + h8] = hit ? nx[ks][h8] : f[0][2 * sel + h8];
+            f[1][2 * sel + h8] = hit ? 0u : f[1][2 * sel + h8];
+            f[2][2 * sel + h8] = hit ? ny[ks][h8] : f[2][2 * sel + h8];
+            f[3][2 * sel + h8] = hit ? 0u : f[3][2 * sel + h8];
+          }
+      }
+      const uint32_t r = static_cast<uint32_t>(bq - r0 - th * kDecTile);
+      const int c = lane & 15;
+      if (lane >= 16) {
+        const uint32_t addr = kbase + 16384 + (c >> 3) * 8192 + sw128(r, c & 7);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(new_row.x),
+                     "r"(new_row.y), "r"(new_row.z), "r"(new_row.w)
+                     : "memory");
+      }
+      if (p.write_new) {
+        const size_t dst = (static_cast<size_t>(head) * kWindow + bq) * kD;
+        reinterpret_cast<uint4 *>((lane < 16 ? p.k_cache : p.v_cache) + dst)[c] = new_row;
+      }
+      __syncwarp();
+    }
+    if (!early && patch_here && ok) {
       const uint32_t r = static_cast<uint32_t>(bq - r0 - th * kDecTile);
       const int c = lane & 15;
       const uint32_t addr = kbase + (lane < 16 ? 0 : 16384) + (c >> 3) * 8192 + sw128(r, c & 7);
@@ -371,6 +471,19 @@ __global__ void __launch_bounds__(kLocThreads, 1)
       float acc[2][4];
       zero4(acc[0]);
       zero4(acc[1]);
+      if (early) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          mma_16816(acc[0], qf[ks], kfr[ks][0][0], kfr[ks][0][1]);
+          mma_16816(acc[1], qf[ks], kfr[ks][0][2], kfr[ks][0][3]);
+          mma_16816(acc[0], qf[ks + 4], kfr[ks][2][0], kfr[ks][2][1]);
+          mma_16816(acc[1], qf[ks + 4], kfr[ks][2][2], kfr[ks][2][3]);
+          mma_16816(acc[0], qf[ks], kfr[ks][1][0], kfr[ks][1][1]);
+          mma_16816(acc[1], qf[ks], kfr[ks][1][2], kfr[ks][1][3]);
+          mma_16816(acc[0], qf[ks + 4], kfr[ks][3][0], kfr[ks][3][1]);
+          mma_16816(acc[1], qf[ks + 4], kfr[ks][3][2], kfr[ks][3][3]);
+        }
+      } else
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         uint32_t kx[4], ky[4];  // dims 16 ks.. and 64 + 16 ks..
@@ -613,6 +726,11 @@ cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtens
   // 16 CTAs run at once (one per GPC), 15 of 8, 33 of 4: the fewest rounds
   // per CTA that put every pair in one wave.
   const int pairs = p.batch * kHkv;
+  // The early start pays only while this kernel's clusters can be resident
+  // beside the previous kernel's (two sets of 16-CTA clusters in 7 GPCs):
+  // otherwise the late clusters would read the query after their keys
+  // instead of beside them.
+  if (pairs > 3) p.early = 0;
   if (pairs <= 7) return launch_local_rounds<1>(p, tk, tv, s, 2);
   if (pairs <= 15) return launch_local_rounds<2>(p, tk, tv, s, 7);
   return launch_local_rounds<4>(p, tk, tv, s, 8);

@@ -342,7 +342,8 @@ T *at(void *base, size_t off) {
 cudaError_t launch_local(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
                          int32_t n, int32_t max_len, const void *q, const void *k_new,
                          const void *v_new, bool write_new, void *o, uint32_t *d_err,
-                         const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s) {
+                         const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s,
+                         bool early = false) {
   LocalParams p;
   p.pos = d_pos;
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -356,6 +357,7 @@ cudaError_t launch_local(const mg_layer *layer, const mg_cache *cache, const int
   p.n = n;
   p.max_len = max_len;
   p.write_new = write_new ? 1 : 0;
+  p.early = early ? 1 : 0;
   p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
   const RopeTables t = rope_tables(layer->rope_theta);
   std::memcpy(p.turn, t.turn, sizeof p.turn);
@@ -524,7 +526,8 @@ int mg_kv_commit_layers(int32_t n_layers, const mg_layer *layers, const mg_cache
 static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
                        int32_t max_len, const void *q, const void *k_new, const void *v_new,
                        void *o, void *ws, size_t ws_bytes, uint32_t *d_err, void *stream,
-                       uint64_t wait_ns = kWaitLimitNs, int32_t stall_tile = -1) {
+                       uint64_t wait_ns = kWaitLimitNs, int32_t stall_tile = -1,
+                       bool early = false) {
   int st = check_layer(layer);
   if (st != MG_OK) return st;
   if ((st = check_cache(layer, cache)) != MG_OK) return st;
@@ -558,7 +561,7 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (layer->kind == MG_LOCAL)
     return launch_status(launch_local(layer, cache, d_pos, 1, max_len, q, k_new, v_new,
-                                      k_new != nullptr, o, d_err, tk, tv, s));
+                                      k_new != nullptr, o, d_err, tk, tv, s, early));
   DecodeParams p;
   p.pos = d_pos;
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -583,6 +586,7 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   }
   p.wait_ns = wait_ns;
   p.stall_tile = stall_tile;
+  p.early = early && !e4m3 ? 1 : 0;
   cudaError_t e = e4m3 ? launch_decode_e4m3(p, tk, tv, s) : launch_decode(p, tk, tv, s);
   if (e != cudaSuccess) return MG_ERR_CUDA;
   if (!split) return MG_OK;
@@ -673,6 +677,16 @@ int mg_append_decode(const mg_layer *layer, const mg_cache *cache, const int32_t
   if (k_new == nullptr || v_new == nullptr) return MG_ERR_INVALID;
   return decode_impl(layer, cache, d_pos, max_len, q, k_new, v_new, o, ws, ws_bytes, d_err,
                      stream);
+}
+
+int mg_append_decode_ex(const mg_layer *layer, const mg_cache *cache, const int32_t *d_pos,
+                        int32_t max_len, const void *q, const void *k_new, const void *v_new,
+                        void *o, void *ws, size_t ws_bytes, uint32_t *d_err, uint32_t flags,
+                        void *stream) {
+  if (k_new == nullptr || v_new == nullptr) return MG_ERR_INVALID;
+  if ((flags & ~MG_EARLY_START) != 0) return MG_ERR_INVALID;
+  return decode_impl(layer, cache, d_pos, max_len, q, k_new, v_new, o, ws, ws_bytes, d_err,
+                     stream, kWaitLimitNs, -1, (flags & MG_EARLY_START) != 0);
 }
 
 }  // extern "C"

@@ -160,6 +160,7 @@ struct DecodeParams {  // global layers
   // out.
   uint64_t wait_ns;
   int32_t stall_tile;
+  int32_t early;  // 1: position and the first tiles read before the dependency wait
 };
 
 
@@ -175,6 +176,7 @@ struct LocalParams {  // local layers, n <= kMaxLocalTokens query tokens
   uint32_t *err;
   int32_t batch, n, max_len;
   int32_t write_new;   // 1: also store the block rows into the ring (fused append, n == 1)
+  int32_t early;       // 1: position and ring read before the dependency wait (decode, n == 1)
   float scale_log2;
   uint64_t turn[64];   // as in RopeTurns
   float2 step[3][64];  // (cos, sin) of kRopeSteps[k] * w_i, from double

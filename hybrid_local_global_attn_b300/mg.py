@@ -68,6 +68,8 @@ lib.mg_kv_commit.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, _P]
 lib.mg_kv_commit_layers.argtypes = [_i32, _LP, _CP, _P, _i32, _P, _P, _P, _P, _P, _P]
 lib.mg_attn_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_append_decode.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
+lib.mg_append_decode_ex.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P,
+                                    ctypes.c_uint32, _P]
 lib.mg_attn_verify.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_attn_prefill.argtypes = [_LP, _CP, _P, _i32, _i32, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]
 lib.mg_qkv_workspace_bytes.argtypes = [_i32, _i32]
@@ -77,8 +79,8 @@ lib.mg_qkv_append.restype = ctypes.c_int
 lib.mg_debug_decode_stall.argtypes = [_LP, _CP, _P, _i32, _P, _P, _P, ctypes.c_size_t, _P, _P,
                                       ctypes.c_uint64, _i32]
 lib.mg_debug_decode_stall.restype = ctypes.c_int
-for _f in (lib.mg_kv_append, lib.mg_kv_commit, lib.mg_kv_commit_layers, lib.mg_attn_decode, lib.mg_append_decode, lib.mg_attn_verify,
-           lib.mg_attn_prefill):
+for _f in (lib.mg_kv_append, lib.mg_kv_commit, lib.mg_kv_commit_layers, lib.mg_attn_decode, lib.mg_append_decode,
+           lib.mg_append_decode_ex, lib.mg_attn_verify, lib.mg_attn_prefill):
     _f.restype = ctypes.c_int
 
 
@@ -294,6 +296,18 @@ def mg_append_decode(layer, cache: KVCache, pos, max_len, q, k_new, v_new, o, ws
           _ptr(v_new, torch.bfloat16), _ptr(o, torch.bfloat16), _ptr(ws),
           ws.numel() * ws.element_size() if ws is not None else 0, _ptr(err, torch.int32),
           _stream(stream))
+
+
+EARLY_START = 1  # MG_EARLY_START
+
+
+def mg_append_decode_ex(layer, cache: KVCache, pos, max_len, q, k_new, v_new, o, ws, err, flags,
+                        stream=None):
+    _call(lib.mg_append_decode_ex, ctypes.byref(layer), ctypes.byref(cache.struct),
+          _ptr(pos, torch.int32), int(max_len), _ptr(q, torch.bfloat16), _ptr(k_new, torch.bfloat16),
+          _ptr(v_new, torch.bfloat16), _ptr(o, torch.bfloat16), _ptr(ws),
+          ws.numel() * ws.element_size() if ws is not None else 0, _ptr(err, torch.int32),
+          int(flags), _stream(stream))
 
 
 def mg_attn_verify(layer, cache: KVCache, pos0, max_len, q, k_new, v_new, o, ws, err, stream=None):

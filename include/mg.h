@@ -271,6 +271,35 @@ int mg_append_decode(const mg_layer *layer, const mg_cache *cache,
                      const void *k_new, const void *v_new, void *o, void *ws,
                      size_t ws_bytes, uint32_t *d_err, void *stream);
 
+/* flags of mg_append_decode_ex */
+#define MG_EARLY_START 1u /* the previous kernel writes neither the cache nor d_pos */
+
+/*
+ * mg_append_decode with flags; flags == 0 is mg_append_decode itself (any
+ * other bit: MG_ERR_INVALID).
+ *
+ * MG_EARLY_START: the caller promises that the kernel enqueued on `stream`
+ * just before this call writes neither this layer's cache nor d_pos -- it
+ * may produce q, k_new and v_new, as a projection that leaves the cache to
+ * the fused append does, or be another layer's attention.  The decode
+ * kernels then read the position and start their cache loads before their
+ * programmatic-dependent-launch wait, so that these overlap the previous
+ * kernel's tail: a local layer also rotates its ring keys there, a global
+ * layer issues its first pipeline stages.  q, k_new and v_new are read, and
+ * everything is written, after the wait.  The results equal
+ * mg_append_decode's bit for bit when the promise holds; when it does not,
+ * they may be wrong (stale cache rows or position) but no access leaves
+ * the cache or the buffers passed.  Local layers use it for a batch of one
+ * sequence (where this call's clusters fit on the GPU beside the previous
+ * call's), bf16 global layers on a linear cache for any batch; other cases
+ * ignore the flag.
+ */
+int mg_append_decode_ex(const mg_layer *layer, const mg_cache *cache,
+                        const int32_t *d_pos, int32_t max_len, const void *q,
+                        const void *k_new, const void *v_new, void *o, void *ws,
+                        size_t ws_bytes, uint32_t *d_err, uint32_t flags,
+                        void *stream);
+
 /*
  * Fused QKV projection with the KV append in its epilogue: the step before
  * the attention calls.  [P1 §01] gives the hidden size (6656), 32 query heads

@@ -286,3 +286,68 @@ def test_local_decode_rounds_peaked(mg, B, case):
     for b in range(B):
         ref = orc.attention(olay, k[b], v[b], [p], q[b:b + 1])[0]
         compare(o[b], ref, f"{case} B {B} b {b}")
+
+
+@pytest.mark.parametrize("B", [1, 3, 4])
+def test_append_decode_early_matches_plain(mg, B):
+    """mg_append_decode_ex with MG_EARLY_START: a local and a global layer
+    decoded in turn for 24 steps (each call's previous kernel is the other
+    layer's, which writes neither this cache nor the positions), captured in
+    one CUDA graph so that the calls overlap as in a decode step.  Outputs
+    and caches equal the plain mg_append_decode run bit for bit, and every
+    step's outputs match the oracle."""
+    bases = [2040, 3000, 4090, 100][:B]
+    S = 24
+    T = max(bases) + S
+    layers = []
+    for kind, li in ((0, 4), (1, 5)):
+        k, v = synth.history(B, T, 21, li)
+        q = synth.queries(B, S, 21, li)
+        layers.append(dict(kind=kind, k=k, v=v, q=q, kd=k.cuda(), vd=v.cuda(), qd=q.cuda(),
+                           lay=mg.make_layer(kind), ws=mg.workspace(mg.OP_DECODE, mg.make_layer(kind), B, 1, T),
+                           fill=fill_for_decode(mg, kind, k[:, :max(bases)], v[:, :max(bases)],
+                                                [p - 1 for p in bases], T)))
+    pos_all = torch.tensor([[p + i for p in bases] for i in range(S)], dtype=torch.int32, device="cuda")
+    kn_all = [torch.stack([torch.stack([L["kd"][b, p + i] for b, p in enumerate(bases)])[:, None]
+                           for i in range(S)]).contiguous() for L in layers]
+    vn_all = [torch.stack([torch.stack([L["vd"][b, p + i] for b, p in enumerate(bases)])[:, None]
+                           for i in range(S)]).contiguous() for L in layers]
+    q_all = [L["qd"].transpose(0, 1).contiguous() for L in layers]  # [S][B][32][128]
+
+    def run(early):
+        caches = []
+        for L in layers:
+            c = mg.KVCache(L["kind"], B, T)
+            c.k.copy_(L["fill"].k)
+            c.v.copy_(L["fill"].v)
+            caches.append(c)
+        outs = torch.zeros((S, 2, B, 32, 128), dtype=torch.bfloat16, device="cuda")
+        err = mg.error_word()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(S):
+                for li, L in enumerate(layers):
+                    args = (L["lay"], caches[li], pos_all[i], T, q_all[li][i], kn_all[li][i], vn_all[li][i],
+                            outs[i, li], L["ws"], err)
+                    if early:
+                        mg.mg_append_decode_ex(*args, mg.EARLY_START)
+                    else:
+                        mg.mg_append_decode(*args)
+        g.replay()
+        torch.cuda.synchronize()
+        check_err(err)
+        return outs, caches
+
+    oa, ca = run(False)
+    ob, cb = run(True)
+    assert torch.equal(oa, ob), "early decode differs from the plain call"
+    for x, y in zip(ca, cb):
+        assert torch.equal(x.k, y.k) and torch.equal(x.v, y.v), "caches differ"
+    for li, L in enumerate(layers):
+        olay = orc.layer(oracle_kind(L["kind"]))
+        for i in (0, S // 2, S - 1):
+            for b, p in enumerate(bases):
+                ref = orc.attention(olay, L["k"][b, :p + i + 1], L["v"][b, :p + i + 1], [p + i],
+                                    L["q"][b, i:i + 1])[0]
+                compare(ob[i, li, b], ref, f"layer kind {L['kind']} step {i} seq {b}")
