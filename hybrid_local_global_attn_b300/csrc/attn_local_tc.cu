@@ -34,11 +34,15 @@
 //    the last written position.
 //  * Softmax: thread = (row, half of the keys); maxima and sums meet in
 //    shared memory; P goes back to TMEM (bf16) as the A operand of P.V.
-//  * Cluster merge: each CTA owns 16 / (cluster size) heads; every CTA
-//    stages its normalised rows and log-sum-exps per head in shared memory
-//    and sends each one bulk copy (cp.async.bulk into the owner's shared
-//    memory), whose bytes complete on the owner's mbarrier; the owner merges
-//    the partials per token.
+//  * Cluster merge through L2: each CTA owns 16 / (cluster size) heads;
+//    every CTA stages its normalised rows and log-sum-exps in shared memory
+//    (a transpose: a thread holds one row), copies them with coalesced
+//    stores into its slots of an exchange buffer in the workspace, and one
+//    cluster barrier (release / acquire) publishes them; each owner then
+//    reads its heads' partials from L2 and merges them per token in
+//    registers.  (All-to-all pushes over distributed shared memory -- bulk
+//    copies or remote stores -- moved these 64 KB per CTA at ~25 GB/s per SM
+//    here, ~3 us per layer; the L2 route takes ~2.)
 //  * Cluster size by batch: at most 7 clusters of 16 CTAs run at once on
 //    this B300 (a 16-CTA cluster takes 16 SMs of one GPC), 15 of 8, 33 of 4.
 //    With more (sequence, KV head, token group) triples than one wave of 16,
@@ -62,17 +66,16 @@ constexpr int kBoxBytes = kKeysMax * 128;      // one 64-dim box of 144 key rows
 constexpr int kKVSmem = 2 * kBoxBytes;         // dims 0-63 box, dims 64-127 box
 constexpr int kAngSmem = 2 * 64 * 8;           // R(-b), R(-b - 2048) per frequency
 constexpr int kRedSmem = 4 * kTcRows * 4;      // [half][m, l][row]
-// Inbox of an owning CTA: rows [head owned][source][token][128] fp32, then
-// lse [head owned][source][8 tokens] -- 16 (head, source) blocks in all.
-// One source's rows of one head are contiguous: they travel as one bulk copy.
-constexpr int kInboxRows = kLocCluster * kTpc * kD * 4;  // 64 KB
-constexpr int kInboxLse = kLocCluster * kTpc * 4;        // 512 B
 // Staging of this CTA's normalised rows, [head][token][128] fp32 with the
 // head blocks 16 bytes apart beyond their size (so that the 32 rows a warp
 // stores at once fall on different banks), and lse [head][8]: over the key
 // buffers, free once the last Q.K^T has run.
 constexpr int kStageOwner = kTpc * kD * 4 + 16;
-static_assert(kLocCluster * kStageOwner + kInboxLse <= 2 * kKVSmem, "staging fits the key buffers");
+static_assert(kLocCluster * kStageOwner + kLocCluster * kTpc * 4 <= 2 * kKVSmem,
+              "staging fits the key buffers");
+// Each CTA allocates all 512 TMEM columns, so a second CTA on the same SM
+// would wait in tcgen05.alloc: the dynamic shared memory keeps it to one.
+constexpr int kOneCtaPerSm = 120 * 1024;
 
 template <int kRounds> struct TcLocPlan {
   static constexpr int kCl = kLocCluster / kRounds;  // CTAs per cluster
@@ -84,10 +87,9 @@ template <int kRounds> struct TcLocPlan {
   static constexpr int kOffAng = kOffV + kVBufs * kKVSmem;
   static constexpr int kOffRed = kOffAng + kAngSmem;
   static constexpr int kOffTurn = kOffRed + kRedSmem;  // 64 turns (uint64), then R(128 w_f)
-  static constexpr int kOffW = kOffTurn + 64 * 8 + 64 * 8;  // merge weights [head][token][source]
-  static constexpr int kOffBars = kOffW + kLocCluster * kTpc * 4;
-  static constexpr int kOffInbox = kOffBars + 64;
-  static constexpr int kSmem = kOffInbox + kInboxRows + kInboxLse + 1024;  // + alignment slack
+  static constexpr int kOffBars = kOffTurn + 64 * 8 + 64 * 8;
+  static constexpr int kUsed = kOffBars + 64 + 1024;  // + alignment slack
+  static constexpr int kSmem = kUsed > kOneCtaPerSm ? kUsed : kOneCtaPerSm;
   static constexpr int kOffStage = kOffK;
   static constexpr int kOffStageLse = kOffK + kLocCluster * kStageOwner;
 };
@@ -100,47 +102,22 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
+// All threads of every CTA of the cluster: the global writes made before it
+// are visible to every thread of the cluster after it.
+__device__ __forceinline__ void cluster_sync_release_acquire() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+__device__ __forceinline__ float4 ld_cg_f4(const float *p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
 }
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into
-// another CTA's, completing the bytes on that CTA's mbarrier.
-__device__ __forceinline__ void bulk_to_cta(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                            uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst_cluster),
-      "r"(src), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_wait_read() {
-  asm volatile("cp.async.bulk.commit_group;\ncp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-  auto test = [&]() {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred P;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, P;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-  };
-  if (test()) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (test()) return true;
-    if ((it & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
-  }
+__device__ __forceinline__ float ld_cg_f(const float *p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
@@ -203,12 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = sbase + Plan::kOffK, sKl = sbase + Plan::kOffKl, sV0 = sbase + Plan::kOffV;
   float2 *ang = reinterpret_cast<float2 *>(smem + Plan::kOffAng);
   float *red = reinterpret_cast<float *>(smem + Plan::kOffRed);
-  float *inbox = reinterpret_cast<float *>(smem + Plan::kOffInbox);
   uint64_t *turns = reinterpret_cast<uint64_t *>(smem + Plan::kOffTurn);
   float2 *step_round = reinterpret_cast<float2 *>(smem + Plan::kOffTurn + 64 * 8);  // R(128 w_f)
-  float *wts = reinterpret_cast<float *>(smem + Plan::kOffW);
   const uint32_t bar_k = sbase + Plan::kOffBars, bar_s = bar_k + 8, bar_o = bar_k + 16;
-  const uint32_t bar_inbox = bar_k + 24, bar_v = bar_k + 32;  // bar_v: one per V buffer
+  const uint32_t bar_v = bar_k + 24;  // one per V buffer
 
   const int nq = (p.n + kTpc - 1) / kTpc;  // token groups per sequence
   const int g = blockIdx.y, b = blockIdx.z / nq;
@@ -240,11 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_k, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
-    mbar_init(bar_inbox, 1);
     for (int i = 0; i < kVBufs; ++i) mbar_init(bar_v + 8 * i, 1);
     fence_mbar_init();
-    // from each (head, source) block of the inbox: cnt rows and 8 lse
-    mbar_arrive_expect_tx(bar_inbox, kLocCluster * (cnt * kD * 4 + kTpc * 4));
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
     for (int x = 0; x < 2; ++x) {
@@ -261,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kRounds > 1) {
       float cs, sn;
       rope_cos_sin(kPiece, p.turn[tid], cs, sn);
-      step_round[tid] = make_float2(cs, sn);
+      step_round[(tid & 31) * 2 + (tid >> 5)] = make_float2(cs, sn);
     }
   }
   __syncthreads();
@@ -280,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_slot;
-  cluster_arrive_relaxed();
   pdl_wait();
   pdl_launch_dependents();
 
@@ -323,10 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool bad = p0 < 0 || static_cast<int64_t>(p0) + p.n > p.max_len;
   if (bad && my_rank == 0 && g == 0 && i0 == 0 && tid == 0) set_err(p.err, MG_DERR_POSITION);
   const int32_t b0 = p0 & (kWindow - 1);  // slot of the block start
-  if (tid < 128) {  // R(-b w_f) and R(-(b + 2048) w_f)
+  if (tid < 128) {  // R(-b w_f) and R(-(b + 2048) w_f) at [f mod 32][f / 32][variant]
     float cs, sn;
-    rope_cos_sin(-(b0 + kWindow * (tid >> 6)), turns[tid & 63], cs, sn);
-    ang[tid] = make_float2(cs, sn);
+    const int f = tid & 63, variant = tid >> 6;
+    rope_cos_sin(-(b0 + kWindow * variant), turns[f], cs, sn);
+    ang[((f & 31) * 2 + (f >> 5)) * 2 + variant] = make_float2(cs, sn);
   }
   // rotated query halves into TMEM: row r, dims 32 hh.. (columns 16 hh..)
   // and 64 + 32 hh.. (columns 32 + 16 hh..)
@@ -383,9 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // by R(s) R(-b) or R(s) R(-b - 2048) and split it
     {
       float2 a[32];
-      const float2 *ab = ang + ((rs0 + krow > b0) ? 64 : 0) + 32 * kh;
+      // the row's variant; the two halves (kh) and variants of a warp read
+      // neighbouring entries (no bank conflicts)
+      const float2 *ab = ang + kh * 2 + ((rs0 + krow > b0) ? 1 : 0);
 #pragma unroll
-      for (int f = 0; f < 32; ++f) a[f] = cmul(kang[f], ab[f]);
+      for (int f = 0; f < 32; ++f) a[f] = cmul(kang[f], ab[4 * f]);
       ok = mbar_wait(bar_k, u & 1, &abort_flag) && ok;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -400,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (kRounds > 1)
 #pragma unroll
-        for (int f = 0; f < 32; ++f) kang[f] = cmul(kang[f], step_round[32 * kh + f]);
+        for (int f = 0; f < 32; ++f) kang[f] = cmul(kang[f], step_round[2 * f + kh]);
     }
     fence_proxy_async_smem();  // the tensor core reads what the threads wrote
     if (u == 0) tmem_wait_st();  // and the rotated queries are in TMEM
@@ -547,9 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const float L = red[1 * kTcRows + r] + red[3 * kTcRows + r];
 
-  // ---------------- send this CTA's normalised rows to the owning CTAs ----
+  // ------------- publish this CTA's normalised rows through the workspace ----
   // Stage [head][token][128] and lse [head][8] over the key buffers (every
-  // MMA has retired), then one bulk copy per head.
+  // MMA has retired; a thread holds one row), then copy them with coalesced
+  // stores into this CTA's slots of the cluster's exchange buffer:
+  // rows [head][source][token][128], lse [head][source][token].
   const bool have = ok && row_live && L > 0.f;
   const float inv = have ? 1.f / L : 0.f;
   const int hd = r & 15;
@@ -570,59 +546,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                                have ? __uint_as_float(ov[j + 3]) * inv : 0.f);
   }
   if (hh == 0) stage_lse[hd * kTpc + rt] = have ? m_run + __log2f(L) : -INFINITY;
-  fence_proxy_async_smem();  // the bulk copies read what the threads wrote
   tc_fence_before();
   __syncthreads();  // staging complete; TMEM reads done
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
-  cluster_wait();  // every CTA of the cluster runs, its inbox barrier is set
-  if (tid < kLocCluster) {  // thread h sends head h's rows and lse to its owner
-    const uint32_t h = static_cast<uint32_t>(tid);
-    const uint32_t own = h / kOwned, blk = (h % kOwned) * kCl + my_rank;  // (head owned, source)
-    const uint32_t inbox_s = smem_u32(inbox);
-    const uint32_t obar = map_to_rank(bar_inbox, own);
-    bulk_to_cta(map_to_rank(inbox_s + blk * (kTpc * kD * 4), own),
-                sbase + Plan::kOffStage + h * kStageOwner, cnt * kD * 4, obar);
-    bulk_to_cta(map_to_rank(inbox_s + kInboxRows + blk * (kTpc * 4), own),
-                sbase + Plan::kOffStageLse + h * (kTpc * 4), kTpc * 4, obar);
-    bulk_commit_wait_read();  // the staging is not reused, but copies finish reading first
+  const size_t cid = static_cast<size_t>(head) * nq + blockIdx.z % nq;  // this cluster
+  float *xr = p.x_rows + cid * (kGroup * kCl * kTpc * kD);
+  float *xl = p.x_lse + cid * (kGroup * kCl * kTpc);
+#pragma unroll 4
+  for (int i = tid; i < kGroup * kTpc * (kD / 4); i += kThreads) {
+    const int h = i / (kTpc * (kD / 4)), rem = i % (kTpc * (kD / 4));  // rem: token * 32 + d4
+    reinterpret_cast<float4 *>(xr + (static_cast<size_t>(h) * kCl + my_rank) * (kTpc * kD))[rem] =
+        *reinterpret_cast<const float4 *>(stage + (h * kStageOwner) / 4 + rem * 4);
   }
+  if (tid < kGroup * kTpc) xl[((tid / kTpc) * kCl + my_rank) * kTpc + tid % kTpc] = stage_lse[tid];
+  // Every CTA of the cluster reaches this barrier (all waits above are
+  // bounded), and its partials are visible to the others after it.
+  cluster_sync_release_acquire();
 
   // -- merge the rows this CTA owns (heads kOwned * rank + j of the group) ----
-  // (CTA-uniform: the block below has a barrier)
-  const bool all_in = __syncthreads_and(mbar_wait_cluster(bar_inbox, 0));
-  if (!all_in && tid == 0) set_err(p.err, MG_DERR_TIMEOUT);
-  if (all_in) {
-    const float *lse = inbox + kInboxRows / 4;  // [head owned][source][8]
-    for (int i = tid; i < kOwned * kTpc * kCl; i += kThreads) {  // weights, normalised
-      const int j = i / (kTpc * kCl), t = (i / kCl) % kTpc, c = i % kCl;
-      if (t >= cnt) continue;
-      const float *lj = lse + j * kCl * kTpc;
-      float Mx = -INFINITY;
+  // thread: (head owned j, token t, 4 dims); the partials come from L2 (.cg:
+  // the exchange buffer is rewritten by every call, L1 may hold old lines)
+  for (int i = tid; i < kOwned * kTpc * (kD / 4); i += kThreads) {
+    const int j = i / (kTpc * (kD / 4)), t = (i / (kD / 4)) % kTpc, d4 = i % (kD / 4);
+    if (t >= cnt) continue;
+    const int hq = static_cast<int>(my_rank) * kOwned + j;
+    float ls[kCl];
+    float4 rv[kCl];
 #pragma unroll
-      for (int k = 0; k < kCl; ++k) Mx = fmaxf(Mx, lj[k * kTpc + t]);
-      float den = 0.f;
-#pragma unroll
-      for (int k = 0; k < kCl; ++k)
-        den += (Mx == -INFINITY || lj[k * kTpc + t] == -INFINITY) ? 0.f : fast_exp2(lj[k * kTpc + t] - Mx);
-      const float mine = lj[c * kTpc + t];
-      wts[(j * kTpc + t) * kCl + c] =
-          (den > 0.f && mine != -INFINITY) ? fast_exp2(mine - Mx) / den : 0.f;
+    for (int c = 0; c < kCl; ++c) {
+      ls[c] = ld_cg_f(xl + (hq * kCl + c) * kTpc + t);
+      rv[c] = ld_cg_f4(xr + ((static_cast<size_t>(hq) * kCl + c) * kTpc + t) * kD + 4 * d4);
     }
-    __syncthreads();
-    const int d = tid & (kD - 1);
-    for (int i = tid >> 7; i < kOwned * kTpc; i += kThreads / kD) {
-      const int j = i / kTpc, t = i % kTpc;
-      if (t >= cnt) continue;
-      float acc = 0.f;
+    float Mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kCl; ++c)
-        acc = fmaf(wts[(j * kTpc + t) * kCl + c], inbox[((j * kCl + c) * kTpc + t) * kD + d], acc);
-      const size_t orow = (static_cast<size_t>(b) * p.n + i0 + t) * kHq + g * kGroup + my_rank * kOwned + j;
-      p.o[orow * kD + d] = __float2bfloat16_rn(acc);
+    for (int c = 0; c < kCl; ++c) Mx = fmaxf(Mx, ls[c]);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < kCl; ++c) {
+      const float w = (Mx == -INFINITY || ls[c] == -INFINITY) ? 0.f : fast_exp2(ls[c] - Mx);
+      den += w;
+      acc.x = fmaf(w, rv[c].x, acc.x);
+      acc.y = fmaf(w, rv[c].y, acc.y);
+      acc.z = fmaf(w, rv[c].z, acc.z);
+      acc.w = fmaf(w, rv[c].w, acc.w);
     }
+    const float iv = den > 0.f ? 1.f / den : 0.f;
+    const size_t orow = (static_cast<size_t>(b) * p.n + i0 + t) * kHq + g * kGroup + hq;
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x * iv, acc.y * iv);
+    pk.y = pack_bf16x2(acc.z * iv, acc.w * iv);
+    reinterpret_cast<uint2 *>(p.o + orow * kD)[d4] = pk;
   }
 }
 
@@ -658,14 +635,14 @@ cudaError_t launch_local_tc_rounds(const LocalParams &p, const CUtensorMap &tk,
 cudaError_t launch_local_tc(const LocalParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                             cudaStream_t s) {
   static_assert(kGroup == kLocCluster, "a 16-CTA cluster gives each CTA one head to merge");
-  if (p.n < 1 || p.n > kMaxLocalTokens || p.batch < 1 || p.k_new == nullptr)
+  if (p.n < 1 || p.n > kMaxLocalTokens || p.batch < 1 || p.k_new == nullptr ||
+      p.x_rows == nullptr || p.x_lse == nullptr)
     return cudaErrorInvalidValue;
-  // One cluster per (sequence, KV head, group of 8 tokens).  On this B300 at
-  // most 7 clusters of 16 CTAs run at once, 15 of 8, 33 of 4: the fewest
-  // rounds per CTA that put every triple in one wave.
-  const int triples = p.batch * kHkv * ((p.n + kTpc - 1) / kTpc);
-  if (triples <= 7) return launch_local_tc_rounds<1>(p, tk, tv, s, 3);
-  if (triples <= 15) return launch_local_tc_rounds<2>(p, tk, tv, s, 9);
+  // One cluster per (sequence, KV head, group of 8 tokens), its size by the
+  // number of clusters (the workspace's exchange buffers are sized the same way).
+  const int cl = local_tc_cluster(static_cast<int64_t>(p.batch) * kHkv * ((p.n + kTpc - 1) / kTpc));
+  if (cl == 16) return launch_local_tc_rounds<1>(p, tk, tv, s, 3);
+  if (cl == 8) return launch_local_tc_rounds<2>(p, tk, tv, s, 9);
   return launch_local_tc_rounds<4>(p, tk, tv, s, 10);
 }
 

@@ -296,9 +296,20 @@ bool ws_layout(int32_t op, const mg_layer *L, int32_t batch, int32_t n, int32_t 
       }
     }
   } else if (op == MG_OP_VERIFY && local) {
-    // the ring kernel: one cluster per (sequence, KV head, token), no workspace
+    // the ring kernels: one cluster per (sequence, KV head) for one token (no
+    // workspace); for a block, one per (sequence, KV head, 8 tokens), whose
+    // CTAs exchange their partial rows through the workspace
     if (n > MG_VERIFY_MAX) return false;
     w->splits = kLocCluster;
+    if (n > 1) {
+      const int64_t triples =
+          static_cast<int64_t>(batch) * kHkv * ((n + kTcPosPerTile - 1) / kTcPosPerTile);
+      const size_t slots = static_cast<size_t>(triples) * kGroup * local_tc_cluster(triples) * kTcPosPerTile;
+      w->part_o = off;
+      off = align256(off + slots * kD * sizeof(float));
+      w->part_lse = off;
+      off = align256(off + slots * sizeof(float));
+    }
   } else if (op == MG_OP_VERIFY || op == MG_OP_PREFILL) {
     if (op == MG_OP_VERIFY && n > MG_VERIFY_MAX) return false;
     w->splits = op == MG_OP_VERIFY ? splits_verify(L->kind, batch, n, max_len) : 1;
@@ -343,7 +354,7 @@ cudaError_t launch_local(const mg_layer *layer, const mg_cache *cache, const int
                          int32_t n, int32_t max_len, const void *q, const void *k_new,
                          const void *v_new, bool write_new, void *o, uint32_t *d_err,
                          const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s,
-                         bool early = false) {
+                         bool early = false, float *x_rows = nullptr, float *x_lse = nullptr) {
   LocalParams p;
   p.pos = d_pos;
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -358,6 +369,8 @@ cudaError_t launch_local(const mg_layer *layer, const mg_cache *cache, const int
   p.max_len = max_len;
   p.write_new = write_new ? 1 : 0;
   p.early = early ? 1 : 0;
+  p.x_rows = x_rows;
+  p.x_lse = x_lse;
   p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
   const RopeTables t = rope_tables(layer->rope_theta);
   std::memcpy(p.turn, t.turn, sizeof p.turn);
@@ -730,7 +743,9 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
         !map_rows(&tv, cache->v, cache->slots, outer, rows))
       return MG_ERR_CUDA;
     return launch_status(launch_local(layer, cache, d_pos0, n, max_len, q, k_new, v_new, false, o,
-                                      d_err, tk, tv, s));
+                                      d_err, tk, tv, s, false,
+                                      n > 1 ? at<float>(ws, w.part_o) : nullptr,
+                                      n > 1 ? at<float>(ws, w.part_lse) : nullptr));
   }
   const void *qsrc = q;
   CUtensorMap tq, tka, tva, tkb, tvb, tql, tkl;

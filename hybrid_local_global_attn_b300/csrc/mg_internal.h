@@ -57,6 +57,11 @@ constexpr int kTcKeys = 256;
 constexpr int kTcVRows = kTcKeys / 2;             // V streams in half tiles
 constexpr int kTcPosPerTile = kTcRows / kGroup;   // 8
 constexpr int kTcPosPerCta = kTcPosPerTile;       // 8
+// Local verify of 2..16 tokens: CTAs per cluster by the number of (sequence,
+// KV head, group of 8 tokens) triples -- the fewest rounds per CTA that put
+// every cluster in one wave (on this B300 at most 7 clusters of 16 CTAs run
+// at once, 15 of 8, 33 of 4).
+inline int local_tc_cluster(int64_t triples) { return triples <= 7 ? 16 : triples <= 15 ? 8 : 4; }
 constexpr int kTcKStages = 2;                     // K tiles (64 KB)
 constexpr int kTcVStages = 2;                     // V half tiles (32 KB)
 constexpr int kTcKTileBytes = kTcKeys * kRowBytes;   // 64 KB (two 64-dim boxes)
@@ -177,6 +182,9 @@ struct LocalParams {  // local layers, n <= kMaxLocalTokens query tokens
   int32_t batch, n, max_len;
   int32_t write_new;   // 1: also store the block rows into the ring (fused append, n == 1)
   int32_t early;       // 1: position and ring read before the dependency wait (decode, n == 1)
+  // local verify (n >= 2): the clusters' exchange buffers in the workspace,
+  // rows [cluster][16 heads][cluster size][8 tokens][128] and lse [.][.][.][8]
+  float *x_rows, *x_lse;
   float scale_log2;
   uint64_t turn[64];   // as in RopeTurns
   float2 step[3][64];  // (cos, sin) of kRopeSteps[k] * w_i, from double

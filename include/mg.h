@@ -155,9 +155,11 @@ size_t mg_page_pool_bytes(int32_t num_pages, int32_t page_size);
  * mg_attn_verify (MG_OP_VERIFY, n = draft tokens) or mg_attn_prefill
  * (MG_OP_PREFILL, n = chunk tokens) need for this layer, batch and
  * max_len.  The workspace holds split-KV partials (global decode, global
- * verify) and, for local prefill, RoPE-rotated copies of the queries and
- * of the keys in the window; local decode and local verify merge inside a
- * thread-block cluster and need none.  Nothing in a workspace needs
+ * verify), the partial rows the CTAs of a local verify cluster exchange
+ * (blocks of 2..16 tokens) and, for local prefill, RoPE-rotated copies of
+ * the queries and of the keys in the window; local decode (and a one-token
+ * local verify) merges inside a thread-block cluster and needs none.
+ * Nothing in a workspace needs
  * initialising.  A global-layer decode with one split per (sequence, KV
  * head) -- large batches -- writes its output directly and needs none.
  * Returns 0 if no workspace is needed, (size_t)-1 for bad arguments. */
