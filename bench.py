@@ -910,28 +910,45 @@ def run_gpu(args, rank, world):
     log(f"decode: {dec_ms / K * 1e3:.1f} us/step, {gbs:.1f} GB/s, clocks {clocks}")
 
     # ------------------------------------------ roofline: global decode pass ----
-    # The 13 global-layer decode calls back to back from one CUDA graph (so
-    # host launch overhead is not timed), averaged over the launches.
+    # The 13 global-layer decode calls of the last timed step, as that step
+    # makes them (fused append of the step's own token -- the same rows
+    # again -- and the early start), back to back from one CUDA graph (so
+    # host launch overhead is not timed), averaged over the launches; the
+    # same pass through plain mg_attn_decode calls is timed beside it.
     glob = [l for l in range(N_LAYERS) if kinds[l] == mg.GLOBAL]
-    p_last = PROMPT + W + K - 1
-    pos_r = torch.tensor([p_last], dtype=torch.int32, device=dev)
-    for l in glob:
-        mg.mg_attn_decode(layers[l], caches[l], pos_r, cap, q_cur[l], o_cur[l], ws_dec[l], err)
-    torch.cuda.synchronize()
-    g_r = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_r):
+    i_last = W + K - 1
+    p_last = PROMPT + i_last
+    pos_r = pos_steps[i_last:i_last + 1]
+
+    def roof_pass(early):
         for l in glob:
-            mg.mg_attn_decode(layers[l], caches[l], pos_r, cap, q_cur[l], o_cur[l], ws_dec[l], err)
-    g_r.replay()
-    reps = 8
-    e0.record()
-    for _ in range(reps):
+            if early:
+                append_decode(True, layers[l], caches[l], pos_r, cap, wl.dec_q[i_last, l],
+                              wl.dec_k[i_last, l], wl.dec_v[i_last, l], o_cur[l], ws_dec[l], err)
+            else:
+                mg.mg_attn_decode(layers[l], caches[l], pos_r, cap, wl.dec_q[i_last, l], o_cur[l],
+                                  ws_dec[l], err)
+
+    roof_ms = {}
+    for early in (True, False):
+        roof_pass(early)
+        torch.cuda.synchronize()
+        g_r = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_r):
+            roof_pass(early)
         g_r.replay()
-    e1.record()
-    e1.synchronize()
-    kern_ms = e0.elapsed_time(e1) / (reps * len(glob))
+        reps = 8
+        e0.record()
+        for _ in range(reps):
+            g_r.replay()
+        e1.record()
+        e1.synchronize()
+        roof_ms[early] = e0.elapsed_time(e1) / (reps * len(glob))
+        del g_r
+    kern_ms = roof_ms[True]
     kern_bytes = decode_layer_bytes(1, p_last)
     achieved = kern_bytes / (kern_ms / 1e3) / 1e9
+    achieved_plain = kern_bytes / (roof_ms[False] / 1e3) / 1e9
     traffic = profile_traffic("attn_decode.cu", "attn_decode_global_262k.md", p_last + 1)
 
     # ---------------------------------------------------------------- e2e ----
@@ -1025,6 +1042,9 @@ def run_gpu(args, rank, world):
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
                      "frac_nominal": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": kern_bytes, "ms_per_launch": kern_ms,
+                     "calls": "as in the timed step (fused append, MG_EARLY_START)",
+                     "achieved_plain_calls": achieved_plain,
+                     "ms_per_launch_plain_calls": roof_ms[False],
                      "traffic": traffic},
         **line_extra,
         "allocator": {"model_global_gib_at_131072": model_global / 2 ** 30,
