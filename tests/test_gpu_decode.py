@@ -288,15 +288,15 @@ def test_local_decode_rounds_peaked(mg, B, case):
         compare(o[b], ref, f"{case} B {B} b {b}")
 
 
-@pytest.mark.parametrize("B", [1, 3, 4])
-def test_append_decode_early_matches_plain(mg, B):
+@pytest.mark.parametrize("bases", [[2040], [100], [2040, 3000, 4090], [2040, 3000, 4090, 100]])
+def test_append_decode_early_matches_plain(mg, bases):
     """mg_append_decode_ex with MG_EARLY_START: a local and a global layer
     decoded in turn for 24 steps (each call's previous kernel is the other
     layer's, which writes neither this cache nor the positions), captured in
     one CUDA graph so that the calls overlap as in a decode step.  Outputs
     and caches equal the plain mg_append_decode run bit for bit, and every
     step's outputs match the oracle."""
-    bases = [2040, 3000, 4090, 100][:B]
+    B = len(bases)
     S = 24
     T = max(bases) + S
     layers = []

@@ -58,7 +58,11 @@ def run_verify(mg, kind, cache, p0s, q, kn, vn, max_len):
                                    ([2032, 2048], 16), ([700, 300], 1),
                                    # blocks that wrap the ring inside themselves, a second
                                    # group of 3 tokens, three sequences
-                                   ([2040, 4090, 9], 11), ([6139, 31], 13), ([4095, 2047], 2)])
+                                   ([2040, 4090, 9], 11), ([6139, 31], 13), ([4095, 2047], 2),
+                                   # eight sequences: local clusters of 4 CTAs walking
+                                   # their ring pieces in rounds, ragged token groups
+                                   ([3, 130, 2047, 2048, 2100, 4095, 5000, 10], 5),
+                                   ([600, 1, 2030, 3000, 4096, 2049, 129, 7000], 13)])
 def test_verify_against_oracle(mg, kind, p0s, n):
     B = len(p0s)
     T = max(p0s) + n
