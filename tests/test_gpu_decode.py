@@ -351,3 +351,34 @@ def test_append_decode_early_matches_plain(mg, bases):
                 ref = orc.attention(olay, L["k"][b, :p + i + 1], L["v"][b, :p + i + 1], [p + i],
                                     L["q"][b, i:i + 1])[0]
                 compare(ob[i, li, b], ref, f"layer kind {L['kind']} step {i} seq {b}")
+
+
+def test_append_decode_early_broken_promise_stays_in_bounds(mg):
+    """MG_EARLY_START right after a kernel that does write the cache (the
+    promise broken on purpose, both layer kinds, batch 1):
+    the result may use stale rows, but every access stays inside the cache,
+    no error is flagged and the outputs are finite."""
+    T = 3000
+    for kind in (0, 1):
+        k, v = synth.history(1, T + 2, 23, 6 + kind)
+        q = synth.queries(1, 1, 23, 6 + kind)[:, 0]
+        cache = fill_for_decode(mg, kind, k[:, :T], v[:, :T], [T - 1], T + 2)
+        lay = mg.make_layer(kind)
+        ws = mg.workspace(mg.OP_DECODE, lay, 1, 1, T + 2)
+        err = mg.error_word()
+        pos = torch.tensor([T], dtype=torch.int32, device="cuda")
+        kn = k[:, T:T + 1].contiguous().cuda()
+        vn = v[:, T:T + 1].contiguous().cuda()
+        qd = q.contiguous().cuda()
+        o = torch.empty((1, 32, 128), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            # the kernel just before the early-start call writes the cache row
+            # at T, which the early start may read before that write lands
+            mg.mg_kv_append(lay, cache, pos, kn, vn, err)
+            mg.mg_append_decode_ex(lay, cache, pos, T + 2, qd, kn, vn, o, ws, err, mg.EARLY_START)
+        g.replay()
+        torch.cuda.synchronize()
+        check_err(err)
+        assert torch.isfinite(o.float()).all()
