@@ -70,6 +70,7 @@ constexpr int kLocTiles = kRound / kDecTile;      // 2 tiles of 64 slots per rou
 constexpr int kRoundSmem = kLocTiles * kDecStageBytes;  // K + V of a round
 constexpr int kPRow = kRound + 8;                 // padded bf16 row of P
 constexpr int kPSmem = kGroup * kPRow * 2;
+static_assert(kPSmem >= kGroup * kD * 2, "the P buffer holds the query tile before the first softmax");
 constexpr int kAngSmem = 2 * 64 * 8;              // R(-b), R(-b - 2048) per frequency
 constexpr int kRedSmem = 2 * kLocWarps * kGroup * 4;
 constexpr int kConstSmem = 3 * 64 * 8;            // turns, step of 8 slots, step of a round
@@ -292,24 +293,33 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   if (tid == 0)
     for (int u = 0; u < kBufs; ++u) issue_round(u);
   int issued = kBufs;  // rounds whose copies went out (thread 0's count)
-  // Q fragments (A operand, 16 heads x 128 dims) straight from memory
+  // Q fragments (A operand, 16 heads x 128 dims)
   uint32_t qf[8][4];
   uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
   const size_t new_src = (static_cast<size_t>(b) * kHkv + g) * kD;  // the new row of (b, g)
+  // The group's 16 query rows (4 KB): one coalesced 16-byte load per thread
+  // into shared memory (the P buffer, unused until the first softmax; rows
+  // 256 bytes apart, 16-byte chunks XOR-swizzled by the row), then ldmatrix
+  // into the A fragments -- far sooner ready than 32 scattered 4-byte loads
+  // per thread.
   auto load_query = [&]() {
-    const __nv_bfloat16 *q0 = p.q + (static_cast<size_t>(b) * kHq + g * kGroup + gr) * kD;
-    const __nv_bfloat16 *q1 = q0 + 8 * kD;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int c = ks * 16 + 2 * tq;
-      qf[ks][0] = __ldg(reinterpret_cast<const unsigned int *>(q0 + c));
-      qf[ks][1] = __ldg(reinterpret_cast<const unsigned int *>(q1 + c));
-      qf[ks][2] = __ldg(reinterpret_cast<const unsigned int *>(q0 + c + 8));
-      qf[ks][3] = __ldg(reinterpret_cast<const unsigned int *>(q1 + c + 8));
-    }
+    const int qr = tid >> 4, qc = tid & 15;
+    const uint4 v4 = __ldg(reinterpret_cast<const uint4 *>(
+                               p.q + (static_cast<size_t>(b) * kHq + g * kGroup + qr) * kD) + qc);
+    const uint32_t qs = smem_u32(pmat);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qs + qr * 256 + ((qc ^ (qr & 7)) << 4)),
+                 "r"(v4.x), "r"(v4.y), "r"(v4.z), "r"(v4.w)
+                 : "memory");
     if (patch_mode)  // the row's address needs no position; only the owning warp uses it
       new_row = lane < 16 ? __ldg(reinterpret_cast<const uint4 *>(p.k_new + new_src) + (lane & 15))
                           : __ldg(reinterpret_cast<const uint4 *>(p.v_new + new_src) + (lane & 15));
+    consumers_sync();
+    const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int chunk = 2 * ks + (lane >> 4);
+      ldsm_x4(qs + row * 256 + ((chunk ^ (row & 7)) << 4), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+    }
   };
   if (!early) load_query();
 
