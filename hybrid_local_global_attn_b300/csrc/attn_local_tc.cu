@@ -88,7 +88,8 @@ template <int kRounds> struct TcLocPlan {
   static constexpr int kOffRed = kOffAng + kAngSmem;
   static constexpr int kOffTurn = kOffRed + kRedSmem;  // 64 turns (uint64), then R(128 w_f)
   static constexpr int kOffBars = kOffTurn + 64 * 8 + 64 * 8;
-  static constexpr int kUsed = kOffBars + 64 + 1024;  // + alignment slack
+  static constexpr int kOffQ = kOffBars + 64;          // raw queries [128 rows][256 B], swizzled
+  static constexpr int kUsed = kOffQ + kTcRows * kD * 2 + 1024;  // + alignment slack
   static constexpr int kSmem = kUsed > kOneCtaPerSm ? kUsed : kOneCtaPerSm;
   static constexpr int kOffStage = kOffK;
   static constexpr int kOffStageLse = kOffK + kLocCluster * kStageOwner;
@@ -265,18 +266,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = 0; u < kVBufs; ++u) issue_v(u);
   }
   int issued_k = 1, issued_v = kVBufs;  // (thread 0's counts)
-  // raw query of row r, dims 32 hh.. and 64 + 32 hh..
-  uint4 qx[4], qy[4];
-  {
-    const bool live = rt < cnt;
-    const __nv_bfloat16 *src =
-        p.q + ((static_cast<size_t>(b) * p.n + i0 + (live ? rt : 0)) * kHq + g * kGroup + (r & 15)) * kD +
-        32 * hh;
+  // The raw queries of the 8 tokens x 16 heads (32 KB), coalesced (a token's
+  // 16 heads are 4 KB in a row), into shared memory: row R = 16 token + head,
+  // 16-byte chunk c at c ^ (R mod 16) so that a warp's per-row reads below
+  // hit distinct banks.
+  const uint32_t sQ = sbase + Plan::kOffQ;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      qx[c] = live ? __ldg(reinterpret_cast<const uint4 *>(src) + c) : make_uint4(0u, 0u, 0u, 0u);
-      qy[c] = live ? __ldg(reinterpret_cast<const uint4 *>(src + 64) + c) : make_uint4(0u, 0u, 0u, 0u);
-    }
+  for (int it = 0; it < 8; ++it) {
+    const int i = it * kThreads + tid, t = i >> 8, R = i >> 4, c = i & 15;  // t = token
+    const uint4 v4 = t < cnt ? __ldg(reinterpret_cast<const uint4 *>(
+                                   p.q + ((static_cast<size_t>(b) * p.n + i0 + t) * kHq + g * kGroup + (R & 15)) * kD) + c)
+                             : make_uint4(0u, 0u, 0u, 0u);
+    sts128(sQ + R * 256 + ((c ^ (R & 15)) << 4), v4);
   }
   // block rows 128..143 of K and V (first CTA): thread tid < 128 takes row
   // tid / 8, 8-dim chunk tid % 8 (and its partner 64 dims on)
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     rope_cos_sin(-(b0 + kWindow * variant), turns[f], cs, sn);
     ang[((f & 31) * 2 + (f >> 5)) * 2 + variant] = make_float2(cs, sn);
   }
+  __syncthreads();  // the raw queries are in shared memory
   // rotated query halves into TMEM: row r, dims 32 hh.. (columns 16 hh..)
   // and 64 + 32 hh.. (columns 32 + 16 hh..)
   {
@@ -307,7 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint4 xh, xl, yh, yl;
-      rot8_split(qx[c], qy[c], qang + 8 * c, xh, xl, yh, yl);
+      const int cx = 4 * hh + c, cy = 8 + 4 * hh + c;  // chunks of dims 32 hh + 8 c and 64 + ..
+      rot8_split(lds128(sQ + r * 256 + ((cx ^ (r & 15)) << 4)), lds128(sQ + r * 256 + ((cy ^ (r & 15)) << 4)),
+                 qang + 8 * c, xh, xl, yh, yl);
       h0[4 * c] = xh.x; h0[4 * c + 1] = xh.y; h0[4 * c + 2] = xh.z; h0[4 * c + 3] = xh.w;
       l0[4 * c] = xl.x; l0[4 * c + 1] = xl.y; l0[4 * c + 2] = xl.z; l0[4 * c + 3] = xl.w;
       h1[4 * c] = yh.x; h1[4 * c + 1] = yh.y; h1[4 * c + 2] = yh.z; h1[4 * c + 3] = yh.w;
