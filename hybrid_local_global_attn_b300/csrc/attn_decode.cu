@@ -37,7 +37,10 @@ namespace mg {
 namespace {
 
 constexpr int kStages = kDecStages;
-constexpr int kSmem = kStages * kDecStageBytes + 1024 + 2 * 8 * kStages + 256;
+// stages, barriers, the query tile [16 rows][256 B], + alignment slack
+constexpr int kOffQ = kStages * kDecStageBytes + 256;
+constexpr int kSmem = kOffQ + kGroup * kD * 2 + 1024;
+static_assert(2 * 8 * kStages <= 256, "barriers fit before the query tile");
 
 }  // namespace
 
@@ -209,18 +212,27 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const int tq = lane & 3;   // thread in quad
     const int tid = threadIdx.x;
 
-    // Q fragments (A operand, 16 heads x 128 dims)
+    // Q fragments (A operand, 16 heads x 128 dims): the group's 4 KB of
+    // query rows with coalesced 16-byte loads into shared memory (rows 256
+    // bytes apart, 16-byte chunks XOR-swizzled by the row), then ldmatrix
     uint32_t qf[8][4];
     {
-      const __nv_bfloat16 *q0 = p.q + (row0 + gr) * kD;
-      const __nv_bfloat16 *q1 = q0 + 8 * kD;
+      const uint32_t qs = smem_base + kOffQ;
+      const int qr = tid >> 3;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = (tid & 7) + 8 * h;
+        const uint4 v4 = __ldg(reinterpret_cast<const uint4 *>(p.q + (row0 + qr) * kD) + c);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qs + qr * 256 + ((c ^ (qr & 7)) << 4)),
+                     "r"(v4.x), "r"(v4.y), "r"(v4.z), "r"(v4.w)
+                     : "memory");
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+      const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const int c = ks * 16 + 2 * tq;
-        qf[ks][0] = __ldg(reinterpret_cast<const unsigned int *>(q0 + c));
-        qf[ks][1] = __ldg(reinterpret_cast<const unsigned int *>(q1 + c));
-        qf[ks][2] = __ldg(reinterpret_cast<const unsigned int *>(q0 + c + 8));
-        qf[ks][3] = __ldg(reinterpret_cast<const unsigned int *>(q1 + c + 8));
+        const int chunk = 2 * ks + (lane >> 4);
+        ldsm_x4(qs + row * 256 + ((chunk ^ (row & 7)) << 4), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
       }
     }
 

@@ -34,8 +34,6 @@ constexpr int kDecStages = 3;             // TMA ring depth (2 CTAs per SM)
 constexpr int kDecWarps = 4;              // consumer warps, 16 keys each per stage
 constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one TMA producer warp
 constexpr int kDecStageBytes = 2 * kDecTile * kRowBytes;  // K + V
-constexpr int kDecSmem = kDecStages * kDecStageBytes + 1024 /*align*/ + 256 /*barriers*/ +
-                         64 * 8 /*rope turns*/;
 constexpr int kDecMaxSplits = 296;
 constexpr int kDecPrefetchTiles = 8;  // L2-prefetched tiles per global-layer CTA
 // FP8 (e4m3) global decode: 128-key stages of 32 KB (K codes + transposed V
