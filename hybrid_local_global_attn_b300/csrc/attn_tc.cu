@@ -553,15 +553,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_ld32(tL + kColO + 64 * hh + 32, oa[1]);
       tmem_wait_ld();
     }
+    // Stage the normalised rows in shared memory (the key buffers: every
+    // MMA has retired) -- a thread holds one row -- then store them with
+    // coalesced 16-byte stores, a warp per row.  Rows are padded by 16
+    // bytes so that the 32 rows a warp stages at once hit distinct banks.
+    const bool part = p.splits > 1;
+    constexpr int kStPadF = kD + 4;  // fp32 partial rows: 528 bytes
+    constexpr int kStPadH = kD + 8;  // bf16 output rows: 272 bytes
+    if (part) {
+      float *st = reinterpret_cast<float *>(smem + Plan::kQ) + r * kStPadF + 64 * hh;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int d0 = 64 * hh + 32 * c;  // first dim of this 32-column chunk
-      const uint32_t *a = oa[c];
-      if (!row_valid) continue;
-      if (p.splits == 1) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD + d0);
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          reinterpret_cast<float4 *>(st + 32 * c)[q4] =
+              make_float4(have ? __uint_as_float(oa[c][4 * q4 + 0]) * inv : 0.f,
+                          have ? __uint_as_float(oa[c][4 * q4 + 1]) * inv : 0.f,
+                          have ? __uint_as_float(oa[c][4 * q4 + 2]) * inv : 0.f,
+                          have ? __uint_as_float(oa[c][4 * q4 + 3]) * inv : 0.f);
+    } else {
+      __nv_bfloat16 *st = reinterpret_cast<__nv_bfloat16 *>(smem + Plan::kQ) + r * kStPadH + 64 * hh;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t *a = oa[c];
           uint4 w;
           w.x = pack_bf16x2(have ? __uint_as_float(a[8 * q4 + 0]) * inv : 0.f,
                             have ? __uint_as_float(a[8 * q4 + 1]) * inv : 0.f);
@@ -571,16 +587,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             have ? __uint_as_float(a[8 * q4 + 5]) * inv : 0.f);
           w.w = pack_bf16x2(have ? __uint_as_float(a[8 * q4 + 6]) * inv : 0.f,
                             have ? __uint_as_float(a[8 * q4 + 7]) * inv : 0.f);
-          dst[q4] = w;
+          reinterpret_cast<uint4 *>(st + 32 * c)[q4] = w;
+        }
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    {
+      const int tsm = threadIdx.x;  // 0..255 (the softmax warps)
+      if (part) {
+#pragma unroll 4
+        for (int i = tsm; i < kTcRows * (kD / 4); i += 256) {
+          const int rr = i >> 5, c4 = i & 31;
+          const int32_t tl = kTcPosPerCta * qb + (rr >> 4);
+          if (tl >= p.n) continue;
+          const size_t orr = (static_cast<size_t>(b) * p.n + tl) * kHq + kGroup * g + (rr & 15);
+          reinterpret_cast<float4 *>(p.part_o + (orr * p.splits + split) * kD)[c4] =
+              reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(smem + Plan::kQ) +
+                                               rr * kStPadF)[c4];
         }
       } else {
-        float4 *dst = reinterpret_cast<float4 *>(p.part_o + (orow * p.splits + split) * kD + d0);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          dst[q4] = make_float4(have ? __uint_as_float(a[4 * q4 + 0]) * inv : 0.f,
-                                have ? __uint_as_float(a[4 * q4 + 1]) * inv : 0.f,
-                                have ? __uint_as_float(a[4 * q4 + 2]) * inv : 0.f,
-                                have ? __uint_as_float(a[4 * q4 + 3]) * inv : 0.f);
+#pragma unroll 4
+        for (int i = tsm; i < kTcRows * (kD / 8); i += 256) {
+          const int rr = i >> 4, c8 = i & 15;
+          const int32_t tl = kTcPosPerCta * qb + (rr >> 4);
+          if (tl >= p.n) continue;
+          const size_t orr = (static_cast<size_t>(b) * p.n + tl) * kHq + kGroup * g + (rr & 15);
+          reinterpret_cast<uint4 *>(p.o + orr * kD)[c8] = reinterpret_cast<const uint4 *>(
+              reinterpret_cast<const __nv_bfloat16 *>(smem + Plan::kQ) + rr * kStPadH)[c8];
+        }
       }
     }
     if (p.splits > 1 && row_valid && hh == 0)
