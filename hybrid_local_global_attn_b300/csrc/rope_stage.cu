@@ -27,11 +27,12 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t 
   lo = pack_bf16x2(a - bf16lo(hi), b - bf16hi(hi));
 }
 
-// Rotate dims i0..i0+7 (x) and their partners i0+64.. (y) by position pos;
+// Rotate dims 8c..8c+7 (x) and their partners 8c+64.. (y) by position pos;
 // the rotated values come back as hi parts in (x, y) and lo parts in
-// (xl, yl).
+// (xl, yl).  tt holds the turns as [e][c] (frequency 8c + e at 8e + c), so
+// that the 8 values of c that a warp's lanes take sit side by side.
 __device__ __forceinline__ void rotate8(uint4 &x, uint4 &y, uint4 &xl, uint4 &yl, int32_t pos,
-                                        int i0, const RopeTurns &rt) {
+                                        int c, const uint64_t *tt) {
   uint32_t *l = reinterpret_cast<uint32_t *>(&x);
   uint32_t *h = reinterpret_cast<uint32_t *>(&y);
   uint32_t *ll = reinterpret_cast<uint32_t *>(&xl);
@@ -39,8 +40,8 @@ __device__ __forceinline__ void rotate8(uint4 &x, uint4 &y, uint4 &xl, uint4 &yl
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     float c0, s0, c1, s1;
-    rope_cos_sin(pos, rt.turn[i0 + 2 * e], c0, s0);
-    rope_cos_sin(pos, rt.turn[i0 + 2 * e + 1], c1, s1);
+    rope_cos_sin(pos, tt[8 * (2 * e) + c], c0, s0);
+    rope_cos_sin(pos, tt[8 * (2 * e + 1) + c], c1, s1);
     const float x0 = bf16lo(l[e]), x1 = bf16hi(l[e]);
     const float y0 = bf16lo(h[e]), y1 = bf16hi(h[e]);
     split2(x0 * c0 - y0 * s0, x1 * c1 - y1 * s1, l[e], ll[e]);
@@ -51,6 +52,11 @@ __device__ __forceinline__ void rotate8(uint4 &x, uint4 &y, uint4 &xl, uint4 &yl
 }  // namespace
 
 __global__ void __launch_bounds__(256) rope_stage_kernel(const __grid_constant__ StageParams p) {
+  // The turns in shared memory, transposed: a warp's lanes index them by
+  // their own 8-dim chunk, which the kernel-parameter bank would serialise.
+  __shared__ uint64_t tt[64];
+  if (threadIdx.x < 64) tt[8 * (threadIdx.x & 7) + (threadIdx.x >> 3)] = p.rope.turn[threadIdx.x];
+  __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -82,7 +88,7 @@ __global__ void __launch_bounds__(256) rope_stage_kernel(const __grid_constant__
       khi = __ldg(reinterpret_cast<const uint4 *>(ksrc + 64 + 8 * c));
       vlo = __ldg(reinterpret_cast<const uint4 *>(vsrc + 8 * c));
       vhi = __ldg(reinterpret_cast<const uint4 *>(vsrc + 64 + 8 * c));
-      rotate8(klo, khi, klo_l, khi_l, static_cast<int32_t>(pos), 8 * c, p.rope);
+      rotate8(klo, khi, klo_l, khi_l, static_cast<int32_t>(pos), c, tt);
     }
     const size_t dst = ((static_cast<size_t>(b) * kHkv + g) * p.R + r) * kD;
     *reinterpret_cast<uint4 *>(p.ks + dst + 8 * c) = klo;
@@ -102,7 +108,7 @@ __global__ void __launch_bounds__(256) rope_stage_kernel(const __grid_constant__
     uint4 lo = __ldg(reinterpret_cast<const uint4 *>(p.q + off + 8 * c));
     uint4 hi = __ldg(reinterpret_cast<const uint4 *>(p.q + off + 64 + 8 * c));
     uint4 lo_l, hi_l;
-    rotate8(lo, hi, lo_l, hi_l, c0 + t, 8 * c, p.rope);
+    rotate8(lo, hi, lo_l, hi_l, c0 + t, c, tt);
     *reinterpret_cast<uint4 *>(p.qs + off + 8 * c) = lo;
     *reinterpret_cast<uint4 *>(p.qs + off + 64 + 8 * c) = hi;
     *reinterpret_cast<uint4 *>(p.qs_lo + off + 8 * c) = lo_l;
