@@ -50,7 +50,10 @@ constexpr int kT = kE4m3Tile;                  // keys per stage (32 per consume
 constexpr int kVT = 64;                        // positions per transposed V tile (layout)
 constexpr int kKBytes = kT * kD;               // 16 KB of K codes per stage
 constexpr int kStage = 2 * kKBytes;            // + 16 KB of V codes (two transposed tiles)
-constexpr int kSmem = NS * kStage + 1024 + 2 * 8 * NS + 256;
+// stages, barriers, the query tile [16 rows][256 B], + alignment slack
+constexpr int kOffQ = NS * kStage + 256;
+constexpr int kSmem = kOffQ + kGroup * kD * 2 + 1024;
+static_assert(2 * 8 * NS <= 256, "barriers fit before the query tile");
 
 // Four e4m3 codes (bytes 0..3 of x) -> two f16 x2 (bytes 0, 1 and bytes 2,
 // 3; lower byte to the lower half), exact: one conversion per 16-bit half,
@@ -210,14 +213,32 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     uint32_t qf[8][4];
     float sl2[2];
     {
-      const __nv_bfloat16 *qr[2] = {p.q + (row0 + gr) * kD, p.q + (row0 + gr + 8) * kD};
+      // the group's 4 KB of query rows with coalesced 16-byte loads into
+      // shared memory (rows 256 bytes apart, 16-byte chunks XOR-swizzled by
+      // the row), then each lane's 8-byte pieces from there
+      const uint32_t qs = smem_base + kOffQ;
+      {
+        const int qrow = tid >> 3;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int c = (tid & 7) + 8 * h2;
+          const uint4 v4 = __ldg(reinterpret_cast<const uint4 *>(p.q + (row0 + qrow) * kD) + c);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qs + qrow * 256 + ((c ^ (qrow & 7)) << 4)),
+                       "r"(v4.x), "r"(v4.y), "r"(v4.z), "r"(v4.w)
+                       : "memory");
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+      }
       uint2 raw[2][8];
       float amax[2] = {0.f, 0.f};
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          raw[h][ks] = __ldg(reinterpret_cast<const uint2 *>(qr[h] + ks * 16 + 4 * tq));
+          const int row = gr + 8 * h, chunk = 2 * ks + (tq >> 1);
+          asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                       : "=r"(raw[h][ks].x), "=r"(raw[h][ks].y)
+                       : "r"(qs + row * 256 + ((chunk ^ (row & 7)) << 4) + 8 * (tq & 1)));
           amax[h] = fmaxf(amax[h], fmaxf(fmaxf(fabsf(bf16lo(raw[h][ks].x)), fabsf(bf16hi(raw[h][ks].x))),
                                          fmaxf(fabsf(bf16lo(raw[h][ks].y)), fabsf(bf16hi(raw[h][ks].y)))));
         }

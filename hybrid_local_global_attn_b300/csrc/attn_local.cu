@@ -230,8 +230,17 @@ __global__ void __launch_bounds__(kLocThreads, 1)
     return w;
   };
 
-  // ---- prologue: reads only kernel parameters, so it overlaps the previous
-  // kernel under programmatic dependent launch ----
+  // Early start (single-round kernel, caller's promise that the kernel
+  // before this one writes neither the ring nor the positions): the
+  // position, the ring tiles, the R(-b) table and the rotated keys are all
+  // prepared before the dependency wait; only the query and the new row --
+  // which that kernel may produce -- are read after it.
+  bool early = false;
+  if constexpr (kRounds == 1) early = p.early != 0;
+
+  // ---- prologue: reads only kernel parameters (and, with the early start,
+  // the ring), so it overlaps the previous kernel under programmatic
+  // dependent launch ----
   if (tid == 0) {
     abort_flag = 0;
     for (int t = 0; t < kBufs * kLocTiles; ++t) mbar_init(bar_full + 8 * t, 1);
@@ -239,6 +248,7 @@ __global__ void __launch_bounds__(kLocThreads, 1)
     fence_mbar_init();
     // every CTA of the cluster pushes one row and one lse per owned head
     mbar_arrive_expect_tx(bar_inbox, Plan::kInboxBytes);
+    if (early) issue_round(0);  // the piece does not depend on the position
   }
   if (tid < 64) {
     turns[tid] = p.turn[tid];
@@ -249,7 +259,14 @@ __global__ void __launch_bounds__(kLocThreads, 1)
       step_round[tid] = make_float2(cs, sn);
     }
   }
-  if (tid == 0) {
+  // The query rows and the new token's K/V rows may come from the kernel
+  // before this one: only their L2 lines are fetched before the wait.
+  if (warp == 1) {
+    prefetch_l2(p.q + (static_cast<size_t>(b) * kHq + g * kGroup) * kD + 64 * lane);
+    if (patch_mode && lane < 4)
+      prefetch_l2((lane < 2 ? p.k_new : p.v_new) + (static_cast<size_t>(b) * kHkv + g) * kD + 64 * (lane & 1));
+  }
+  if (tid == 0 && !early) {
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
     for (int t = 0; t < kBufs * kLocTiles; ++t)
@@ -273,13 +290,6 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   // First half of a cluster barrier whose wait (before the first store into
   // another CTA's shared memory) proves every CTA of the cluster is running.
   cluster_arrive_relaxed();
-  // Early start (single-round kernel, caller's promise that the kernel
-  // before this one writes neither the ring nor the positions): the
-  // position, the ring tiles, the R(-b) table and the rotated keys are all
-  // prepared before the dependency wait; only the query and the new row --
-  // which that kernel may produce -- are read after it.
-  bool early = false;
-  if constexpr (kRounds == 1) early = p.early != 0;
   if (!early) {
     pdl_wait();
     pdl_launch_dependents();
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   // the query and the new row (for an invalid position they are read and
   // then dropped).
   const int32_t pq = p.pos[b];
-  if (tid == 0)
+  if (tid == 0 && !early)
     for (int u = 0; u < kBufs; ++u) issue_round(u);
   int issued = kBufs;  // rounds whose copies went out (thread 0's count)
   // Q fragments (A operand, 16 heads x 128 dims)

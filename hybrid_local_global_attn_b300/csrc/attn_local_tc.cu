@@ -225,6 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_l2_3d(&tv, 64 * x, s0, head);
     }
   }
+  // The raw queries and the block's K/V rows may come from the kernel
+  // before this one: only their L2 lines are fetched before the wait.
+  if ((tid >> 5) < cnt)
+    prefetch_l2(p.q + ((static_cast<size_t>(b) * p.n + i0 + (tid >> 5)) * kHq + g * kGroup) * kD +
+                64 * (tid & 31));
+  if (blk_here && tid < 4 * p.n)
+    prefetch_l2(((tid >> 1) & 1 ? p.v_new : p.k_new) +
+                ((static_cast<size_t>(b) * p.n + (tid >> 2)) * kHkv + g) * kD + 64 * (tid & 1));
   if (warp == 0) {
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tmem_relinquish();

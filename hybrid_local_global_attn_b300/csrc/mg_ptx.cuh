@@ -116,6 +116,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// Bring the 128-byte line holding `a` into L2 (no data reaches the thread).
+// Issued before a dependency wait on a buffer the previous kernel may still
+// write, it is harmless: L2 is where those writes land, so the loads after
+// the wait see them, only sooner.
+__device__ __forceinline__ void prefetch_l2(const void *a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(a)) : "memory");
+}
+
 // Warm L2 with a box of a tensor (no shared-memory write, no completion
 // tracking); later loads of the same box then hit L2.
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *m, int32_t c0, int32_t c1,
