@@ -8,8 +8,10 @@
 // RoPE; 16 query heads share one KV head.
 //
 // Design (HBM-bound: every K/V byte is read once):
-//  * One CTA per (split, KV head, sequence), two CTAs per SM; the splits cut
-//    [0, p] into equal runs of 64-key tiles.
+//  * One CTA per (split, KV head, sequence), two CTAs per SM; split s of S
+//    takes the 64-key tiles s, s + S, s + 2S, ... of [0, p], so that at any
+//    moment the CTAs stream neighbouring tiles (contiguous runs per split
+//    were ~2.5 % slower).
 //  * A producer warp streams the tiles with TMA (128-byte swizzle, two
 //    64-dim boxes per tile) through a 3-stage mbarrier ring; before the
 //    dependency wait it warms L2 with the first tiles of the range the split
@@ -77,15 +79,14 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     // kernel is still running.  The range is what the split gets when the
     // query sits at max_len - 1; only a prefetch -- the loads that feed the
     // math come after pdl_wait().
-    int32_t c = (p.max_len + p.splits - 1) / p.splits;
-    c = (c + kDecTile - 1) / kDecTile * kDecTile;
-    const int32_t first = split * c;
-    const int32_t upto = min(first + min(c, kDecPrefetchTiles * kDecTile), min(p.max_len, p.slots));
     // (a paged cache's table may still be changing: a stale entry only
     // warms the wrong page)
-    for (int32_t row = first; row < upto; row += kDecTile) {
-      int32_t r, o;
-      cache_coord(p.map, b, g, row, &r, &o, nullptr);
+    const int32_t lim = min(p.max_len, p.slots);
+    for (int t = 0; t < kDecPrefetchTiles; ++t) {
+      const int32_t pos = (split + t * p.splits) * kDecTile;
+      if (pos >= lim) break;
+      int32_t r = pos, o = b * kHkv + g;
+      if (p.map.table != nullptr) cache_coord(p.map, b, g, pos, &r, &o, nullptr);
       for (int x = 0; x < 2; ++x) {
         tma_prefetch_l2_3d(&tk, 64 * x, r, o);
         tma_prefetch_l2_3d(&tv, 64 * x, r, o);
@@ -106,20 +107,19 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const int32_t pq = p.pos[b];
   const bool bad = pq < 0 || pq >= p.max_len || pq >= p.slots;
   const int32_t n_slots = bad ? 0 : pq + 1;
-  int32_t chunk = (n_slots + p.splits - 1) / p.splits;
-  chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
-  const int32_t s0 = split * chunk;
-  const int32_t s1 = min(s0 + chunk, n_slots);
-  const bool empty = bad || s0 >= s1;
-  const int ntiles = empty ? 0 : (s1 - s0 + kDecTile - 1) / kDecTile;
+  const int32_t n_tiles_all = (n_slots + kDecTile - 1) / kDecTile;  // tiles of [0, p]
+  const int ntiles = split < n_tiles_all ? (n_tiles_all - split + p.splits - 1) / p.splits : 0;
+  const bool empty = ntiles == 0;
+  // first slot of the CTA's t-th tile (keys at or past n_slots are masked)
+  auto tile_pos = [&](int t) -> int32_t { return (split + t * p.splits) * kDecTile; };
   const size_t row0 = static_cast<size_t>(b) * kHq + g * kGroup;  // first query row of the group
-  const bool fused_here = p.k_new != nullptr && !empty && pq >= s0 && pq < s1;
+  const bool fused_here = p.k_new != nullptr && !empty && (pq / kDecTile) % p.splits == split;
   // tiles issued before the wait (early start, linear cache): the first
   // stages, short of the tile that will hold the new row
   int npre = 0;
   if (early && warp == kDecWarps && lane == 0 && !empty && p.map.table == nullptr) {
     npre = min(NS, ntiles);
-    if (fused_here) npre = min(npre, (pq - s0) / kDecTile);
+    if (fused_here) npre = min(npre, (pq / kDecTile) / p.splits);
     for (int t = 0; t < npre; ++t) {
       if (t == p.stall_tile) {
         npre = t;
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
       const uint32_t dst = smem_base + t * kDecStageBytes;
       const uint32_t fb = bar_full + 8 * t;
-      const int32_t row = s0 + t * kDecTile;
+      const int32_t row = tile_pos(t);
       mbar_arrive_expect_tx(fb, kDecStageBytes);
       tma_load_3d(dst, &tk, fb, 0, row, b * kHkv + g);
       tma_load_3d(dst + 8192, &tk, fb, 64, row, b * kHkv + g);
@@ -170,12 +170,17 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
       if (lane == 0) {
         int issued = npre;
-        // a tile never straddles two pages (64 | split start, 256 | page size);
-        // the page entry is reloaded only when the tile enters a new page
-        int32_t cur_lp = -1, cur_row0 = 0, cur_outer = b * kHkv + g;
+        // A tile never straddles two pages (64 | 256 | page size).  The
+        // coordinates of the next tile (a page-table load for a paged
+        // cache) are fetched while the producer waits for a free stage.
+        const bool paged = p.map.table != nullptr;
+        int32_t nrow = 0, nouter = b * kHkv + g;
+        if (paged && npre < ntiles) cache_coord(p.map, b, g, tile_pos(npre), &nrow, &nouter, p.err);
         for (int t = npre; t < ntiles; ++t) {
           const int st = t % NS;
           if (t == p.stall_tile) break;  // self-test: tiles from here on never arrive
+          const int32_t row = paged ? nrow : tile_pos(t), outer = nouter;
+          if (paged && t + 1 < ntiles) cache_coord(p.map, b, g, tile_pos(t + 1), &nrow, &nouter, p.err);
           if (t >= NS &&
               !mbar_wait(bar_empty + 8 * st, ((t / NS) - 1) & 1, &abort_flag, p.wait_ns)) {
             abort_flag = 1;
@@ -184,19 +189,11 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           }
           const uint32_t dst = smem_base + st * kDecStageBytes;
           const uint32_t fb = bar_full + 8 * st;
-          const int32_t pos = s0 + t * kDecTile;
-          if (p.map.table != nullptr && pos / p.map.rows != cur_lp) {
-            cur_lp = pos / p.map.rows;
-            int32_t r;
-            cache_coord(p.map, b, g, pos, &r, &cur_outer, p.err);
-            cur_row0 = cur_lp * p.map.rows;
-          }
-          const int32_t row = pos - cur_row0;
           mbar_arrive_expect_tx(fb, kDecStageBytes);
-          tma_load_3d(dst, &tk, fb, 0, row, cur_outer);
-          tma_load_3d(dst + 8192, &tk, fb, 64, row, cur_outer);
-          tma_load_3d(dst + 16384, &tv, fb, 0, row, cur_outer);
-          tma_load_3d(dst + 24576, &tv, fb, 64, row, cur_outer);
+          tma_load_3d(dst, &tk, fb, 0, row, outer);
+          tma_load_3d(dst + 8192, &tk, fb, 64, row, outer);
+          tma_load_3d(dst + 16384, &tv, fb, 0, row, outer);
+          tma_load_3d(dst + 24576, &tv, fb, 64, row, outer);
           ++issued;
         }
         // Never leave the CTA with copies in flight: wait (bounded) for the
@@ -258,8 +255,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         ok = false;
         break;
       }
-      const int32_t key0 = s0 + t * kDecTile + warp * 16;  // slot of this warp's first key
-      if (key0 < s1) {
+      const int32_t key0 = tile_pos(t) + warp * 16;  // slot of this warp's first key
+      if (key0 < n_slots) {
         const uint32_t kbase = smem_base + st * kDecStageBytes;
         const uint32_t vbase = kbase + 16384;
         float sacc[2][4];
@@ -284,7 +281,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int32_t key = key0 + 8 * j + 2 * tq + (e & 1);
-            sacc[j][e] = (key < s1) ? sacc[j][e] * sl2 : -INFINITY;
+            sacc[j][e] = (key < n_slots) ? sacc[j][e] * sl2 : -INFINITY;
           }
         }
         float mx0 = fmaxf(fmaxf(sacc[0][0], sacc[0][1]), fmaxf(sacc[1][0], sacc[1][1]));
@@ -293,7 +290,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: key0 < s1
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: key0 < n_slots
         const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
         m0 = mn0;
         m1 = mn1;

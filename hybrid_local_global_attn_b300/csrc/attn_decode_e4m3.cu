@@ -14,6 +14,8 @@
 // group in the column order c(j) = 4 ((j % 8) / 2) + 2 (j / 8) + j % 2.
 //
 // Design (differences from the bf16 kernel):
+//  * Split s of S takes the 128-key tiles s, s + S, s + 2S, ... (as the
+//    bf16 kernel does with its 64-key tiles).
 //  * A stage is 128 keys: 16 KB of K (one 128-byte-swizzled box) + 16 KB
 //    of V (one 64-byte-swizzled box of two transposed tiles); 3 stages in
 //    flight, 2 CTAs per SM.  Each of the 4 consumer warps takes 32 keys of a
@@ -113,11 +115,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     tma_prefetch_desc(&tv);
     // warm L2 with the first tiles of the range the split gets when the
     // query sits at max_len - 1 (a prefetch only)
-    int32_t c = (p.max_len + p.splits - 1) / p.splits;
-    c = (c + kT - 1) / kT * kT;
-    const int32_t first = split * c;
-    const int32_t upto = min(first + min(c, kE4m3PrefetchTiles * kT), min(p.max_len, p.slots));
-    for (int32_t row = first; row < upto; row += kT) {
+    const int32_t lim = min(p.max_len, p.slots);
+    for (int t = 0; t < kE4m3PrefetchTiles; ++t) {
+      const int32_t row = (split + t * p.splits) * kT;
+      if (row >= lim) break;
       tma_prefetch_l2_3d(&tk, 0, row, c2);
       tma_prefetch_l2_4d(&tv, 0, 0, row / kVT, c2);
     }
@@ -129,12 +130,12 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const int32_t pq = p.pos[b];
   const bool bad = pq < 0 || pq >= p.max_len || pq >= p.slots;
   const int32_t n_slots = bad ? 0 : pq + 1;
-  int32_t chunk = (n_slots + p.splits - 1) / p.splits;
-  chunk = (chunk + kT - 1) / kT * kT;
-  const int32_t s0 = split * chunk;
-  const int32_t s1 = min(s0 + chunk, n_slots);
-  const bool empty = bad || s0 >= s1;
-  const int ntiles = empty ? 0 : (s1 - s0 + kT - 1) / kT;
+  // split s of S takes the tiles s, s + S, s + 2S, ... of [0, p]: at any
+  // moment the CTAs stream neighbouring tiles
+  const int32_t n_tiles_all = (n_slots + kT - 1) / kT;
+  const int ntiles = split < n_tiles_all ? (n_tiles_all - split + p.splits - 1) / p.splits : 0;
+  const bool empty = ntiles == 0;
+  auto tile_pos = [&](int t) -> int32_t { return (split + t * p.splits) * kT; };
   const size_t row0 = static_cast<size_t>(b) * kHq + g * kGroup;
   if (bad && split == 0 && threadIdx.x == 0) set_err(p.err, MG_DERR_POSITION);
   auto part_o = [&](int r, int d) -> float & {
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   };
   auto part_lse = [&](int r) -> float & { return p.part_lse[(row0 + r) * p.splits + split]; };
 
-  const bool fused_here = p.k_new != nullptr && !empty && pq >= s0 && pq < s1;
+  const bool fused_here = p.k_new != nullptr && !empty && (pq / kT) % p.splits == split;
   bool ok = true;
   if (warp == kDecWarps) {
     // ------------------------------------------------ TMA producer warp ----
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           }
           const uint32_t dst = smem_base + st * kStage;
           const uint32_t fb = bar_full + 8 * st;
-          const int32_t row = s0 + t * kT;
+          const int32_t row = tile_pos(t);
           mbar_arrive_expect_tx(fb, kStage);
           tma_load_3d(dst, &tk, fb, 0, row, c2);                   // 128 keys x 128 dims
           tma_load_4d(dst + kKBytes, &tv, fb, 0, 0, row / kVT, c2);  // two transposed tiles
@@ -280,8 +281,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         break;
       }
       // this warp: keys key0 .. key0 + 31 of the tile, as two groups of 16
-      const int32_t key0 = s0 + t * kT + warp * 32;
-      if (key0 < s1) {
+      const int32_t key0 = tile_pos(t) + warp * 32;
+      if (key0 < n_slots) {
         const uint32_t kbase = smem_base + st * kStage;
         const uint32_t vbase = kbase + kKBytes;
         float sacc[2][2][4];  // [group][8-key block][fragment]
@@ -312,7 +313,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int32_t key = key0 + 16 * kg + 8 * j + 2 * tq + (e & 1);
-              sacc[kg][j][e] = (key < s1) ? sacc[kg][j][e] * sl2[e >> 1] : -INFINITY;
+              sacc[kg][j][e] = (key < n_slots) ? sacc[kg][j][e] * sl2[e >> 1] : -INFINITY;
             }
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll

@@ -36,8 +36,10 @@
 // Per key tile: S = Q K^T, softmax in registers with a lazily rescaled
 // running max (rescale only when the max grows by more than 2^8), P to TMEM,
 // O += P V (V as an MN-major operand).
-// Splits (verify): the cache part is cut across CTAs; each writes (o/l, lse)
-// and the combine kernel merges them.
+// Splits (verify): the cache part is cut across CTAs, split s of S taking
+// every S-th key tile (s, s + S, ...: the CTAs then stream neighbouring
+// tiles at any moment); each writes (o/l, lse) and the combine kernel
+// merges them.
 //
 // Local layers (operands staged by rope_stage, rotated by their absolute
 // positions) run the precise form of the kernel: queries and keys arrive as
@@ -76,10 +78,11 @@ struct TileInfo {
   int32_t cbase;          // cache tiles end here: c0, or c0 rounded up to 256 (paged)
   int32_t ncache, nnew;   // tiles from the cache part / the block part
   int32_t u_begin, v_lo;  // first cache tile index (from cbase down), first block tile
+  int32_t u_step;         // cache tile index step between a CTA's tiles (the split count)
 };
 
 __device__ __forceinline__ int32_t tile_kp0(const TileInfo &ti, int t) {
-  if (t < ti.ncache) return ti.cbase - kTcKeys * (ti.u_begin + t + 1);
+  if (t < ti.ncache) return ti.cbase - kTcKeys * (ti.u_begin + t * ti.u_step + 1);
   return ti.c0 + kTcKeys * (ti.v_lo + (t - ti.ncache));
 }
 
@@ -137,12 +140,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   ti.qa = ti.c0 + kTcPosPerCta * qb;
   ti.qz = min(ti.qa + kTcPosPerCta - 1, ti.c0 + p.n - 1);
   ti.ncache = ti.nnew = ti.u_begin = ti.v_lo = 0;
+  ti.u_step = p.splits;
   if (!bad) {
     const int32_t lo = local ? max(0, ti.qa - p.window + 1) : 0;
     const int32_t U = ti.c0 > lo ? (ti.c0 - lo + kTcKeys - 1) / kTcKeys : 0;
-    ti.u_begin = static_cast<int32_t>(static_cast<int64_t>(split) * U / p.splits);
-    const int32_t u_end = static_cast<int32_t>(static_cast<int64_t>(split + 1) * U / p.splits);
-    ti.ncache = u_end - ti.u_begin;
+    // split s takes the cache tiles s, s + S, s + 2S, ... (S splits)
+    ti.u_begin = split;
+    ti.ncache = split < U ? (U - split + p.splits - 1) / p.splits : 0;
     if (split == p.splits - 1) {
       ti.v_lo = local ? max(0, ti.qa - p.window + 1 - ti.c0) / kTcKeys : 0;
       const int32_t v_hi = (ti.qz - ti.c0) / kTcKeys;

@@ -84,7 +84,7 @@ def test_decode_scaled_queries(mg, kind, factor):
 
 @pytest.mark.parametrize("kind,p,sink", [
     (1, 39999, 5),       # first tile of split 0: one split's lse ~40 above the rest
-    (1, 39999, 39996),   # last tile of the last split: the running max jumps at the end
+    (1, 39999, 39996),   # the last tile its split visits: the running max jumps at the end
     (1, 2047, 2047),     # the query's own key, one split per KV head at batch 3
     (0, 5000, 3100),     # one ring piece of the cluster dominates the merge
     (0, 5000, 4998),     # the piece just below the query's slot
@@ -137,7 +137,7 @@ def test_verify_scaled_queries(mg, kind, factor):
 
 
 @pytest.mark.parametrize("kind,sinks", [
-    (1, [5]),              # last cache tile of split 0: split lse far apart
+    (1, [5]),              # the lowest cache tile (its split's only one): split lse far apart
     (1, [4000, 5010]),     # a cache sink, then one inside the block for tokens >= 10
     (0, [3600]),           # one ring piece dominates the cluster merge
     (0, [4990, 5007]),     # ring sink, then a block sink (token 7 onwards)
