@@ -39,6 +39,7 @@ namespace mg {
 namespace {
 
 constexpr int kStages = kDecStages;
+constexpr int kPageAhead = 128;  // paged cache: tiles whose pages are looked up together
 // stages, barriers, the query tile [16 rows][256 B], + alignment slack
 constexpr int kOffQ = kStages * kDecStageBytes + 256;
 constexpr int kSmem = kOffQ + kGroup * kD * 2 + 1024;
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   constexpr int NS = kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
+  __shared__ int32_t page_outer[kPageAhead];  // outer index of the CTA's first tiles (paged)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NS * kDecStageBytes);
@@ -72,19 +74,19 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     }
     fence_mbar_init();
   }
-  if (warp == kDecWarps && lane == 0) {
-    tma_prefetch_desc(&tk);
-    tma_prefetch_desc(&tv);
-    // Warm L2 with the first tiles this CTA will stream while the previous
-    // kernel is still running.  The range is what the split gets when the
-    // query sits at max_len - 1; only a prefetch -- the loads that feed the
-    // math come after pdl_wait().
-    // (a paged cache's table may still be changing: a stale entry only
-    // warms the wrong page)
-    const int32_t lim = min(p.max_len, p.slots);
-    for (int t = 0; t < kDecPrefetchTiles; ++t) {
-      const int32_t pos = (split + t * p.splits) * kDecTile;
-      if (pos >= lim) break;
+  if (warp == kDecWarps) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+    }
+    // Warm L2 with the CTA's first tiles while the previous kernel is still
+    // running, one lane per tile (a paged cache's table loads then run side
+    // by side); only a prefetch -- the loads that feed the math come after
+    // pdl_wait().  (A paged cache's table may still be changing: a stale
+    // entry only warms the wrong page.)
+    static_assert(kDecPrefetchTiles <= 32, "one lane per prefetched tile");
+    const int32_t pos = (split + lane * p.splits) * kDecTile;
+    if (lane < kDecPrefetchTiles && pos < min(p.max_len, p.slots)) {
       int32_t r = pos, o = b * kHkv + g;
       if (p.map.table != nullptr) cache_coord(p.map, b, g, pos, &r, &o, nullptr);
       for (int x = 0; x < 2; ++x) {
@@ -168,19 +170,35 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         fence_proxy_async_global();
         __syncwarp();
       }
+      // A tile never straddles two pages (64 | 256 | page size).  Paged
+      // cache: the warp's lanes look up the pages of the CTA's first
+      // kPageAhead tiles together (one round of parallel table loads); a
+      // later tile's page is fetched one tile ahead by the issuing lane.
+      const bool paged = p.map.table != nullptr;
+      if (paged) {
+        for (int t = lane; t < min(ntiles, kPageAhead); t += 32) {
+          int32_t r, o;
+          cache_coord(p.map, b, g, tile_pos(t), &r, &o, p.err);
+          page_outer[t] = o;
+        }
+        __syncwarp();
+      }
       if (lane == 0) {
         int issued = npre;
-        // A tile never straddles two pages (64 | 256 | page size).  The
-        // coordinates of the next tile (a page-table load for a paged
-        // cache) are fetched while the producer waits for a free stage.
-        const bool paged = p.map.table != nullptr;
-        int32_t nrow = 0, nouter = b * kHkv + g;
-        if (paged && npre < ntiles) cache_coord(p.map, b, g, tile_pos(npre), &nrow, &nouter, p.err);
+        int32_t nrow = 0, nouter = 0;
+        if (paged && kPageAhead < ntiles) cache_coord(p.map, b, g, tile_pos(kPageAhead), &nrow, &nouter, p.err);
         for (int t = npre; t < ntiles; ++t) {
           const int st = t % NS;
           if (t == p.stall_tile) break;  // self-test: tiles from here on never arrive
-          const int32_t row = paged ? nrow : tile_pos(t), outer = nouter;
-          if (paged && t + 1 < ntiles) cache_coord(p.map, b, g, tile_pos(t + 1), &nrow, &nouter, p.err);
+          int32_t row = tile_pos(t), outer = b * kHkv + g;
+          if (paged && t < kPageAhead) {
+            row %= p.map.rows;
+            outer = page_outer[t];
+          } else if (paged) {
+            row = nrow;
+            outer = nouter;
+            if (t + 1 < ntiles) cache_coord(p.map, b, g, tile_pos(t + 1), &nrow, &nouter, p.err);
+          }
           if (t >= NS &&
               !mbar_wait(bar_empty + 8 * st, ((t / NS) - 1) & 1, &abort_flag, p.wait_ns)) {
             abort_flag = 1;
