@@ -386,8 +386,10 @@ def leg_pr1(wl, P0=2000, steps=256):
     def fused(early=False):
         for i in range(steps):
             for j in range(2):
-                append_decode(early, layers[j], caches[j], pos[i:i + 1], T, q[i, j], kn[i, j],
-                              vn[i, j], o[i, j], ws[j], err)
+                # MG_EARLY_START only: the steps follow each other in one
+                # graph, and a layer's next step reads the row this one appends
+                append_decode(mg.EARLY_START if early else 0, layers[j], caches[j], pos[i:i + 1], T,
+                              q[i, j], kn[i, j], vn[i, j], o[i, j], ws[j], err)
 
     us_sep = _graph_us(separate, reps=5, calls=steps)
     us_fused = _graph_us(fused, reps=5, calls=steps)
@@ -542,14 +544,23 @@ def leg_verify(wl):
             "commit_us_52_layers": c1_ms * 1e3, "commit_us_52_layers_per_layer_calls": c_ms * 1e3}
 
 
-def append_decode(early, *args):
-    """mg_append_decode, or mg_append_decode_ex with MG_EARLY_START when the
-    previous kernel is known to leave this call's cache and position alone."""
+def append_decode(flags, *args):
+    """mg_append_decode (flags 0), or mg_append_decode_ex with the given flags."""
     from hybrid_local_global_attn_b300 import mg
-    if early:
-        mg.mg_append_decode_ex(*args, mg.EARLY_START)
+    if flags:
+        mg.mg_append_decode_ex(*args, flags)
     else:
         mg.mg_append_decode(*args)
+
+
+def step_flags():
+    """The flags of the calls of one decode step: every call's cache and
+    position are written by no other call of the step (the positions are
+    set before it), and consecutive steps are separate graph launches or
+    have a position update between them, so each call may start loading
+    under all the calls before it in the step."""
+    from hybrid_local_global_attn_b300 import mg
+    return mg.EARLY_START | mg.OVERLAP_NEXT
 
 
 def _graph_us(fn, reps=8, calls=1):
@@ -723,7 +734,8 @@ def leg_sweep(wl, hbm_peak, ctx=32768, batches=(1, 4, 16), steps=128):
 
         def step():
             for l in range(N_LAYERS):
-                append_decode(True, layers[l], caches[l], pos, cap, q[l], kn[l], vn[l], o[l], ws[l], err)
+                append_decode(step_flags(), layers[l], caches[l], pos, cap, q[l], kn[l], vn[l], o[l],
+                              ws[l], err)
 
         step()
         torch.cuda.synchronize()
@@ -826,14 +838,14 @@ def run_gpu(args, rank, world):
     pos_cur = stage_view(qb + 2 * kvb, 4, torch.int32, (1,))
     o_cur = torch.empty((N_LAYERS, 1, 32, 128), dtype=torch.bfloat16, device=dev)
 
-    # Every decode call of a step follows another layer's kernels, which
-    # write neither its cache nor the position: the calls pass
-    # MG_EARLY_START, so each layer's cache loads start under the previous
-    # layer's tail (the plain-call step is timed too, below).
+    # No decode call of a step writes another call's cache or the position
+    # (set before the step): the calls pass MG_EARLY_START | MG_OVERLAP_NEXT,
+    # so each layer's cache loads start under the layers before it (the
+    # plain-call step is timed too, below).
     def decode_step(early=True):
         for l in range(N_LAYERS):
-            append_decode(early, layers[l], caches[l], pos_cur, cap, q_cur[l], k_cur[l], v_cur[l],
-                          o_cur[l], ws_dec[l], err)
+            append_decode(step_flags() if early else 0, layers[l], caches[l], pos_cur, cap, q_cur[l],
+                          k_cur[l], v_cur[l], o_cur[l], ws_dec[l], err)
 
     def stage(i):
         pos_cur.fill_(PROMPT + i)
@@ -858,7 +870,8 @@ def run_gpu(args, rank, world):
 
     def decode_step_at(i, early=True):
         for l in range(N_LAYERS):
-            append_decode(early, layers[l], caches[l], pos_steps[i:i + 1], cap, wl.dec_q[i, l],
+            append_decode(step_flags() if early else 0, layers[l], caches[l], pos_steps[i:i + 1], cap,
+                          wl.dec_q[i, l],
                           wl.dec_k[i, l], wl.dec_v[i, l], o_cur[l], ws_dec[l], err)
 
     step_graphs = []
@@ -923,7 +936,7 @@ def run_gpu(args, rank, world):
     def roof_pass(early):
         for l in glob:
             if early:
-                append_decode(True, layers[l], caches[l], pos_r, cap, wl.dec_q[i_last, l],
+                append_decode(step_flags(), layers[l], caches[l], pos_r, cap, wl.dec_q[i_last, l],
                               wl.dec_k[i_last, l], wl.dec_v[i_last, l], o_cur[l], ws_dec[l], err)
             else:
                 mg.mg_attn_decode(layers[l], caches[l], pos_r, cap, wl.dec_q[i_last, l], o_cur[l],
@@ -978,7 +991,7 @@ def run_gpu(args, rank, world):
         v2 = sd[qb + kvb:qb + 2 * kvb].view(torch.bfloat16).view(N_LAYERS, 1, 1, 2, 128)
         p2 = sd[qb + 2 * kvb:qb + 2 * kvb + 4].view(torch.int32)
         for l in range(N_LAYERS):
-            append_decode(True, layers[l], caches[l], p2, cap, q2[l], k2[l], v2[l], out2[1][l],
+            append_decode(step_flags(), layers[l], caches[l], p2, cap, q2[l], k2[l], v2[l], out2[1][l],
                           ws_dec[l], err)
     graphs2.append(g2)
     main = torch.cuda.current_stream()
@@ -1034,7 +1047,7 @@ def run_gpu(args, rank, world):
             "cache_fill": "prefill" if args.fill != "random" else "random (profiling run)"},
         "pct_of_8tbs": gbs / world / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": gbs / world / hbm_peak,
-        "decode_calls": "mg_append_decode_ex with MG_EARLY_START (cache loads start under the previous layer)",
+        "decode_calls": "mg_append_decode_ex with MG_EARLY_START | MG_OVERLAP_NEXT (a layer's cache loads start under the layers before it in the step)",
         "plain_calls_us_per_step": plain_us,
         "roofline": {"bound": "hbm", "kernel": "attn_decode (split-KV pass + combine), global "
                                               "layer at context 131072+",
@@ -1042,7 +1055,7 @@ def run_gpu(args, rank, world):
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
                      "frac_nominal": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": kern_bytes, "ms_per_launch": kern_ms,
-                     "calls": "as in the timed step (fused append, MG_EARLY_START)",
+                     "calls": "as in the timed step (fused append, MG_EARLY_START | MG_OVERLAP_NEXT)",
                      "achieved_plain_calls": achieved_plain,
                      "ms_per_launch_plain_calls": roof_ms[False],
                      "traffic": traffic},

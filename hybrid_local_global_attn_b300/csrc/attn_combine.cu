@@ -20,8 +20,10 @@ constexpr int kCombineParts = kD / 32;  // CTAs per row, 32 dims each
 }
 
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
+  // MG_OVERLAP_NEXT: the next kernel may begin at once
+  if (p.overlap) pdl_launch_dependents();
   pdl_wait();  // the partials come from the previous kernel
-  pdl_launch_dependents();
+  if (!p.overlap) pdl_launch_dependents();
   __shared__ float red[kCombineWarps][32];
   __shared__ float den_w[kCombineWarps], max_w[kCombineWarps];
   const int row = blockIdx.x / kCombineParts;
@@ -88,8 +90,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
 constexpr int kRowSplitsMax = 64;  // above this the wide kernel is used
 template <int kRowChunk>
 __global__ void __launch_bounds__(kD) combine_rows_kernel(const CombineParams p) {
+  // MG_OVERLAP_NEXT: the next kernel may begin at once
+  if (p.overlap) pdl_launch_dependents();
   pdl_wait();  // the partials come from the previous kernel
-  pdl_launch_dependents();
+  if (!p.overlap) pdl_launch_dependents();
   const int row = blockIdx.x, d = threadIdx.x;
   const int S = p.splits;
   const float *lse = p.part_lse + static_cast<size_t>(row) * S;

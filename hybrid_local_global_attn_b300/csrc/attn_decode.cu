@@ -64,6 +64,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const uint32_t bar_full = smem_u32(bars);
   const uint32_t bar_empty = bar_full + 8 * NS;
 
+  // MG_OVERLAP_NEXT with a single split (this kernel writes o itself, no
+  // combine follows): the next kernel may begin at once
+  const bool release_now = p.overlap != 0 && p.splits == 1;
+  if (release_now) pdl_launch_dependents();
   // Prologue that touches no memory written by earlier kernels: it overlaps
   // the previous kernel's tail under programmatic dependent launch.
   if (threadIdx.x == 0) {
@@ -96,14 +100,14 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     }
   }
   __syncthreads();
-  // Early start (caller's promise that the kernel before this one writes
-  // neither the cache nor the positions): the position is read and the
-  // first stages are issued before the dependency wait; everything that
-  // kernel may produce (q, the new row) and every write come after it.
+  // Early start (caller's promise that no kernel still running writes the
+  // cache or the positions): the position is read and the first stages are
+  // issued before the dependency wait; everything an earlier kernel may
+  // produce (q, the new row) and every write come after it.
   const bool early = p.early != 0;
   if (!early) {
     pdl_wait();
-    pdl_launch_dependents();
+    if (!release_now) pdl_launch_dependents();
   }
 
   const int32_t pq = p.pos[b];
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   }
   if (early) {
     pdl_wait();
-    pdl_launch_dependents();
+    if (!release_now) pdl_launch_dependents();
   }
   if (bad && split == 0 && threadIdx.x == 0) set_err(p.err, MG_DERR_POSITION);
   // this CTA's partial of row r: o already divided by its softmax sum, and lse

@@ -24,10 +24,13 @@
 //    the CTA computes once the position is known; the key in the query's own
 //    slot (d = 0) enters unrotated.
 //  * Early start (MG_EARLY_START, batch 1): when the caller
-//    promises that the previous kernel writes neither the ring nor the
+//    promises that no kernel still running writes the ring or the
 //    positions, the position, the tiles, R(-b) and the rotated key
 //    fragments are all ready before the dependency wait; the query and the
 //    new row are read after it, the new key entering the fragments as is.
+//    With MG_OVERLAP_NEXT the kernel lets the next one begin at once, so
+//    that in a chain of such calls each layer's part before the wait runs
+//    under the layers before it.
 //  * Precision: the rotated key k' is kept as two bf16 values, hi = bf16(k')
 //    and lo = bf16(k' - hi), and Q.K^T accumulates q.hi + q.lo (two
 //    mma.sync m16n8k16 per fragment, fp32 accumulate).  The score then
@@ -230,13 +233,19 @@ __global__ void __launch_bounds__(kLocThreads, 1)
     return w;
   };
 
-  // Early start (single-round kernel, caller's promise that the kernel
-  // before this one writes neither the ring nor the positions): the
-  // position, the ring tiles, the R(-b) table and the rotated keys are all
-  // prepared before the dependency wait; only the query and the new row --
-  // which that kernel may produce -- are read after it.
-  bool early = false;
-  if constexpr (kRounds == 1) early = p.early != 0;
+  // Early start (single-round kernel, caller's promise that no kernel still
+  // running writes the ring or the positions): the position, the ring
+  // tiles, the R(-b) table and the rotated keys are all prepared before the
+  // dependency wait; only the query and the new row -- which an earlier
+  // kernel may produce -- are read after it.
+  bool early = false, overlap = false;
+  if constexpr (kRounds == 1) {
+    early = p.early != 0;
+    overlap = p.overlap != 0;
+  }
+  // MG_OVERLAP_NEXT: the next kernel may begin at once, its part before the
+  // dependency wait then running under this whole kernel
+  if (overlap) pdl_launch_dependents();
 
   // ---- prologue: reads only kernel parameters (and, with the early start,
   // the ring), so it overlaps the previous kernel under programmatic
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(kLocThreads, 1)
   cluster_arrive_relaxed();
   if (!early) {
     pdl_wait();
-    pdl_launch_dependents();
+    if (!overlap) pdl_launch_dependents();
   }
 
   // The position is loaded first, but nothing below waits for it until the
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(kLocThreads, 1)
       }
     }
     pdl_wait();
-    pdl_launch_dependents();
+    if (!overlap) pdl_launch_dependents();
     load_query();
   }
   if (bad && my_rank == 0 && g == 0 && tid == 0) set_err(p.err, MG_DERR_POSITION);
@@ -750,7 +759,7 @@ cudaError_t launch_local_attn(LocalParams p, const CUtensorMap &tk, const CUtens
   // beside the previous kernel's (two sets of 16-CTA clusters in 7 GPCs):
   // otherwise the late clusters would read the query after their keys
   // instead of beside them.
-  if (pairs > 3) p.early = 0;
+  if (pairs > 3) p.early = p.overlap = 0;
   if (pairs <= 7) return launch_local_rounds<1>(p, tk, tv, s, 2);
   if (pairs <= 15) return launch_local_rounds<2>(p, tk, tv, s, 7);
   return launch_local_rounds<4>(p, tk, tv, s, 8);

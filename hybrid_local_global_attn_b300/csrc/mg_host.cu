@@ -354,7 +354,8 @@ cudaError_t launch_local(const mg_layer *layer, const mg_cache *cache, const int
                          int32_t n, int32_t max_len, const void *q, const void *k_new,
                          const void *v_new, bool write_new, void *o, uint32_t *d_err,
                          const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s,
-                         bool early = false, float *x_rows = nullptr, float *x_lse = nullptr) {
+                         bool early = false, float *x_rows = nullptr, float *x_lse = nullptr,
+                         bool overlap = false) {
   LocalParams p;
   p.pos = d_pos;
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -369,6 +370,7 @@ cudaError_t launch_local(const mg_layer *layer, const mg_cache *cache, const int
   p.max_len = max_len;
   p.write_new = write_new ? 1 : 0;
   p.early = early ? 1 : 0;
+  p.overlap = overlap ? 1 : 0;
   p.x_rows = x_rows;
   p.x_lse = x_lse;
   p.scale_log2 = layer->scale * static_cast<float>(M_LOG2E);
@@ -540,7 +542,7 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
                        int32_t max_len, const void *q, const void *k_new, const void *v_new,
                        void *o, void *ws, size_t ws_bytes, uint32_t *d_err, void *stream,
                        uint64_t wait_ns = kWaitLimitNs, int32_t stall_tile = -1,
-                       bool early = false) {
+                       bool early = false, bool overlap = false) {
   int st = check_layer(layer);
   if (st != MG_OK) return st;
   if ((st = check_cache(layer, cache)) != MG_OK) return st;
@@ -574,7 +576,8 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (layer->kind == MG_LOCAL)
     return launch_status(launch_local(layer, cache, d_pos, 1, max_len, q, k_new, v_new,
-                                      k_new != nullptr, o, d_err, tk, tv, s, early));
+                                      k_new != nullptr, o, d_err, tk, tv, s, early, nullptr,
+                                      nullptr, overlap));
   DecodeParams p;
   p.pos = d_pos;
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -600,6 +603,7 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   p.wait_ns = wait_ns;
   p.stall_tile = stall_tile;
   p.early = early && !e4m3 ? 1 : 0;
+  p.overlap = overlap && !e4m3 && p.map.table == nullptr ? 1 : 0;
   cudaError_t e = e4m3 ? launch_decode_e4m3(p, tk, tv, s) : launch_decode(p, tk, tv, s);
   if (e != cudaSuccess) return MG_ERR_CUDA;
   if (!split) return MG_OK;
@@ -609,6 +613,7 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   c.o = static_cast<__nv_bfloat16 *>(o);
   c.rows = cache->batch * kHq;
   c.splits = w.splits;
+  c.overlap = p.overlap;
   return launch_status(launch_combine(c, s));
 }
 
@@ -697,9 +702,10 @@ int mg_append_decode_ex(const mg_layer *layer, const mg_cache *cache, const int3
                         void *o, void *ws, size_t ws_bytes, uint32_t *d_err, uint32_t flags,
                         void *stream) {
   if (k_new == nullptr || v_new == nullptr) return MG_ERR_INVALID;
-  if ((flags & ~MG_EARLY_START) != 0) return MG_ERR_INVALID;
+  if ((flags & ~(MG_EARLY_START | MG_OVERLAP_NEXT)) != 0) return MG_ERR_INVALID;
   return decode_impl(layer, cache, d_pos, max_len, q, k_new, v_new, o, ws, ws_bytes, d_err,
-                     stream, kWaitLimitNs, -1, (flags & MG_EARLY_START) != 0);
+                     stream, kWaitLimitNs, -1, (flags & MG_EARLY_START) != 0,
+                     (flags & MG_OVERLAP_NEXT) != 0);
 }
 
 }  // extern "C"
@@ -823,6 +829,7 @@ int block_attention(int32_t op, const mg_layer *layer, const mg_cache *cache,
     c.o = p.o;
     c.rows = B * n * kHq;
     c.splits = w.splits;
+    c.overlap = 0;
     return launch_status(launch_combine(c, s));
   }
   return MG_OK;

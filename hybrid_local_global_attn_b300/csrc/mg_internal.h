@@ -164,6 +164,7 @@ struct DecodeParams {  // global layers
   uint64_t wait_ns;
   int32_t stall_tile;
   int32_t early;  // 1: position and the first tiles read before the dependency wait
+  int32_t overlap;  // 1: with a single split, let the next kernel start at once
 };
 
 
@@ -180,6 +181,7 @@ struct LocalParams {  // local layers, n <= kMaxLocalTokens query tokens
   int32_t batch, n, max_len;
   int32_t write_new;   // 1: also store the block rows into the ring (fused append, n == 1)
   int32_t early;       // 1: position and ring read before the dependency wait (decode, n == 1)
+  int32_t overlap;     // 1: let the next kernel start at once (decode, n == 1)
   // local verify (n >= 2): the clusters' exchange buffers in the workspace,
   // rows [cluster][16 heads][cluster size][8 tokens][128] and lse [.][.][.][8]
   float *x_rows, *x_lse;
@@ -193,6 +195,7 @@ struct CombineParams {
   const float *part_lse;  // [rows][splits]
   __nv_bfloat16 *o;       // [rows][128]
   int32_t rows, splits;
+  int32_t overlap;        // 1: let the next kernel start at once
 };
 
 struct StageParams {

@@ -299,6 +299,7 @@ def mg_append_decode(layer, cache: KVCache, pos, max_len, q, k_new, v_new, o, ws
 
 
 EARLY_START = 1  # MG_EARLY_START
+OVERLAP_NEXT = 2  # MG_OVERLAP_NEXT
 
 
 def mg_append_decode_ex(layer, cache: KVCache, pos, max_len, q, k_new, v_new, o, ws, err, flags,

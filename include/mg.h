@@ -274,27 +274,40 @@ int mg_append_decode(const mg_layer *layer, const mg_cache *cache,
                      size_t ws_bytes, uint32_t *d_err, void *stream);
 
 /* flags of mg_append_decode_ex */
-#define MG_EARLY_START 1u /* the previous kernel writes neither the cache nor d_pos */
+#define MG_EARLY_START 1u  /* kernels still running write neither the cache nor d_pos */
+#define MG_OVERLAP_NEXT 2u /* the next kernel on the stream may begin at once */
 
 /*
  * mg_append_decode with flags; flags == 0 is mg_append_decode itself (any
- * other bit: MG_ERR_INVALID).
+ * other bit: MG_ERR_INVALID).  Both flags apply to a local layer with a
+ * batch of one sequence (where this call's clusters fit on the GPU beside
+ * the previous call's) and to a bf16 global layer on a linear cache (any
+ * batch); other cases ignore them.
  *
- * MG_EARLY_START: the caller promises that the kernel enqueued on `stream`
- * just before this call writes neither this layer's cache nor d_pos -- it
- * may produce q, k_new and v_new, as a projection that leaves the cache to
- * the fused append does, or be another layer's attention.  The decode
- * kernels then read the position and start their cache loads before their
- * programmatic-dependent-launch wait, so that these overlap the previous
- * kernel's tail: a local layer also rotates its ring keys there, a global
- * layer issues its first pipeline stages.  q, k_new and v_new are read, and
- * everything is written, after the wait.  The results equal
- * mg_append_decode's bit for bit when the promise holds; when it does not,
- * they may be wrong (stale cache rows or position) but no access leaves
- * the cache or the buffers passed.  Local layers use it for a batch of one
- * sequence (where this call's clusters fit on the GPU beside the previous
- * call's), bf16 global layers on a linear cache for any batch; other cases
- * ignore the flag.
+ * MG_EARLY_START: the caller promises that no kernel that may still be
+ * running when this call's kernels start writes this layer's cache or
+ * d_pos.  Those kernels are the one enqueued on `stream` just before this
+ * call and, when that kernel came from a call with MG_OVERLAP_NEXT, also
+ * every kernel that may still have been running when that call started
+ * (and so on back).  With the flag the decode kernels read the position and
+ * start their cache loads before their programmatic-dependent-launch wait:
+ * a local layer also rotates its ring keys there, a global layer issues its
+ * first pipeline stages.  q, k_new and v_new are read, and everything is
+ * written, after the wait, so the kernel before may produce them (a
+ * projection that leaves the append to this call) or be another layer's
+ * attention.  The results equal mg_append_decode's bit for bit when the
+ * promise holds; when it does not, they may be wrong (stale cache rows or
+ * position) but no access leaves the cache or the buffers passed.
+ *
+ * MG_OVERLAP_NEXT: this call's last kernel lets the next kernel on `stream`
+ * begin at once rather than after its own dependency wait, so that a chain
+ * of MG_EARLY_START calls -- the layers of one decode step -- runs each
+ * call's loads under the calls before it.  A next kernel that waits before
+ * reading anything (a plain call of this library, or any kernel that is not
+ * this library's) sees no difference.  A chain must not contain a call that
+ * depends on an append of an earlier call of the same chain: decode steps
+ * in a row need a kernel without the flag between them (a position update,
+ * the next step's projections).
  */
 int mg_append_decode_ex(const mg_layer *layer, const mg_cache *cache,
                         const int32_t *d_pos, int32_t max_len, const void *q,

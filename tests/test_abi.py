@@ -157,12 +157,14 @@ def test_host_side_rejections_launch_nothing(mg):
                                   fake, None) in (1, 2)
     # mg_append_decode_ex: unknown flag bits, and the checks of mg_append_decode
     gc = mg.mg_cache(0x10000, 0x20000, 1, 1000)
-    assert lib.mg_append_decode_ex(by(G), by(gc), fake, 1000, fake, fake, fake, fake, fake, 1 << 30,
-                                   fake, 2, None) == 1
-    assert lib.mg_append_decode_ex(by(G), by(gc), fake, 1001, fake, fake, fake, fake, fake, 1 << 30,
-                                   fake, mg.EARLY_START, None) == 3
-    assert lib.mg_append_decode_ex(by(G), by(gc), fake, 1000, fake, None, fake, fake, fake, 1 << 30,
-                                   fake, mg.EARLY_START, None) == 1
+    for unknown in (4, 8 | mg.EARLY_START, 1 << 31):
+        assert lib.mg_append_decode_ex(by(G), by(gc), fake, 1000, fake, fake, fake, fake, fake,
+                                       1 << 30, fake, unknown, None) == 1
+    for flags in (mg.EARLY_START, mg.OVERLAP_NEXT, mg.EARLY_START | mg.OVERLAP_NEXT):
+        assert lib.mg_append_decode_ex(by(G), by(gc), fake, 1001, fake, fake, fake, fake, fake,
+                                       1 << 30, fake, flags, None) == 3
+        assert lib.mg_append_decode_ex(by(G), by(gc), fake, 1000, fake, None, fake, fake, fake,
+                                       1 << 30, fake, flags, None) == 1
     # global decode past capacity
     assert lib.mg_attn_decode(by(G), by(gc), fake, 1001, fake, fake, fake, 1 << 30, fake, None) == 3
     # workspace too small

@@ -353,6 +353,77 @@ def test_append_decode_early_matches_plain(mg, bases):
                 compare(ob[i, li, b], ref, f"layer kind {L['kind']} step {i} seq {b}")
 
 
+@pytest.mark.parametrize("bases", [[2040], [100], [2040, 3000, 4090]])
+def test_append_decode_overlap_chain_matches_plain(mg, bases):
+    """MG_EARLY_START | MG_OVERLAP_NEXT on every call of a step of three local
+    layers and one global layer, as a model's decode step orders them, for
+    12 steps in one CUDA graph; a torch kernel between steps (the position
+    update of a real loop) ends each chain, since a layer's next step reads
+    the row this step appends.  Inside a step each call's loads run under
+    the calls before it (at batch 1; larger batches ignore the flags for the
+    local layers).  Outputs and caches equal the plain mg_append_decode run
+    bit for bit, and sampled steps match the oracle."""
+    B = len(bases)
+    S = 12
+    T = max(bases) + S
+    kinds = (0, 0, 0, 1)
+    layers = []
+    for li, kind in enumerate(kinds):
+        k, v = synth.history(B, T, 31, 10 + li)
+        q = synth.queries(B, S, 31, 10 + li)
+        layers.append(dict(kind=kind, k=k, v=v, q=q, kd=k.cuda(), qd=q.cuda(), vd=v.cuda(),
+                           lay=mg.make_layer(kind), ws=mg.workspace(mg.OP_DECODE, mg.make_layer(kind), B, 1, T),
+                           fill=fill_for_decode(mg, kind, k[:, :max(bases)], v[:, :max(bases)],
+                                                [p - 1 for p in bases], T)))
+    pos_all = torch.tensor([[p + i for p in bases] for i in range(S)], dtype=torch.int32, device="cuda")
+    kn_all = [torch.stack([torch.stack([L["kd"][b, p + i] for b, p in enumerate(bases)])[:, None]
+                           for i in range(S)]).contiguous() for L in layers]
+    vn_all = [torch.stack([torch.stack([L["vd"][b, p + i] for b, p in enumerate(bases)])[:, None]
+                           for i in range(S)]).contiguous() for L in layers]
+    q_all = [L["qd"].transpose(0, 1).contiguous() for L in layers]  # [S][B][32][128]
+
+    def run(flags):
+        caches = []
+        for L in layers:
+            c = mg.KVCache(L["kind"], B, T)
+            c.k.copy_(L["fill"].k)
+            c.v.copy_(L["fill"].v)
+            caches.append(c)
+        outs = torch.zeros((S, len(layers), B, 32, 128), dtype=torch.bfloat16, device="cuda")
+        steps_done = torch.zeros(1, dtype=torch.int32, device="cuda")
+        err = mg.error_word()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(S):
+                for li, L in enumerate(layers):
+                    args = (L["lay"], caches[li], pos_all[i], T, q_all[li][i], kn_all[li][i], vn_all[li][i],
+                            outs[i, li], L["ws"], err)
+                    if flags:
+                        mg.mg_append_decode_ex(*args, flags)
+                    else:
+                        mg.mg_append_decode(*args)
+                steps_done.add_(1)  # a kernel without the flags between steps
+        g.replay()
+        torch.cuda.synchronize()
+        check_err(err)
+        assert int(steps_done.item()) == S
+        return outs, caches
+
+    oa, ca = run(0)
+    ob, cb = run(mg.EARLY_START | mg.OVERLAP_NEXT)
+    assert torch.equal(oa, ob), "overlapped decode differs from the plain calls"
+    for x, y in zip(ca, cb):
+        assert torch.equal(x.k, y.k) and torch.equal(x.v, y.v), "caches differ"
+    for li, L in enumerate(layers):
+        olay = orc.layer(oracle_kind(L["kind"]))
+        for i in (0, S - 1):
+            for b, p in enumerate(bases):
+                ref = orc.attention(olay, L["k"][b, :p + i + 1], L["v"][b, :p + i + 1], [p + i],
+                                    L["q"][b, i:i + 1])[0]
+                compare(ob[i, li, b], ref, f"layer {li} kind {L['kind']} step {i} seq {b}")
+
+
 def test_append_decode_early_broken_promise_stays_in_bounds(mg):
     """MG_EARLY_START right after a kernel that does write the cache (the
     promise broken on purpose, both layer kinds, batch 1):
