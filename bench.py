@@ -664,8 +664,9 @@ def leg_e4m3(wl, steps=16):
     """Global layers from FP8 (e4m3) caches: each of the 13 global caches is
     quantised into its own FP8 cache (per-head scales 1.0: N(0,1) data sits
     well inside the e4m3 range), then (a) the 13 global decodes from one
-    graph and (b) the whole 52-layer decode step with the global layers on
-    FP8, beside the same graphs on the bf16 caches."""
+    graph, (b) the whole 52-layer decode step with the global layers on
+    FP8, beside the same graphs on the bf16 caches, and (c) that step with
+    the decode leg's calls (fused append, the step flags)."""
     import torch
     mg, dev, err = wl.mg, wl.dev, wl.err
     glob = [l for l in range(N_LAYERS) if wl.kinds[l] == mg.GLOBAL]
@@ -701,6 +702,19 @@ def leg_e4m3(wl, steps=16):
                                                   ws[l], err) for l in range(N_LAYERS)])
         res[f"step_us_{name}"] = us
         res[f"tokens_per_s_{name}"] = 1e6 / us
+    # (c) the step as the decode leg makes its calls: each layer appends the
+    # token's own K/V (position PROMPT) and passes MG_EARLY_START |
+    # MG_OVERLAP_NEXT (FP8 global layers honour the second flag only)
+    kn = torch.randn((N_LAYERS, 1, 1, 2, 128), device=dev).to(torch.bfloat16)
+    vn = torch.randn_like(kn)
+    pos_n = torch.tensor([PROMPT], dtype=torch.int32, device=dev)
+    ws_n = [mg.workspace(mg.OP_DECODE, wl.layers[l], 1, 1, PROMPT + 1, device=dev) for l in range(N_LAYERS)]
+    for name in ("bf16", "e4m3"):
+        caches = [e4[l] if (name == "e4m3" and l in e4) else wl.caches[l] for l in range(N_LAYERS)]
+        us = _graph_us(lambda: [append_decode(step_flags(), wl.layers[l], caches[l], pos_n, PROMPT + 1, q[l],
+                                              kn[l], vn[l], o[l], ws_n[l], err) for l in range(N_LAYERS)])
+        res[f"step_us_fused_overlap_{name}"] = us
+        res[f"tokens_per_s_fused_overlap_{name}"] = 1e6 / us
     torch.cuda.synchronize()
     assert int(err.item()) == 0, f"device error word {int(err.item()):#x} after the e4m3 leg"
     del e4

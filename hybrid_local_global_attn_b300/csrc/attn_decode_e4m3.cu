@@ -102,6 +102,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const int32_t vtiles = p.slots / kVT;  // transposed V tiles per (sequence, head)
   const int32_t c2 = b * kHkv + g;
 
+  // MG_OVERLAP_NEXT with a single split (this kernel writes o itself, no
+  // combine follows): the next kernel may begin at once
+  const bool release_now = p.overlap != 0 && p.splits == 1;
+  if (release_now) pdl_launch_dependents();
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < NS; ++i) {
@@ -125,7 +129,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   }
   __syncthreads();
   pdl_wait();
-  pdl_launch_dependents();
+  if (!release_now) pdl_launch_dependents();
 
   const int32_t pq = p.pos[b];
   const bool bad = pq < 0 || pq >= p.max_len || pq >= p.slots;

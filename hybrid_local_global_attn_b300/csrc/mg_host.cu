@@ -603,7 +603,7 @@ static int decode_impl(const mg_layer *layer, const mg_cache *cache, const int32
   p.wait_ns = wait_ns;
   p.stall_tile = stall_tile;
   p.early = early && !e4m3 ? 1 : 0;
-  p.overlap = overlap && !e4m3 && p.map.table == nullptr ? 1 : 0;
+  p.overlap = overlap && p.map.table == nullptr ? 1 : 0;
   cudaError_t e = e4m3 ? launch_decode_e4m3(p, tk, tv, s) : launch_decode(p, tk, tv, s);
   if (e != cudaSuccess) return MG_ERR_CUDA;
   if (!split) return MG_OK;

@@ -282,7 +282,8 @@ int mg_append_decode(const mg_layer *layer, const mg_cache *cache,
  * other bit: MG_ERR_INVALID).  Both flags apply to a local layer with a
  * batch of one sequence (where this call's clusters fit on the GPU beside
  * the previous call's) and to a bf16 global layer on a linear cache (any
- * batch); other cases ignore them.
+ * batch); MG_OVERLAP_NEXT also to a global layer on an FP8 cache.  Other
+ * cases ignore them.
  *
  * MG_EARLY_START: the caller promises that no kernel that may still be
  * running when this call's kernels start writes this layer's cache or
