@@ -38,6 +38,17 @@ def test_library_exports_every_declared_symbol(mg):
         assert ctypes.cast(getattr(mg.lib, n), ctypes.c_void_p).value
 
 
+def test_binding_constants_match_header(mg):
+    """The binding's flag, kind and op constants equal the header's #defines
+    (a mismatch would pass the wrong bits through the C ABI)."""
+    text = open(HEADER).read()
+    defines = {k: int(v.rstrip("uU"), 0) for k, v in
+               re.findall(r"#define\s+(MG_\w+)\s+(0x[0-9a-fA-F]+[uU]?|\d+[uU]?)\b", text)}
+    assert defines["MG_EARLY_START"] == mg.EARLY_START == 1
+    assert defines["MG_OVERLAP_NEXT"] == mg.OVERLAP_NEXT == 2
+    assert mg.EARLY_START & mg.OVERLAP_NEXT == 0
+
+
 def test_byte_model_matches_pages(mg, golden_bytes):
     gb = golden_bytes
     per_tok = mg.mg_cache_bytes(mg.GLOBAL, 1, 1)
